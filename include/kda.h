@@ -1,0 +1,218 @@
+/*
+ * kda.h -- C ABI of libkda: the Kimi Delta Attention (KDA) RecoverSSM
+ * speculative verify and accepted-state commit on one GB300 (sm_103a).
+ *
+ * Operations (vLLM pages on the Kimi-K3 RecoverSSM path):
+ *   kda_verify  "vllm.models.kimi_k3.nvidia.recoverssm.kernels",
+ *               CuteRecoverSSMVerify.__call__: the short causal conv + SiLU
+ *               fused in front of the verify of
+ *               "vLLM/vllm/models/kimi_k3/nvidia/ops/recoverssm.py",
+ *               kda_recoverssm_verify / _kda_recoverssm_verify_kernel
+ *               (gate _kda_gate, step _kda_recurrent_step).
+ *   kda_commit  same ops page, KDARecoverSSMCommitContext.commit /
+ *               _commit_kda_state_kernel, and the kernels page,
+ *               cute_recoverssm_commit: all layers folded in one launch.
+ *
+ * Conventions for every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates nothing, keeps no pointer past the call, and never
+ *     synchronises (kda_read_device_error is the one exception).
+ *   - Kernels are enqueued on `stream` and run asynchronously, in stream order.
+ *   - Strides are in ELEMENTS of the buffer's own type.  Innermost dimensions
+ *     are contiguous (unit stride) as stated per field.
+ *   - A non-zero status means nothing was enqueued; kda_last_error() then
+ *     describes the cause (thread-local, valid until the next call).
+ *   - Errors that only the device can see (a slot or record row out of range,
+ *     a decreasing query_start_loc, a token range past T) skip the affected
+ *     (request, head) work item and OR a KDA_DEVERR_* bit into workspace[0];
+ *     kda_read_device_error() fetches it.  workspace may be NULL (no report).
+ *   - No device wait is unbounded: a wait that exceeds about one second sets
+ *     KDA_DEVERR_TIMEOUT and the work item returns.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* a null pointer, a bad size, stride or enum */
+    KDA_ERR_UNSUPPORTED = 2,  /* a valid configuration this build does not serve */
+    KDA_ERR_MISALIGNED = 3,   /* a static tensor off its required alignment */
+    KDA_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+    KDA_ERR_DEVICE = 5        /* kda_read_device_error: the device reported errors */
+} kda_status;
+
+typedef enum kda_gate_mode {
+    KDA_GATE_SOFTPLUS = 0,    /* g = -exp(A_log) * softplus(raw_g + dt_bias) */
+    KDA_GATE_LOWER_BOUND = 1  /* g = lower_bound * sigmoid(exp(A_log) * (raw_g + dt_bias)) */
+} kda_gate_mode;
+
+typedef enum kda_conv_layout {
+    KDA_CONV_DIM_FIRST = 0,   /* conv state [slots, 3HK, Q+W-2], taps contiguous     */
+    KDA_CONV_SEQ_FIRST = 1    /* conv state [slots, Q+W-2, 3HK], channels contiguous */
+} kda_conv_layout;
+
+typedef enum kda_dtype { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP32 = 1 } kda_dtype;
+
+/* Device error bits (workspace[0]). */
+enum {
+    KDA_DEVERR_SLOT_RANGE = 1,  /* state_indices[b] >= num_slots                     */
+    KDA_DEVERR_ROW_RANGE = 2,   /* record row < 0 or >= num_record_rows              */
+    KDA_DEVERR_TOKEN_RANGE = 4, /* query_start_loc decreasing, negative, or past T   */
+    KDA_DEVERR_TIMEOUT = 8,     /* a bounded device wait gave up                     */
+    KDA_DEVERR_MISALIGNED = 16  /* a per-layer table entry off 16-byte alignment     */
+};
+
+/*
+ * kda_verify -- verify one KDA layer's speculative windows without touching
+ * the checkpointed SSM state.
+ *
+ * For request b: tokens are rows [bos, bos + n) of the activation buffers,
+ * bos = query_start_loc[b], n = min(query_start_loc[b+1] - bos, Q); slot
+ * s = state_indices[b]; record row r = record_indices ? record_indices[b] : s.
+ * If s <= null_block_id the request writes zeros to out[bos .. bos+n) (its
+ * heads' columns) and nothing else.  Otherwise, per head h:
+ *   1. conv: for each of the head's q, k and v channels c (channel blocks
+ *      [0,HK) q, [HK,2HK) k, [2HK,3HK) v; head h owns c = blk*HK + h*K + i),
+ *      history = the W-1 stored taps starting at tap a-1 of slot s, where
+ *      a = clamp(num_accepted_prev[b], 1, Q) (a = 1 when the pointer is NULL);
+ *      seq = history followed by mixed_qkv[bos..bos+n, c];
+ *      y_t = bf16_rne(silu(sum_j w[c,j] * seq[t+j])), w[c,W-1] on the newest
+ *      input, rounded from the exact sum (a result the device cannot round
+ *      with certainty in fp32 is recomputed in fp64);
+ *      the slot then stores seq[1 .. W-2+n] at taps 0 .. W-3+n (in place;
+ *      later taps are left as they were).
+ *   2. q^ = q * rsqrt(|q|^2 + 1e-6) * K^-1/2, k^ = k * rsqrt(|k|^2 + 1e-6),
+ *      beta = sigmoid(raw_beta), g per the gate mode (A = exp(A_log[h])).
+ *   3. from S = state[s, h] (read only): per token t < n,
+ *      S <- S diag(e^g); c = beta (v - S k^); S <- S + c k^T; o = S q^.
+ *      out[bos+t, h*V .. h*V+V) = bf16_rne(o); corr[r, h, t, :] = c (fp32);
+ *      key_gate[r, h, t, 0..K) = k (the bf16 conv output);
+ *      key_gate[r, h, t, K..2K) = raw_gate[bos+t, h*K ..] (bit copy).
+ *      Rows and records of tokens t >= n are not written.
+ * T == 0 or B == 0 is a no-op returning KDA_OK.
+ *
+ * Supported: K == V in {64, 128}, W == 4, 1 <= Q <= 8.  Alignment: state,
+ * corr, key_gate, conv_state, conv_weight, A_log and dt_bias must start on
+ * 16 bytes, and their slot / row strides must be multiples of 16 bytes
+ * (KDA_ERR_MISALIGNED otherwise).  Activation buffers (mixed_qkv, raw_gate,
+ * raw_beta, out) need only element alignment: rows at any offset are handled
+ * in-kernel.  Distinct requests must use distinct slots and record rows.
+ */
+typedef struct kda_verify_args {
+    int32_t B;                    /* requests                                       */
+    int32_t H, K, V;              /* heads, key dim, value dim (K == V)            */
+    int32_t Q;                    /* window (spec_query_len)                        */
+    int32_t W;                    /* conv width                                     */
+    int32_t T;                    /* token rows in the activation buffers, <= B*Q   */
+    int32_t null_block_id;        /* slot s is null when s <= null_block_id         */
+    int64_t num_slots;            /* slots of the state and conv-state pools        */
+    int64_t num_record_rows;      /* rows of corr / key_gate                        */
+
+    const void *mixed_qkv;  int64_t qkv_row_stride;  /* bf16 [T, 3HK], pre-conv       */
+    const void *raw_gate;   int64_t gate_row_stride; /* bf16 [T, HK]                  */
+    const void *raw_beta;   int64_t beta_row_stride; /* bf16 [T, H]                   */
+    void *out;              int64_t out_row_stride;  /* bf16 [T, HV]                  */
+
+    const float *A_log;           /* fp32 [H]                                       */
+    const float *dt_bias;         /* fp32 [H*K]                                     */
+    int32_t gate_mode;            /* kda_gate_mode                                  */
+    float lower_bound;            /* used by KDA_GATE_LOWER_BOUND                   */
+
+    const void *conv_weight;      /* [3HK, W] contiguous, no bias                   */
+    int32_t conv_weight_dtype;    /* kda_dtype                                      */
+    void *conv_state;             /* bf16, kda_conv_layout, updated in place        */
+    int32_t conv_layout;          /* kda_conv_layout                                */
+    int64_t conv_slot_stride;     /* elements between slots (>= 3HK*(Q+W-2))         */
+
+    const float *state;           /* fp32 [slots, H, V, K], inner (V*K, K, 1); read only */
+    int64_t state_slot_stride;    /* elements between slots (>= H*V*K)              */
+    float *corr;                  /* fp32 [rows, H, Q, V], inner contiguous         */
+    int64_t corr_row_stride;      /* elements between rows (>= H*Q*V)               */
+    void *key_gate;               /* bf16 [rows, H, Q, 2K], inner contiguous        */
+    int64_t kg_row_stride;        /* elements between rows (>= H*Q*2K)              */
+
+    const int32_t *query_start_loc;   /* [B+1]                                      */
+    const int32_t *state_indices;     /* [B]                                        */
+    const int32_t *record_indices;    /* [B] or NULL (records at the state slot)    */
+    const int32_t *num_accepted_prev; /* [B] conv read offset, or NULL (a = 1)      */
+    int32_t *workspace;               /* kda_workspace_bytes() bytes, zeroed, or NULL */
+} kda_verify_args;
+
+/*
+ * kda_commit -- fold each request's first m accepted verify records into its
+ * fp32 state, for all L layers in one launch (in place).
+ *
+ * m = min(max(num_accepted[b], 0), n), n = min(query_start_loc[b+1] -
+ * query_start_loc[b], Q).  Requests with a null slot or m == 0 write nothing.
+ * For layer l, head h, with k^_t and g_t recomputed from the key/gate record
+ * of token t and c_t its correction record:
+ *   S <- S diag(prod_t e^{g_t}) + sum_t c_t (k^_t * prod_{u>t} e^{g_u})^T,
+ * which is the verify's running state after m tokens.
+ *
+ * Per-layer buffers are reached through device tables of L int64 entries:
+ * base addresses and slot / row strides (elements).  Every layer shares the
+ * inner layouts of kda_verify: state [slots, H, V, K] fp32, corr
+ * [rows, H, Q, V] fp32, key_gate [rows, H, Q, 2K] bf16.  Entries must be
+ * 16-byte aligned (checked on the device: KDA_DEVERR_MISALIGNED).
+ * A_log is fp32 [L, H] and dt_bias fp32 [L, H*K], contiguous.
+ * Supported: K == V in {64, 128}, 1 <= Q <= 8, L >= 1.
+ */
+typedef struct kda_commit_args {
+    int32_t L, B, H, K, V, Q;
+    int32_t null_block_id;
+    int64_t num_slots, num_record_rows;
+    const int64_t *state_base;        /* device [L]: fp32 state pool addresses     */
+    const int64_t *state_slot_stride; /* device [L]                                */
+    const int64_t *corr_base;         /* device [L]: fp32 correction records       */
+    const int64_t *corr_row_stride;   /* device [L]                                */
+    const int64_t *kg_base;           /* device [L]: bf16 key/gate records         */
+    const int64_t *kg_row_stride;     /* device [L]                                */
+    const float *A_log;               /* fp32 [L, H]                               */
+    const float *dt_bias;             /* fp32 [L, H*K]                             */
+    int32_t gate_mode;
+    float lower_bound;
+    const int32_t *query_start_loc;   /* [B+1] of the verified step                */
+    const int32_t *state_indices;     /* [B]                                       */
+    const int32_t *record_indices;    /* [B] or NULL (records at the state slot)   */
+    const int32_t *num_accepted;      /* [B]                                       */
+    int32_t *workspace;               /* zeroed kda_workspace_bytes(), or NULL     */
+} kda_commit_args;
+
+/* Enqueue the verify of one layer.  Returns before the kernel runs. */
+kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
+
+/* Enqueue the commit of all layers (one kernel launch). */
+kda_status kda_commit(const kda_commit_args *args, kda_stream_t stream);
+
+/* Bytes of device workspace for the error report (int32-aligned, zeroed by
+ * the caller before first use; the library only ORs bits into it). */
+size_t kda_workspace_bytes(void);
+
+/* Synchronise `stream`, copy workspace[0] into *flags, and return KDA_OK if
+ * it is zero, KDA_ERR_DEVICE if not (KDA_ERR_CUDA if the copy failed). */
+kda_status kda_read_device_error(const int32_t *workspace, kda_stream_t stream, int32_t *flags);
+
+/* Description of the last non-OK status returned on this thread. */
+const char *kda_last_error(void);
+
+/* ABI version of this header (bumped on any layout change). */
+int32_t kda_abi_version(void);
+
+#define KDA_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,185 @@
+// kda_api.cpp -- the C ABI of libkda: host-side validation of every argument
+// the host can check, launch-parameter marshalling, dispatch to the sm_103a
+// kernels, and the error report.  The checks mirror the ValueErrors of
+// "vLLM/vllm/models/kimi_k3/nvidia/ops/recoverssm.py" (kda_recoverssm_verify,
+// KDARecoverSSMCommitContext.create / .commit) and the layout / support rules
+// of "vllm.models.kimi_k3.nvidia.recoverssm.kernels" (_check_layouts,
+// can_use_cute_recoverssm), as status codes instead of exceptions.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "kda.h"
+#include "kda_params.h"
+
+namespace kda {
+cudaError_t launch_verify(const VerifyParams& p, int K, cudaStream_t stream);
+cudaError_t launch_commit(const CommitParams& p, int K, cudaStream_t stream);
+}  // namespace kda
+
+namespace {
+
+thread_local char g_error[512] = "no error";
+
+kda_status fail(kda_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_error, sizeof g_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+constexpr int kMaxWindow = 8;
+constexpr int kConvWidth = 4;
+
+kda_status check_dims(int H, int K, int V, int Q) {
+  if (H <= 0 || K <= 0 || V <= 0 || Q <= 0)
+    return fail(KDA_ERR_INVALID_ARG, "H, K, V and Q must be positive (H=%d K=%d V=%d Q=%d)", H, K, V, Q);
+  if (K != V) return fail(KDA_ERR_UNSUPPORTED, "K (%d) must equal V (%d)", K, V);
+  if (K != 64 && K != 128) return fail(KDA_ERR_UNSUPPORTED, "head dim %d: supported 64 and 128", K);
+  if (Q > kMaxWindow) return fail(KDA_ERR_UNSUPPORTED, "window %d: supported 1 to %d tokens", Q, kMaxWindow);
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+size_t kda_workspace_bytes(void) { return 16; }
+
+const char* kda_last_error(void) { return g_error; }
+
+kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
+  if (a == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify: args is NULL");
+  if (a->B < 0 || a->T < 0) return fail(KDA_ERR_INVALID_ARG, "kda_verify: negative B (%d) or T (%d)", a->B, a->T);
+  kda_status st = check_dims(a->H, a->K, a->V, a->Q);
+  if (st != KDA_OK) return st;
+  if (a->W != kConvWidth) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: conv width %d, supported %d", a->W, kConvWidth);
+  if ((long long)a->T > (long long)a->B * a->Q)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: %d token rows exceed B*Q = %lld", a->T, (long long)a->B * a->Q);
+  if (a->B == 0 || a->T == 0) return KDA_OK;
+  const void* required[] = {a->mixed_qkv, a->raw_gate,  a->raw_beta, a->out,   a->A_log,
+                            a->dt_bias,   a->conv_weight, a->conv_state, a->state, a->corr,
+                            a->key_gate,  a->query_start_loc, a->state_indices};
+  for (const void* ptr : required)
+    if (ptr == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify: a required pointer is NULL");
+  if (a->gate_mode != KDA_GATE_SOFTPLUS && a->gate_mode != KDA_GATE_LOWER_BOUND)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: gate_mode %d", a->gate_mode);
+  if (a->gate_mode == KDA_GATE_LOWER_BOUND && !std::isfinite(a->lower_bound))
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: lower_bound is not finite");
+  if (a->conv_layout != KDA_CONV_DIM_FIRST && a->conv_layout != KDA_CONV_SEQ_FIRST)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: conv_layout %d", a->conv_layout);
+  if (a->conv_weight_dtype != KDA_DTYPE_BF16 && a->conv_weight_dtype != KDA_DTYPE_FP32)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: conv_weight_dtype %d", a->conv_weight_dtype);
+  if (a->num_slots <= 0 || a->num_record_rows <= 0)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: num_slots and num_record_rows must be positive");
+  const long long H = a->H, K = a->K, V = a->V, Q = a->Q;
+  const long long conv_len = Q + kConvWidth - 2;
+  if (a->qkv_row_stride < 3 * H * K || a->gate_row_stride < H * K || a->beta_row_stride < H ||
+      a->out_row_stride < H * V)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: an activation row stride is shorter than its row");
+  if (a->conv_slot_stride < 3 * H * K * conv_len)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: conv_slot_stride %lld < 3HK*(Q+W-2) = %lld",
+                (long long)a->conv_slot_stride, 3 * H * K * conv_len);
+  if (a->state_slot_stride < H * V * K)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: state_slot_stride %lld < H*V*K", (long long)a->state_slot_stride);
+  if (a->corr_row_stride < H * Q * V || a->kg_row_stride < H * Q * 2 * K)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: a record row stride is shorter than its row");
+  // static tensors: 16-byte aligned starts and slot / row strides
+  if (!aligned(a->state, 16) || (a->state_slot_stride * 4) % 16 || !aligned(a->corr, 16) ||
+      (a->corr_row_stride * 4) % 16 || !aligned(a->key_gate, 16) || (a->kg_row_stride * 2) % 16 ||
+      !aligned(a->conv_state, 16) || (a->conv_slot_stride * 2) % 16 || !aligned(a->conv_weight, 16) ||
+      !aligned(a->A_log, 16) || !aligned(a->dt_bias, 16))
+    return fail(KDA_ERR_MISALIGNED,
+                "kda_verify: state, records, conv state, conv weight and gate parameters must start on "
+                "16-byte boundaries with 16-byte multiple slot / row strides");
+  if (!aligned(a->mixed_qkv, 2) || !aligned(a->raw_gate, 2) || !aligned(a->raw_beta, 2) || !aligned(a->out, 2))
+    return fail(KDA_ERR_MISALIGNED, "kda_verify: bf16 activations must be 2-byte aligned");
+
+  kda::VerifyParams p{};
+  p.B = a->B; p.H = a->H; p.Q = a->Q; p.T = a->T; p.null_block_id = a->null_block_id;
+  p.num_slots = a->num_slots; p.num_record_rows = a->num_record_rows;
+  p.mixed_qkv = static_cast<const uint16_t*>(a->mixed_qkv); p.qkv_stride = a->qkv_row_stride;
+  p.raw_gate = static_cast<const uint16_t*>(a->raw_gate); p.gate_stride = a->gate_row_stride;
+  p.raw_beta = static_cast<const uint16_t*>(a->raw_beta); p.beta_stride = a->beta_row_stride;
+  p.out = static_cast<uint16_t*>(a->out); p.out_stride = a->out_row_stride;
+  p.A_log = a->A_log; p.dt_bias = a->dt_bias;
+  p.lower_bound_gate = a->gate_mode == KDA_GATE_LOWER_BOUND; p.lower_bound = a->lower_bound;
+  p.conv_weight = a->conv_weight; p.conv_weight_fp32 = a->conv_weight_dtype == KDA_DTYPE_FP32;
+  p.conv_state = static_cast<uint16_t*>(a->conv_state); p.conv_dim_first = a->conv_layout == KDA_CONV_DIM_FIRST;
+  p.conv_slot_stride = a->conv_slot_stride;
+  p.state = a->state; p.state_slot_stride = a->state_slot_stride;
+  p.corr = a->corr; p.corr_stride = a->corr_row_stride;
+  p.key_gate = static_cast<uint16_t*>(a->key_gate); p.kg_stride = a->kg_row_stride;
+  p.qsl = a->query_start_loc; p.state_indices = a->state_indices;
+  p.record_indices = a->record_indices; p.num_accepted_prev = a->num_accepted_prev;
+  p.workspace = a->workspace;
+  p.k_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(K)));
+  if ((long long)p.B * p.H > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: B*H too large");
+  cudaError_t e = kda::launch_verify(p, a->K, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify: launch failed: %s", cudaGetErrorString(e));
+  return KDA_OK;
+}
+
+kda_status kda_commit(const kda_commit_args* a, kda_stream_t stream) {
+  if (a == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_commit: args is NULL");
+  if (a->L <= 0) return fail(KDA_ERR_INVALID_ARG, "kda_commit: needs at least one layer (L=%d)", a->L);
+  if (a->B < 0) return fail(KDA_ERR_INVALID_ARG, "kda_commit: negative B (%d)", a->B);
+  kda_status st = check_dims(a->H, a->K, a->V, a->Q);
+  if (st != KDA_OK) return st;
+  if (a->B == 0) return KDA_OK;
+  const void* required[] = {a->state_base, a->state_slot_stride, a->corr_base, a->corr_row_stride,
+                            a->kg_base,    a->kg_row_stride,     a->A_log,     a->dt_bias,
+                            a->query_start_loc, a->state_indices, a->num_accepted};
+  for (const void* ptr : required)
+    if (ptr == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_commit: a required pointer is NULL");
+  if (a->gate_mode != KDA_GATE_SOFTPLUS && a->gate_mode != KDA_GATE_LOWER_BOUND)
+    return fail(KDA_ERR_INVALID_ARG, "kda_commit: gate_mode %d", a->gate_mode);
+  if (a->gate_mode == KDA_GATE_LOWER_BOUND && !std::isfinite(a->lower_bound))
+    return fail(KDA_ERR_INVALID_ARG, "kda_commit: lower_bound is not finite");
+  if (a->num_slots <= 0 || a->num_record_rows <= 0)
+    return fail(KDA_ERR_INVALID_ARG, "kda_commit: num_slots and num_record_rows must be positive");
+  if (!aligned(a->A_log, 4) || !aligned(a->dt_bias, 4))
+    return fail(KDA_ERR_MISALIGNED, "kda_commit: gate parameters must be 4-byte aligned");
+  if ((long long)a->L * a->B * a->H > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "kda_commit: L*B*H too large");
+
+  kda::CommitParams p{};
+  p.L = a->L; p.B = a->B; p.H = a->H; p.Q = a->Q; p.null_block_id = a->null_block_id;
+  p.num_slots = a->num_slots; p.num_record_rows = a->num_record_rows;
+  p.state_base = reinterpret_cast<const long long*>(a->state_base);
+  p.state_stride = reinterpret_cast<const long long*>(a->state_slot_stride);
+  p.corr_base = reinterpret_cast<const long long*>(a->corr_base);
+  p.corr_stride = reinterpret_cast<const long long*>(a->corr_row_stride);
+  p.kg_base = reinterpret_cast<const long long*>(a->kg_base);
+  p.kg_stride = reinterpret_cast<const long long*>(a->kg_row_stride);
+  p.A_log = a->A_log; p.dt_bias = a->dt_bias;
+  p.lower_bound_gate = a->gate_mode == KDA_GATE_LOWER_BOUND; p.lower_bound = a->lower_bound;
+  p.qsl = a->query_start_loc; p.state_indices = a->state_indices;
+  p.record_indices = a->record_indices; p.num_accepted = a->num_accepted;
+  p.workspace = a->workspace;
+  cudaError_t e = kda::launch_commit(p, a->K, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_commit: launch failed: %s", cudaGetErrorString(e));
+  return KDA_OK;
+}
+
+kda_status kda_read_device_error(const int32_t* workspace, kda_stream_t stream, int32_t* flags) {
+  if (workspace == nullptr || flags == nullptr)
+    return fail(KDA_ERR_INVALID_ARG, "kda_read_device_error: NULL workspace or flags");
+  int32_t host = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_read_device_error: %s", cudaGetErrorString(e));
+  *flags = host;
+  if (host != 0) return fail(KDA_ERR_DEVICE, "device reported error bits 0x%x", host);
+  return KDA_OK;
+}
+
+}  // extern "C"

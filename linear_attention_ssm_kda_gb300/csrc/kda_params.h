@@ -1,0 +1,41 @@
+// kda_params.h -- launch parameters of the verify and commit kernels: plain
+// structs of device pointers, built by the host API from the C-ABI arguments.
+#pragma once
+
+#include <stdint.h>
+
+namespace kda {
+
+struct VerifyParams {
+  int B, H, Q, T, null_block_id;
+  long long num_slots, num_record_rows;
+  const uint16_t* mixed_qkv; long long qkv_stride;
+  const uint16_t* raw_gate; long long gate_stride;
+  const uint16_t* raw_beta; long long beta_stride;
+  uint16_t* out; long long out_stride;
+  const float* A_log;
+  const float* dt_bias;
+  int lower_bound_gate; float lower_bound;
+  const void* conv_weight; int conv_weight_fp32;
+  uint16_t* conv_state; int conv_dim_first; long long conv_slot_stride;
+  const float* state; long long state_slot_stride;
+  float* corr; long long corr_stride;
+  uint16_t* key_gate; long long kg_stride;
+  const int* qsl; const int* state_indices; const int* record_indices; const int* num_accepted_prev;
+  int* workspace;
+  float k_scale;  // K^-1/2
+};
+
+struct CommitParams {
+  int L, B, H, Q, null_block_id;
+  long long num_slots, num_record_rows;
+  const long long* state_base; const long long* state_stride;
+  const long long* corr_base; const long long* corr_stride;
+  const long long* kg_base; const long long* kg_stride;
+  const float* A_log; const float* dt_bias;
+  int lower_bound_gate; float lower_bound;
+  const int* qsl; const int* state_indices; const int* record_indices; const int* num_accepted;
+  int* workspace;
+};
+
+}  // namespace kda

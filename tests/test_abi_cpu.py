@@ -1,0 +1,207 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/kda.h declares, its ctypes mirrors match the C struct layouts, and
+host-side validation returns the documented status codes before any CUDA
+call (only fake, never-dereferenced addresses are passed)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+import linear_attention_ssm_kda_gb300 as kda  # noqa: E402
+from linear_attention_ssm_kda_gb300 import _build  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kda.load_library()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w \*]*?\b(kda_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_function(lib):
+    names = _declared_functions()
+    assert {"kda_verify", "kda_commit", "kda_workspace_bytes", "kda_read_device_error",
+            "kda_last_error", "kda_abi_version"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", kda.lib_path()], capture_output=True, text=True)
+    exported = set(re.findall(r"\bT (kda_\w+)", nm.stdout))
+    assert set(names) <= exported
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define KDA_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.kda_abi_version() == int(m.group(1))
+    assert lib.kda_workspace_bytes() >= 8
+
+
+def _c_layout(struct, fields):
+    """sizeof / offsetof of a header struct, from a C program built with gcc."""
+    body = "\n".join(f'  printf("%s %zu\\n", "{f}", offsetof({struct}, {f}));' for f in fields)
+    prog = f"""#include <stdio.h>
+#include <stddef.h>
+#include "kda.h"
+int main(void) {{
+  printf("sizeof %zu\\n", sizeof({struct}));
+{body}
+  return 0;
+}}
+"""
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        open(c, "w").write(prog)
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    return {k: int(v) for k, v in (line.split() for line in out.splitlines())}
+
+
+@pytest.mark.parametrize("cls,cname", [(kda.VerifyArgs, "kda_verify_args"), (kda.CommitArgs, "kda_commit_args")])
+def test_ctypes_mirror_matches_c_layout(cls, cname):
+    fields = [f for f, _ in cls._fields_]
+    c = _c_layout(cname, fields)
+    assert c["sizeof"] == ctypes.sizeof(cls)
+    for f in fields:
+        assert c[f] == getattr(cls, f).offset, f
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced on the host
+
+
+def _valid_verify_args():
+    a = kda.VerifyArgs()
+    H, K, Q = 4, 64, 4
+    a.B, a.H, a.K, a.V, a.Q, a.W, a.T = 2, H, K, K, Q, 4, 5
+    a.null_block_id = 0
+    a.num_slots, a.num_record_rows = 8, 8
+    for name in ("mixed_qkv", "raw_gate", "raw_beta", "out", "A_log", "dt_bias", "conv_weight",
+                 "conv_state", "state", "corr", "key_gate", "query_start_loc", "state_indices"):
+        setattr(a, name, FAKE)
+    a.qkv_row_stride, a.gate_row_stride, a.beta_row_stride, a.out_row_stride = 4 * H * K + 8, 4 * H * K + 8, 4 * H * K + 8, H * K
+    a.conv_slot_stride = 3 * H * K * (Q + 2)
+    a.state_slot_stride = H * K * K
+    a.corr_row_stride = H * Q * K
+    a.kg_row_stride = H * Q * 2 * K
+    return a
+
+
+def _call_verify(lib, a):
+    return lib.kda_verify(ctypes.byref(a), None)
+
+
+def test_verify_rejects_before_launch(lib):
+    assert lib.kda_verify(None, None) == kda.KDA_ERR_INVALID_ARG
+    cases = [
+        (dict(K=96, V=96), kda.KDA_ERR_UNSUPPORTED),
+        (dict(V=128), kda.KDA_ERR_UNSUPPORTED),
+        (dict(Q=9), kda.KDA_ERR_UNSUPPORTED),
+        (dict(W=3), kda.KDA_ERR_UNSUPPORTED),
+        (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(B=-1), kda.KDA_ERR_INVALID_ARG),
+        (dict(T=9), kda.KDA_ERR_INVALID_ARG),          # T > B*Q
+        (dict(state=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(query_start_loc=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(gate_mode=2), kda.KDA_ERR_INVALID_ARG),
+        (dict(conv_layout=5), kda.KDA_ERR_INVALID_ARG),
+        (dict(conv_weight_dtype=3), kda.KDA_ERR_INVALID_ARG),
+        (dict(num_slots=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(qkv_row_stride=10), kda.KDA_ERR_INVALID_ARG),
+        (dict(conv_slot_stride=100), kda.KDA_ERR_INVALID_ARG),
+        (dict(state_slot_stride=100), kda.KDA_ERR_INVALID_ARG),
+        (dict(corr_row_stride=16), kda.KDA_ERR_INVALID_ARG),
+        (dict(state=FAKE + 4), kda.KDA_ERR_MISALIGNED),
+        (dict(state_slot_stride=4 * 64 * 64 + 1), kda.KDA_ERR_MISALIGNED),
+        (dict(key_gate=FAKE + 8), kda.KDA_ERR_MISALIGNED),
+        (dict(conv_state=FAKE + 2), kda.KDA_ERR_MISALIGNED),
+        (dict(out=FAKE + 1), kda.KDA_ERR_MISALIGNED),
+    ]
+    for change, want in cases:
+        a = _valid_verify_args()
+        for k, v in change.items():
+            setattr(a, k, v)
+        assert _call_verify(lib, a) == want, (change, kda.last_error())
+        assert kda.last_error()
+    # lower-bound gate needs a finite bound
+    a = _valid_verify_args()
+    a.gate_mode, a.lower_bound = kda.GATE_LOWER_BOUND, float("nan")
+    assert _call_verify(lib, a) == kda.KDA_ERR_INVALID_ARG
+    # activation rows at odd element offsets are accepted by validation (handled in-kernel):
+    # not launched here, so only checked through the MISALIGNED path not triggering above.
+
+
+def test_verify_empty_is_a_no_op(lib):
+    for change in (dict(B=0, T=0), dict(T=0)):
+        a = _valid_verify_args()
+        for k, v in change.items():
+            setattr(a, k, v)
+        assert _call_verify(lib, a) == kda.KDA_OK
+
+
+def _valid_commit_args():
+    a = kda.CommitArgs()
+    a.L, a.B, a.H, a.K, a.V, a.Q = 2, 3, 4, 128, 128, 4
+    a.num_slots, a.num_record_rows = 8, 8
+    for name in ("state_base", "state_slot_stride", "corr_base", "corr_row_stride", "kg_base",
+                 "kg_row_stride", "A_log", "dt_bias", "query_start_loc", "state_indices", "num_accepted"):
+        setattr(a, name, FAKE)
+    return a
+
+
+def test_commit_rejects_before_launch(lib):
+    assert lib.kda_commit(None, None) == kda.KDA_ERR_INVALID_ARG
+    cases = [
+        (dict(L=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(B=-2), kda.KDA_ERR_INVALID_ARG),
+        (dict(K=32, V=32), kda.KDA_ERR_UNSUPPORTED),
+        (dict(Q=12), kda.KDA_ERR_UNSUPPORTED),
+        (dict(kg_base=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(num_accepted=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(gate_mode=-1), kda.KDA_ERR_INVALID_ARG),
+        (dict(num_record_rows=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(A_log=FAKE + 2), kda.KDA_ERR_MISALIGNED),
+    ]
+    for change, want in cases:
+        a = _valid_commit_args()
+        for k, v in change.items():
+            setattr(a, k, v)
+        assert lib.kda_commit(ctypes.byref(a), None) == want, (change, kda.last_error())
+    a = _valid_commit_args()
+    a.B = 0
+    assert lib.kda_commit(ctypes.byref(a), None) == kda.KDA_OK
+
+
+def test_read_device_error_rejects_null(lib):
+    assert lib.kda_read_device_error(None, None, None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    from workloads import CONFIGS, make_problem
+    from workloads.drive import device_meta, verify_layer
+    prob = make_problem(CONFIGS["C0"])
+    with pytest.raises(ValueError, match="CUDA device"):
+        verify_layer(prob, 0, device_meta(prob.meta, "cpu"))
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    code = (
+        "import linear_attention_ssm_kda_gb300 as k\n"
+        f"k._LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+        "try:\n    k.load_library()\nexcept ImportError as e:\n    print('raised', e)\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT)
+    assert "raised" in r.stdout and "not built" in r.stdout

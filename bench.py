@@ -240,6 +240,46 @@ def time_oracle(cfg_name: str, steps: int, warmup: int, sample_layers: int = 1, 
 
 # --------------------------------------------------------------------------- GPU arm
 
+def run_e2e(args, prob, dm, step, stream, dev, world):
+    """End to end through the public API with host buffers: every step copies
+    its inputs from pinned host memory, runs, and reads its outputs back."""
+    meta = prob.meta
+    host_fused = torch.empty(prob.fused.shape, dtype=prob.fused.dtype, pin_memory=True)
+    host_fused.copy_(prob.fused)
+    host_meta = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
+                 for k, v in (("qsl", meta.query_start_loc), ("si", meta.state_indices),
+                              ("prev", meta.num_accepted_prev), ("acc", meta.num_accepted)) if v is not None}
+    host_out = torch.empty(prob.out.shape, dtype=prob.out.dtype, pin_memory=True)
+    h2d = host_fused.numel() * 2 + sum(t.numel() * 4 for t in host_meta.values())
+    d2h = host_out.numel() * 2
+
+    def e2e_step():
+        prob.fused.copy_(host_fused, non_blocking=True)
+        dm.query_start_loc.copy_(host_meta["qsl"], non_blocking=True)
+        dm.state_indices.copy_(host_meta["si"], non_blocking=True)
+        if "prev" in host_meta:
+            dm.num_accepted_prev.copy_(host_meta["prev"], non_blocking=True)
+        dm.num_accepted.copy_(host_meta["acc"], non_blocking=True)
+        step()
+        host_out.copy_(prob.out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 2)
+    barrier(world)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e_start.elapsed_time(e_end)
+
+    return e2e_ms, e2e_steps, h2d, d2h
+
+
 def run_gpu(args, rank, local, world):
     import linear_attention_ssm_kda_gb300 as kda
     from linear_attention_ssm_kda_gb300 import _build
@@ -253,6 +293,8 @@ def run_gpu(args, rank, local, world):
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
     cfg = CONFIGS[args.config]
+    if args.layers:
+        cfg = cfg.replace(L=args.layers)
     prob = make_problem(cfg, dev, seed=shard_seed(cfg.seed, rank))
     meta = prob.meta
     acct = step_accounting(cfg, meta)
@@ -303,44 +345,13 @@ def run_gpu(args, rank, local, world):
     verify_ms = [events[k][l].elapsed_time(events[k][l + 1]) for k in range(args.steps) for l in range(L)]
     commit_ms = [events[k][L].elapsed_time(events[k][L + 1]) for k in range(args.steps)]
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the step, D2H of the step's outputs
-    host_fused = torch.empty(prob.fused.shape, dtype=prob.fused.dtype, pin_memory=True)
-    host_fused.copy_(prob.fused)
-    host_meta = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
-                 for k, v in (("qsl", meta.query_start_loc), ("si", meta.state_indices),
-                              ("prev", meta.num_accepted_prev), ("acc", meta.num_accepted)) if v is not None}
-    host_out = torch.empty(prob.out.shape, dtype=prob.out.dtype, pin_memory=True)
-    h2d = host_fused.numel() * 2 + sum(t.numel() * 4 for t in host_meta.values())
-    d2h = host_out.numel() * 2
-
-    def e2e_step():
-        prob.fused.copy_(host_fused, non_blocking=True)
-        dm.query_start_loc.copy_(host_meta["qsl"], non_blocking=True)
-        dm.state_indices.copy_(host_meta["si"], non_blocking=True)
-        if "prev" in host_meta:
-            dm.num_accepted_prev.copy_(host_meta["prev"], non_blocking=True)
-        dm.num_accepted.copy_(host_meta["acc"], non_blocking=True)
-        step()
-        host_out.copy_(prob.out, non_blocking=True)
-
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, args.steps // 2)
-    barrier(world)
-    e_start.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e_end.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e_start.elapsed_time(e_end)
+    e2e_ms, e2e_steps, h2d, d2h = None, 0, 0, 0
+    if not args.no_e2e:
+        e2e_ms, e2e_steps, h2d, d2h = run_e2e(args, prob, dm, step, stream, dev, world)
 
     # aggregate over ranks: units of all ranks / the slowest rank's time
     t_max = max_over_ranks(elapsed_ms, world)
-    e_max = max_over_ranks(e2e_ms, world)
+    e_max = max_over_ranks(e2e_ms, world) if e2e_ms is not None else None
     tokens_all = sum_over_ranks(acct["tokens"] * args.steps, world)
     tokens_e2e = sum_over_ranks(acct["tokens"] * e2e_steps, world)
     bytes_all = sum_over_ranks(acct["step_bytes"] * args.steps, world)
@@ -403,8 +414,9 @@ def run_gpu(args, rank, local, world):
             "kda_commit": {"launches_per_step": 1, "avg_ms": c_avg, "bytes_per_launch": acct["commit_bytes"],
                            "gbs": c_gbs, "share": 1 - v_share, "items": acct["commit_items"]},
         },
-        "e2e": {"value": tokens_e2e / (e_max / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+        "e2e": None if e_max is None else {
+            "value": tokens_e2e / (e_max / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
         "gpu_launches": args.steps * (L + 1),
         "clocks": clk,
         "cpu_baseline": cpu,
@@ -448,7 +460,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default="C2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--cpu-steps", type=int, default=40)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the layer count (small cases for profiling; not a bench line)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

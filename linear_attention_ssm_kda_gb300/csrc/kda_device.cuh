@@ -104,6 +104,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Shared -> global bulk copy (TMA store), tracked by the issuing thread's bulk
+// groups.  dst/src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until the committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Order this thread's generic shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------
 // bf16 conversions
 // ----------------------------------------------------------------------------
@@ -131,43 +145,54 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// The rare fp64 evaluation of bf16_rne(silu(sum_j w_j x_j)), kept out of line.
+static __device__ __noinline__ uint16_t conv_silu_bf16_fp64(float w0, float w1, float w2, float w3, float x0,
+                                                             float x1, float x2, float x3) {
+  double yd = 0.0;
+  yd += static_cast<double>(w0) * static_cast<double>(x0);
+  yd += static_cast<double>(w1) * static_cast<double>(x1);
+  yd += static_cast<double>(w2) * static_cast<double>(x2);
+  yd += static_cast<double>(w3) * static_cast<double>(x3);
+  return f64_to_bf16(yd / (1.0 + exp(-yd)));
+}
+
 // bf16_rne(silu(y)) for y = sum_j w_j x_j (W = 4 taps), rounded from the exact
-// value.  y is carried as an unevaluated pair yh + yl (error-free products by
-// fma and TwoSum), so its error is ~2^-48 sum|w_j x_j|.  silu(yh) in fp32
-// (expf within 2 ulp, IEEE add and divide) has relative error below 1.5*2^-22;
-// the first-order term silu'(yh) yl is added.  Bound used: 2^-21 |s| plus a
-// 2^-40 sum|w_j x_j| margin for the rounding of the pair's low part.  When the bound straddles a bf16
-// rounding boundary (about 2e-4 of the values) the result is recomputed in
-// fp64, where the products of bf16 and fp32 values are exact.
+// value of y.  y is carried as an unevaluated pair y + yr: the products are
+// exact in fp32 for bf16 weights (fp32 weights add their fma residuals), and
+// TwoSum keeps every addition error, so y + yr is y to within 2^-44 of
+// M = |p0 + p1| + |p2 + p3| (2^-40 sum|w_j x_j| for fp32 weights).
+// silu(y) = y * sigma, sigma = 1 / (1 + expf(-y)) with expf within 2 ulp and
+// __fdividef within 2 ulp: relative error below 5 ulp < 2^-20; the first-order
+// term silu'(y) yr is added.  If [s - bound, s + bound] rounds to a single
+// bf16 value (all but ~5e-4 of values) that is the answer; otherwise fp64.
 __device__ __forceinline__ uint16_t conv_silu_bf16(const float w[4], const float x[4], bool exact_products) {
-  float sh = 0.0f, el = 0.0f, A = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float p = __fmul_rn(w[j], x[j]);
-    float t;
-    two_sum(sh, p, sh, t);
-    el = __fadd_rn(el, t);
-    if (!exact_products) el = __fadd_rn(el, __fmaf_rn(w[j], x[j], -p));
-    A = __fadd_rn(A, fabsf(p));
+  const float p0 = __fmul_rn(w[0], x[0]), p1 = __fmul_rn(w[1], x[1]);
+  const float p2 = __fmul_rn(w[2], x[2]), p3 = __fmul_rn(w[3], x[3]);
+  float s01, e01, s23, e23, yh, e;
+  two_sum(p0, p1, s01, e01);
+  two_sum(p2, p3, s23, e23);
+  two_sum(s01, s23, yh, e);
+  float yl = __fadd_rn(__fadd_rn(e01, e23), e);
+  float margin = (fabsf(s01) + fabsf(s23)) * 0x1p-44f;
+  if (!exact_products) {
+    const float r0 = __fmaf_rn(w[0], x[0], -p0), r1 = __fmaf_rn(w[1], x[1], -p1);
+    const float r2 = __fmaf_rn(w[2], x[2], -p2), r3 = __fmaf_rn(w[3], x[3], -p3);
+    yl = __fadd_rn(yl, __fadd_rn(__fadd_rn(r0, r1), __fadd_rn(r2, r3)));
+    margin = (fabsf(p0) + fabsf(p1) + fabsf(p2) + fabsf(p3)) * 0x1p-40f;
   }
-  float yh, yl;
-  two_sum(sh, el, yh, yl);
-  if (fabsf(yh) <= 80.0f) {
-    const float e = expf(-yh);
-    const float d = __fadd_rn(1.0f, e);
-    const float sig = __fdiv_rn(1.0f, d);
-    float s = __fdiv_rn(yh, d);
-    const float dsilu = sig * (1.0f + yh * (1.0f - sig));  // silu'(yh)
-    s = __fmaf_rn(dsilu, yl, s);
-    const float bound = fabsf(s) * 0x1p-21f + A * 0x1p-40f + 0x1p-126f;
+  float y, yr;
+  two_sum(yh, yl, y, yr);
+  if (fabsf(y) <= 80.0f) {
+    const float sig = __fdividef(1.0f, 1.0f + expf(-y));
+    float s = y * sig;
+    const float dsilu = sig * (1.0f + y * (1.0f - sig));  // silu'(y)
+    s = __fmaf_rn(dsilu, yr, s);
+    const float bound = fabsf(s) * 0x1p-20f + margin + 0x1p-126f;
     const uint16_t lo = f32_to_bf16(__fsub_rd(s, bound));
     const uint16_t hi = f32_to_bf16(__fadd_ru(s, bound));
     if (lo == hi) return lo;
   }
-  double yd = 0.0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) yd += static_cast<double>(w[j]) * static_cast<double>(x[j]);
-  return f64_to_bf16(yd / (1.0 + exp(-yd)));
+  return conv_silu_bf16_fp64(w[0], w[1], w[2], w[3], x[0], x[1], x[2], x[3]);
 }
 
 // ----------------------------------------------------------------------------

@@ -128,71 +128,54 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Round a double straight to bf16 (nearest even): first to fp32 with
-// round-to-odd (truncate, then set the last bit when inexact), which keeps
-// the information the second rounding needs since fp32 carries more than two
-// extra bits over bf16; then round that fp32 to bf16.
-__device__ __forceinline__ uint16_t f64_to_bf16(double x) {
-  float f = __double2float_rz(x);
-  if (static_cast<double>(f) != x) f = __uint_as_float(__float_as_uint(f) | 1u);
-  return f32_to_bf16(f);
+// ----------------------------------------------------------------------------
+// The convolution output code.  The conv runs in fp32, as causal_conv1d_update
+// does, and the code stored for every later step is bf16(SiLU(y)).  So that
+// the code does not depend on how a compiler or a math library evaluates it,
+// every step is an IEEE-754 basic operation in a fixed order:
+//   y = w0 x0, then y = fma(wj, xj, y) for the newer taps j = 1 .. W-1;
+//   SiLU(y) = y / (1 + e^-y) (round-to-nearest add and divide);
+//   e^x: x clamped to [-104, 89] (e^-104 rounds to 0 and e^89 overflows, so
+//   the clamp changes no finite result); n = rint(x log2 e); Cody-Waite
+//   reduction r = x - n ln2 with ln2 split in a 15-bit head (n times it is
+//   exact) and a tail; e^r by its Taylor series to r^7/7! in Horner form
+//   (|r| <= 0.347, truncation under 1e-8 relative); e^x = e^r 2^n1 2^n2 with
+//   n1 = floor(n/2), n2 = n - n1 (the first scaling is exact, the second
+//   rounds once).  e^x is within one fp32 ulp of exact, SiLU within three.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float exp_f32(float x) {
+  constexpr float kLog2e = 0x1.715476p+0f;
+  constexpr float kLn2Hi = 0x1.62e4p-1f;
+  constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
+  x = fminf(fmaxf(x, -104.0f), 89.0f);
+  const float nf = rintf(__fmul_rn(x, kLog2e));
+  float r = __fmaf_rn(-nf, kLn2Hi, x);
+  r = __fmaf_rn(-nf, kLn2Lo, r);
+  // 1/k! rounded to fp32, k = 7 .. 2
+  float q = 0x1.a01a02p-13f;
+  q = __fmaf_rn(q, r, 0x1.6c16c2p-10f);
+  q = __fmaf_rn(q, r, 0x1.111112p-7f);
+  q = __fmaf_rn(q, r, 0x1.555556p-5f);
+  q = __fmaf_rn(q, r, 0x1.555556p-3f);
+  q = __fmaf_rn(q, r, 0.5f);
+  q = __fmaf_rn(q, r, 1.0f);
+  q = __fmaf_rn(q, r, 1.0f);
+  const int n = __float2int_rn(nf);
+  const int n1 = n >> 1;  // arithmetic shift: floor(n / 2)
+  const int n2 = n - n1;
+  q = __fmul_rn(q, __int_as_float((n1 + 127) << 23));
+  return __fmul_rn(q, __int_as_float((n2 + 127) << 23));
 }
 
-// Error-free sum: a + b == s + e exactly (Knuth's TwoSum, any magnitudes).
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
+__device__ __forceinline__ float silu_f32(float y) { return __fdiv_rn(y, __fadd_rn(1.0f, exp_f32(-y))); }
 
-// The rare fp64 evaluation of bf16_rne(silu(sum_j w_j x_j)), kept out of line.
-static __device__ __noinline__ uint16_t conv_silu_bf16_fp64(float w0, float w1, float w2, float w3, float x0,
-                                                             float x1, float x2, float x3) {
-  double yd = 0.0;
-  yd += static_cast<double>(w0) * static_cast<double>(x0);
-  yd += static_cast<double>(w1) * static_cast<double>(x1);
-  yd += static_cast<double>(w2) * static_cast<double>(x2);
-  yd += static_cast<double>(w3) * static_cast<double>(x3);
-  return f64_to_bf16(yd / (1.0 + exp(-yd)));
-}
-
-// bf16_rne(silu(y)) for y = sum_j w_j x_j (W = 4 taps), rounded from the exact
-// value of y.  y is carried as an unevaluated pair y + yr: the products are
-// exact in fp32 for bf16 weights (fp32 weights add their fma residuals), and
-// TwoSum keeps every addition error, so y + yr is y to within 2^-44 of
-// M = |p0 + p1| + |p2 + p3| (2^-40 sum|w_j x_j| for fp32 weights).
-// silu(y) = y * sigma, sigma = 1 / (1 + expf(-y)) with expf within 2 ulp and
-// __fdividef within 2 ulp: relative error below 5 ulp < 2^-20; the first-order
-// term silu'(y) yr is added.  If [s - bound, s + bound] rounds to a single
-// bf16 value (all but ~5e-4 of values) that is the answer; otherwise fp64.
-__device__ __forceinline__ uint16_t conv_silu_bf16(const float w[4], const float x[4], bool exact_products) {
-  const float p0 = __fmul_rn(w[0], x[0]), p1 = __fmul_rn(w[1], x[1]);
-  const float p2 = __fmul_rn(w[2], x[2]), p3 = __fmul_rn(w[3], x[3]);
-  float s01, e01, s23, e23, yh, e;
-  two_sum(p0, p1, s01, e01);
-  two_sum(p2, p3, s23, e23);
-  two_sum(s01, s23, yh, e);
-  float yl = __fadd_rn(__fadd_rn(e01, e23), e);
-  float margin = (fabsf(s01) + fabsf(s23)) * 0x1p-44f;
-  if (!exact_products) {
-    const float r0 = __fmaf_rn(w[0], x[0], -p0), r1 = __fmaf_rn(w[1], x[1], -p1);
-    const float r2 = __fmaf_rn(w[2], x[2], -p2), r3 = __fmaf_rn(w[3], x[3], -p3);
-    yl = __fadd_rn(yl, __fadd_rn(__fadd_rn(r0, r1), __fadd_rn(r2, r3)));
-    margin = (fabsf(p0) + fabsf(p1) + fabsf(p2) + fabsf(p3)) * 0x1p-40f;
-  }
-  float y, yr;
-  two_sum(yh, yl, y, yr);
-  if (fabsf(y) <= 80.0f) {
-    const float sig = __fdividef(1.0f, 1.0f + expf(-y));
-    float s = y * sig;
-    const float dsilu = sig * (1.0f + y * (1.0f - sig));  // silu'(y)
-    s = __fmaf_rn(dsilu, yr, s);
-    const float bound = fabsf(s) * 0x1p-20f + margin + 0x1p-126f;
-    const uint16_t lo = f32_to_bf16(__fsub_rd(s, bound));
-    const uint16_t hi = f32_to_bf16(__fadd_ru(s, bound));
-    if (lo == hi) return lo;
-  }
-  return conv_silu_bf16_fp64(w[0], w[1], w[2], w[3], x[0], x[1], x[2], x[3]);
+// bf16 code of SiLU(sum_j w_j x_j) over W = 4 taps, oldest first.
+__device__ __forceinline__ uint16_t conv_silu_bf16(const float w[4], const float x[4]) {
+  float y = __fmul_rn(w[0], x[0]);
+  y = __fmaf_rn(w[1], x[1], y);
+  y = __fmaf_rn(w[2], x[2], y);
+  y = __fmaf_rn(w[3], x[3], y);
+  return f32_to_bf16(silu_f32(y));
 }
 
 // ----------------------------------------------------------------------------
@@ -207,6 +190,22 @@ __device__ __forceinline__ float kda_gate(float raw_g, float dt_bias, float A, i
 }
 
 __device__ __forceinline__ float sigmoidf(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// e^g for the KDA gate with the hardware approximations (ex2 / lg2): g feeds
+// only the decay, where a few 1e-7 of relative error is far below the bf16
+// outputs' resolution.  softplus(u) = log(1 + e^u) below 20, u above.
+__device__ __forceinline__ float kda_decay_fast(float raw_g, float dt_bias, float A, int lower_bound_gate,
+                                                float lower_bound) {
+  const float u = raw_g + dt_bias;
+  float g;
+  if (lower_bound_gate)
+    g = __fdividef(lower_bound, 1.0f + __expf(-A * u));
+  else
+    g = -A * ((u > 20.0f) ? u : __logf(1.0f + __expf(u)));
+  return __expf(g);
+}
+
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

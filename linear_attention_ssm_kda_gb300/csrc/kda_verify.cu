@@ -267,7 +267,7 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
 #pragma unroll
     for (int t = 0; t < QMAX; ++t)
       beta[t] = (im.flags == kLive && t < im.n)
-                    ? sigmoidf(bf16_to_f32(p.raw_beta[static_cast<long long>(im.bos + t) * p.beta_stride + im.h]))
+                    ? sigmoid_fast(bf16_to_f32(p.raw_beta[static_cast<long long>(im.bos + t) * p.beta_stride + im.h]))
                     : 0.0f;
     const int count = min(32, nloc - i0);
     for (int j = 0; j < count && ok; ++j) {
@@ -516,8 +516,8 @@ __device__ void compute(const VerifyParams& p, unsigned char* smem, int ct, vola
                                         bf16_to_f32(seq[t + 3])};
           const float x1[kConvWidth] = {bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]), bf16_to_f32(seq[t + 3]),
                                         bf16_to_f32(seq[t + 4])};
-          const uint16_t y0 = conv_silu_bf16(w, x0, !p.conv_weight_fp32);
-          const uint16_t y1 = conv_silu_bf16(w, x1, !p.conv_weight_fp32);
+          const uint16_t y0 = conv_silu_bf16(w, x0);
+          const uint16_t y1 = conv_silu_bf16(w, x1);
           xg[t * KD + k] = bf16_to_f32(y0);
           if (g == 1) kg[t * 2 * KD + k] = y0;  // key record: the bf16 conv output
           if (t + 1 < n && t + 1 < QMAX) {
@@ -546,7 +546,7 @@ __device__ void compute(const VerifyParams& p, unsigned char* smem, int ct, vola
                 (gate_lo + static_cast<uint32_t>(bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
             const uint16_t rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
             kg[t * 2 * KD + KD + k] = rg;  // gate record: bit copy
-            egs[t * KD + k] = expf(kda_gate(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound));
+            egs[t * KD + k] = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
           }
         }
       }

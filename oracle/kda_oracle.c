@@ -20,10 +20,25 @@
  *             deferred_recoverssm_verify (conv -> split q/k/v -> verify,
  *             records written to record rows).
  *
- * Every quantity is computed in double from the exact values of the bf16 /
- * fp32 inputs.  Values the method stores in a narrower type are rounded once,
- * from the double result: outputs and key/gate records to bf16 (round to
- * nearest even), corrections and committed states to fp32.
+ * Every quantity after the convolution is computed in double from the exact
+ * values of the bf16 / fp32 inputs.  Values the method stores in a narrower
+ * type are rounded once, from the double result: outputs and key/gate records
+ * to bf16 (round to nearest even), corrections and committed states to fp32.
+ *
+ * The convolution output is the one place where floating point decides a
+ * stored code: the bf16 value that every later step consumes.  The pages fuse
+ * the convolution as causal_conv1d_update does, which accumulates and applies
+ * SiLU in fp32 and then casts to bf16, without fixing the order of the sums or
+ * the exp routine.  So the oracle takes that decision in fp32 with a fully
+ * specified procedure (conv_silu_bf16_f32 below): the taps are summed oldest
+ * first, y = w0 x0, then y = fma(wj, xj, y); SiLU is y / (1 + exp_f32(-y))
+ * with IEEE fp32 add and divide; exp_f32 is Cody-Waite argument reduction by
+ * ln 2 (split in a 15-bit head and a tail) with a degree-7 Taylor polynomial
+ * in Horner form and an exact scaling by 2^n; the result is rounded to bf16,
+ * nearest even.  Every step is an IEEE-754 basic operation, so any conforming
+ * implementation gets the same bits.  The pins check it against the exact
+ * double-precision value (within a few fp32 ulp), so it is an accurate fp32
+ * evaluation and not merely a self-consistent one.
  *
  * Readings taken where the pages are silent (each is listed in the design
  * notes of the repository):
@@ -85,7 +100,61 @@ static uint16_t bf16_round(double x) {
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
-static double silu(double x) { return x / (1.0 + exp(-x)); }
+/* ------------------------------------------------------------------------- */
+/* The fp32 convolution output, fully specified (see the header)              */
+/* ------------------------------------------------------------------------- */
+
+static float f32_from_bits(uint32_t w) {
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return f;
+}
+
+/* e^x in fp32: x is clamped to [-104, 89] (e^-104 rounds to 0 and e^89
+ * overflows, so the clamp changes no finite result); n = rint(x log2 e);
+ * r = x - n ln2 with ln2 = LN2_HI + LN2_LO (LN2_HI has 15 significant bits,
+ * so n LN2_HI is exact and each fma rounds once); e^r by the Taylor series
+ * to r^7/7! (|r| <= 0.347: truncation below 1e-8 relative); then
+ * e^x = e^r 2^n1 2^n2 with n1 = floor(n/2), n2 = n - n1, both in the normal
+ * range, so the first scaling is exact and the second rounds once. */
+static float exp_f32(float x) {
+    const float LOG2E = 0x1.715476p+0f;
+    const float LN2_HI = 0x1.62e4p-1f;
+    const float LN2_LO = 0x1.7f7d1cp-20f;
+    x = fminf(fmaxf(x, -104.0f), 89.0f);
+    const float nf = rintf(x * LOG2E);
+    float r = fmaf(-nf, LN2_HI, x);
+    r = fmaf(-nf, LN2_LO, r);
+    /* 1/k! rounded to fp32, k = 7 .. 2 */
+    float p = 0x1.a01a02p-13f;
+    p = fmaf(p, r, 0x1.6c16c2p-10f);
+    p = fmaf(p, r, 0x1.111112p-7f);
+    p = fmaf(p, r, 0x1.555556p-5f);
+    p = fmaf(p, r, 0x1.555556p-3f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    const int n = (int)nf;
+    const int n1 = n >= 0 ? n / 2 : -((1 - n) / 2); /* floor(n / 2) */
+    const int n2 = n - n1;
+    p = p * f32_from_bits((uint32_t)(n1 + 127) << 23);
+    return p * f32_from_bits((uint32_t)(n2 + 127) << 23);
+}
+
+/* SiLU in fp32: y / (1 + e^-y), IEEE add and divide. */
+static float silu_f32(float y) { return y / (1.0f + exp_f32(-y)); }
+
+/* fp32 -> bf16, nearest even: the fp32 value is exact in double, so one
+ * rounding of it is the fp32 -> bf16 rounding. */
+static uint16_t bf16_from_f32(float f) { return bf16_round((double)f); }
+
+/* The conv output code: bf16(SiLU(sum_j w_j x_j)) by the fp32 procedure,
+ * taps oldest first, W of them. */
+static uint16_t conv_silu_bf16_f32(const float *w, const float *x, int W) {
+    float y = w[0] * x[0];
+    for (int j = 1; j < W; ++j) y = fmaf(w[j], x[j], y);
+    return bf16_from_f32(silu_f32(y));
+}
 
 /* [ops] _kda_gate: gate_input = raw_g + dt_bias; the bounded form is
  * lower_bound * sigmoid(A * gate_input); otherwise -A * softplus(gate_input)
@@ -141,9 +210,9 @@ static int64_t conv_index(const kda_oracle_verify_args *a, int64_t s, int64_t c,
                              : s * a->conv_slot_stride + j * C + c;
 }
 
-static double conv_weight_value(const kda_oracle_verify_args *a, int64_t c, int j) {
-    if (a->conv_weight_is_fp32) return (double)((const float *)a->conv_weight)[c * a->W + j];
-    return bf16_value(((const uint16_t *)a->conv_weight)[c * a->W + j]);
+static float conv_weight_value(const kda_oracle_verify_args *a, int64_t c, int j) {
+    if (a->conv_weight_is_fp32) return ((const float *)a->conv_weight)[c * a->W + j];
+    return (float)bf16_value(((const uint16_t *)a->conv_weight)[c * a->W + j]);
 }
 
 /* One (request b, head h) of the verify; returns ORACLE_BAD_DATA on an
@@ -186,9 +255,12 @@ static int verify_item(const kda_oracle_verify_args *a, int b, int h) {
             for (int t = 0; t < n; ++t)
                 seq[W - 1 + t] = a->mixed_qkv[(bos + t) * a->qkv_row_stride + c];
             for (int t = 0; t < n; ++t) {
-                double y = 0.0;
-                for (int j = 0; j < W; ++j) y += conv_weight_value(a, c, j) * bf16_value(seq[t + j]);
-                post[(size_t)(g * K + i) * n + t] = bf16_value(bf16_round(silu(y)));
+                float wv[8], xv[8];
+                for (int j = 0; j < W; ++j) {
+                    wv[j] = conv_weight_value(a, c, j);
+                    xv[j] = (float)bf16_value(seq[t + j]);
+                }
+                post[(size_t)(g * K + i) * n + t] = bf16_value(conv_silu_bf16_f32(wv, xv, W));
             }
             /* rolled state: taps 0 .. W-3+n <- seq[1 .. W-2+n] */
             for (int j = 0; j < W - 2 + n; ++j)
@@ -272,7 +344,7 @@ static int verify_item(const kda_oracle_verify_args *a, int b, int h) {
 }
 
 int kda_oracle_verify(const kda_oracle_verify_args *a) {
-    if (!a || a->B < 0 || a->H <= 0 || a->K <= 0 || a->V != a->K || a->Q <= 0 || a->W < 2)
+    if (!a || a->B < 0 || a->H <= 0 || a->K <= 0 || a->V != a->K || a->Q <= 0 || a->W < 2 || a->W > 8)
         return ORACLE_BAD_ARGS;
     int status = ORACLE_OK;
     const int items = a->B * a->H;
@@ -373,4 +445,13 @@ uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
 double kda_oracle_gate(double raw_g, double dt_bias, double A, int use_lower_bound, double lower_bound) {
     return kda_gate(raw_g, dt_bias, A, use_lower_bound, lower_bound);
 }
-double kda_oracle_silu(double x) { return silu(x); }
+void kda_oracle_exp_f32(const float *x, float *y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = exp_f32(x[i]);
+}
+void kda_oracle_silu_f32(const float *x, float *y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = silu_f32(x[i]);
+}
+/* w, x: [n, W] row-major; out: [n] bf16 codes. */
+void kda_oracle_conv_silu_bf16_f32(const float *w, const float *x, uint16_t *out, int64_t n, int W) {
+    for (int64_t i = 0; i < n; ++i) out[i] = conv_silu_bf16_f32(w + i * W, x + i * W, W);
+}

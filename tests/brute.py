@@ -24,18 +24,52 @@ def bf16_values(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def conv_silu(hist: np.ndarray, x: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """hist [W-1, C], x [n, C] (values), w [C, W] -> bf16-rounded SiLU(conv) [n, C].
-    Causal: the last tap multiplies the newest input."""
+def conv_silu_exact(hist: np.ndarray, x: np.ndarray, w: np.ndarray):
+    """hist [W-1, C], x [n, C] (values), w [C, W] -> (SiLU(conv) in double [n, C],
+    sum_j |w_j x_j| [n, C]).  Causal: the last tap multiplies the newest input."""
     seq = np.concatenate([hist, x], axis=0)
     n = x.shape[0]
     C = x.shape[1]
     y = np.empty((n, C))
+    mag = np.empty((n, C))
     for c in range(C):
         # np.convolve flips its second operand; 'valid' keeps windows fully inside seq
         y[:, c] = np.convolve(seq[:, c], w[c, ::-1], mode="valid")[:n]
-    s = y * expit(y)
-    return np.vectorize(lambda v: bf16_values(np.array([oracle.bf16_round(v)], np.uint16))[0])(s)
+        mag[:, c] = np.convolve(np.abs(seq[:, c]), np.abs(w[c, ::-1]), mode="valid")[:n]
+    return y * expit(y), mag, y
+
+
+def bf16_rne(v: np.ndarray) -> np.ndarray:
+    """bf16 codes of double values, nearest even (the oracle's straight rounding)."""
+    v = np.asarray(v, np.float64)
+    return np.array([oracle.bf16_round(float(e)) for e in v.ravel()], np.uint16).reshape(v.shape)
+
+
+def assert_codes_round_exact(codes: np.ndarray, s: np.ndarray, mag: np.ndarray, y: np.ndarray,
+                             max_frac: float = 2e-3):
+    """bf16 codes of an fp32 evaluation of s = SiLU(y), y = sum_j w_j x_j, are
+    the correct rounding of the exact s except near a rounding boundary: a
+    differing code must be the rounding of some value within the fp32
+    evaluation's error of s.  That error is a few fp32 ulp of s plus
+    |SiLU'(y)| times the summation error 2^-22 sum_j |w_j x_j|."""
+    codes = np.asarray(codes, np.uint16).ravel()
+    s = np.asarray(s, np.float64).ravel()
+    exact = bf16_rne(s)
+    bad = np.nonzero(codes != exact)[0]
+    assert len(bad) <= max(1, max_frac * codes.size), f"{len(bad)} of {codes.size} codes differ"
+    if len(bad) == 0:
+        return
+    yb = np.asarray(y, np.float64).ravel()[bad]
+    sig = expit(yb)
+    dsilu = np.abs(sig * (1 + yb * (1 - sig)))
+    slack = (np.abs(s[bad]) * 2.0 ** -20 + dsilu * np.asarray(mag, np.float64).ravel()[bad] * 2.0 ** -22
+             + 2.0 ** -130)
+    got = bf16_values(codes[bad])
+    lo = bf16_values(bf16_rne(s[bad] - slack))
+    hi = bf16_values(bf16_rne(s[bad] + slack))
+    ok = (got >= lo) & (got <= hi)
+    assert np.all(ok), (f"codes {codes[bad][~ok][:4]} for exact values {s[bad][~ok][:4]} "
+                        "are not the rounding of any value within the fp32 error")
 
 
 def gate(raw_g, dt_bias, A, lower_bound):

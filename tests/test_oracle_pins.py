@@ -70,13 +70,90 @@ def test_gate_against_library_routines():
     assert abs(oracle.gate(20.0 + 1e-9, 0, 1) - oracle.gate(20.0 - 1e-9, 0, 1)) < 1e-8
 
 
-def test_silu_against_scipy():
-    for x in np.linspace(-60, 60, 1201):
-        assert oracle.silu(x) == pytest.approx(x * expit(x), rel=1e-13, abs=1e-300)
-    assert oracle.silu(0.0) == 0.0
+def _ulp_f32(v):
+    """fp32 ulp at |v| (v double), the subnormal quantum at the bottom."""
+    f = np.abs(np.asarray(v, np.float64)).astype(np.float32)
+    return np.maximum(np.spacing(f).astype(np.float64), 2.0 ** -149)
+
+
+def test_exp_f32_within_one_ulp_of_exp():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([np.linspace(-103.9, 88.7, 400_001), rng.uniform(-12, 12, 400_000),
+                        rng.standard_normal(200_000) * 3]).astype(np.float32)
+    got = oracle.exp_f32(x).astype(np.float64)
+    want = np.exp(x.astype(np.float64))
+    assert np.all(np.abs(got - want) <= _ulp_f32(want))
+    # monotone on a sorted grid, and the fixed points of the definition
+    xs = np.sort(x)
+    assert np.all(np.diff(oracle.exp_f32(xs).astype(np.float64)) >= 0)
+    special = oracle.exp_f32(np.array([0.0, -0.0, 89.0, 1e30, -104.0, -1e30], np.float32))
+    assert special[0] == 1.0 and special[1] == 1.0
+    assert np.isinf(special[2]) and np.isinf(special[3])
+    assert special[4] == 0.0 and special[5] == 0.0
+    # e^x for integer x against the correctly rounded constants
+    for k in range(-80, 81, 7):
+        assert abs(float(oracle.exp_f32(np.float32(k))[0]) - math.exp(k)) <= _ulp_f32(math.exp(k))
+
+
+def test_silu_f32_within_three_ulp_of_silu():
+    rng = np.random.default_rng(6)
+    x = np.concatenate([np.linspace(-88.0, 88.0, 400_001), rng.standard_normal(300_000) * 4,
+                        rng.uniform(-1e-3, 1e-3, 50_000)]).astype(np.float32)
+    got = oracle.silu_f32(x).astype(np.float64)
+    xd = x.astype(np.float64)
+    want = xd * expit(xd)
+    assert np.all(np.abs(got - want) <= 3 * _ulp_f32(want))
+    # far tails: silu(y) = y above 88 (e^-y vanishes next to 1) and -0 below -89
+    big = np.array([90.0, 1e4, 3e38], np.float32)
+    np.testing.assert_array_equal(oracle.silu_f32(big), big)
+    neg = oracle.silu_f32(np.array([-90.0, -1e4], np.float32))
+    assert np.all(neg == 0.0) and np.all(np.signbit(neg))
+    assert oracle.silu_f32(np.float32(0.0))[0] == 0.0
+
+
+@pytest.mark.parametrize("fp32_weights", [False, True])
+def test_conv_code_is_the_correct_rounding_but_for_near_ties(fp32_weights):
+    """Codes of the fp32 conv + SiLU against the exact double value rounded once."""
+    rng = np.random.default_rng(7 + fp32_weights)
+    n, W = 300_000, 4
+    gen = torch.Generator().manual_seed(17 + fp32_weights)
+    x = brute.bf16_values(torch.randn(n, W, dtype=torch.float32, generator=gen).mul_(1.5)
+                          .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    w = rng.normal(0, 0.5, (n, W)).astype(np.float32)
+    if not fp32_weights:
+        w = brute.bf16_values(torch.from_numpy(w).to(torch.bfloat16).view(torch.int16)
+                              .numpy().view(np.uint16))
+    codes = oracle.conv_silu_bf16_f32(w, x)
+    y = (w.astype(np.float64) * x.astype(np.float64)).sum(axis=1)
+    mag = np.abs(w.astype(np.float64) * x.astype(np.float64)).sum(axis=1)
+    brute.assert_codes_round_exact(codes, y * expit(y), mag, y, max_frac=2e-3)
+    # unit taps pick one input: y is that bf16 value exactly
+    onehot = np.zeros((4, W), np.float32)
+    onehot[np.arange(4), np.arange(4)] = 1.0
+    xs = x[:4]
+    got = oracle.conv_silu_bf16_f32(onehot, xs)
+    yy = xs[np.arange(4), np.arange(4)].astype(np.float64)
+    brute.assert_codes_round_exact(got, yy * expit(yy), np.abs(yy), yy)
+
+
+def test_conv_code_tap_order_is_oldest_first():
+    """fp32 weights, taps whose sum cancels: summing oldest first rounds the
+    running sum at different places than newest first; the codes follow the
+    stated order (w0 x0 first, then fma of each newer tap)."""
+    w = np.array([[1.0, 2.0 ** -30, -1.0, 2.0 ** -30]], np.float32)
+    x = np.array([[1.0, 1.0, 1.0, 1.0]], np.float32)
+    # oldest first: 1 + 2^-30 rounds to 1, - 1 -> 0, + 2^-30 -> 2^-30
+    y = np.float32(2.0 ** -30)
+    want = oracle.bf16_round(float(y) * float(expit(float(y))))
+    assert int(oracle.conv_silu_bf16_f32(w, x)[0]) == want
 
 
 # --------------------------------------------------------------------------- brute force
+
+def _codes(values):
+    """bf16 codes of bf16-exact double values."""
+    return (np.asarray(values, np.float64).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
 
 def _tiny(**kw):
     base = Config("tiny", B=3, H=2, K=4, Q=4, L=1, slots=6, seed=11, state_std=0.3)
@@ -133,9 +210,9 @@ def test_verify_matches_matrix_form_bruteforce(variant):
             it = _item_inputs(prob, fresh, b, h)
             if it["n"] <= 0 or it["s"] <= 0:
                 continue
-            post = brute.conv_silu(it["hist"], it["x"], it["w"])
-            np.testing.assert_array_equal(
-                post, res["post_conv"][it["bos"]: it["bos"] + it["n"]][:, it["chans"]])
+            sx, mag, y = brute.conv_silu_exact(it["hist"], it["x"], it["w"])
+            post = res["post_conv"][it["bos"]: it["bos"] + it["n"]][:, it["chans"]]
+            brute.assert_codes_round_exact(_codes(post), sx, mag, y, max_frac=0.02)
             q, k, v = post[:, :K], post[:, K: 2 * K], post[:, 2 * K:]
             o, c, states = brute.window(it["S0"], q, k, v, it["raw_g"], it["raw_beta"],
                                         fresh.dt_bias[h * K:(h + 1) * K].astype(np.float64),
@@ -315,9 +392,8 @@ def test_conv_unit_taps(dim_first):
             seq = np.concatenate([it["hist"], it["x"]], axis=0)
             for t in range(it["n"]):
                 src = seq[t + tap]
-                ref = np.array([brute.bf16_values(np.array([oracle.bf16_round(y * expit(y))],
-                                                           np.uint16))[0] for y in src])
-                np.testing.assert_array_equal(res["post_conv"][it["bos"] + t, it["chans"]], ref)
+                brute.assert_codes_round_exact(_codes(res["post_conv"][it["bos"] + t, it["chans"]]),
+                                               src * expit(src), np.abs(src), src, max_frac=0.1)
 
 
 @pytest.mark.parametrize("dim_first", [True, False])

@@ -61,13 +61,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to kSuspendNs
+// while the phase is incomplete (it resumes as soon as the phase completes),
+// so that a waiting warp does not spin on issue slots its neighbours need.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return done != 0;
+}
+
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 
 // Wait for phase `parity` of `bar` to complete, giving up after about a second.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_suspend(bar, parity)) {
     if (global_timer_ns() - start > kWaitLimitNs) return false;
   }
   return true;
@@ -82,7 +98,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_suspend(bar, parity)) {
     if (*abort) return false;
     if (global_timer_ns() - start > kWaitLimitNs) return false;
   }
@@ -132,50 +148,76 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 // The convolution output code.  The conv runs in fp32, as causal_conv1d_update
 // does, and the code stored for every later step is bf16(SiLU(y)).  So that
 // the code does not depend on how a compiler or a math library evaluates it,
-// every step is an IEEE-754 basic operation in a fixed order:
+// every step is an IEEE-754 fp32 add, multiply or fma, or integer arithmetic
+// on the bits, in a fixed order, with no branch:
 //   y = w0 x0, then y = fma(wj, xj, y) for the newer taps j = 1 .. W-1;
-//   SiLU(y) = y / (1 + e^-y) (round-to-nearest add and divide);
-//   e^x: x clamped to [-104, 89] (e^-104 rounds to 0 and e^89 overflows, so
-//   the clamp changes no finite result); n = rint(x log2 e); Cody-Waite
-//   reduction r = x - n ln2 with ln2 split in a 15-bit head (n times it is
-//   exact) and a tail; e^r by its Taylor series to r^7/7! in Horner form
-//   (|r| <= 0.347, truncation under 1e-8 relative); e^x = e^r 2^n1 2^n2 with
-//   n1 = floor(n/2), n2 = n - n1 (the first scaling is exact, the second
-//   rounds once).  e^x is within one fp32 ulp of exact, SiLU within three.
+//   z = e^-|y|: x = max(-|y|, -104) (e^-104 rounds to 0); n = x log2 e rounded
+//     to nearest even, from the exact product, by one fma with 1.5 * 2^23
+//     (whose ulp is 1, so n sits in the low mantissa bits); Cody-Waite
+//     reduction r = x - n ln2 with ln2 split in a 15-bit head (n times it is
+//     exact) and a tail; e^r by its Taylor series to r^7/7! in Horner form
+//     (|r| <= 0.347, truncation under 1e-8 relative); z = e^r 2^n1 2^n2 with
+//     n1 = floor(n/2), n2 = n - n1 (the first scaling is exact, the second
+//     rounds once);
+//   1/(1+z), 1+z in [1, 2]: r0 = 24/17 - (8/17)(1+z), then three Newton steps;
+//   SiLU(y) = y sigma with sigma = 1/(1+z) for y >= 0 and z/(1+z) below.
+// e^x is within one fp32 ulp of exact, SiLU within four.
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ float exp_f32(float x) {
+// Two codes at once (tokens a and b of one channel) on the packed fp32x2 unit:
+// every half runs exactly the sequence described above, operation by
+// operation (fma(-n, c, x) is computed as fma(n, -c, x), the same exact value).
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+__device__ __forceinline__ float2 silu_f32x2(float2 y) {
   constexpr float kLog2e = 0x1.715476p+0f;
+  constexpr float kShifter = 0x1.8p+23f;
   constexpr float kLn2Hi = 0x1.62e4p-1f;
   constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
-  x = fminf(fmaxf(x, -104.0f), 89.0f);
-  const float nf = rintf(__fmul_rn(x, kLog2e));
-  float r = __fmaf_rn(-nf, kLn2Hi, x);
-  r = __fmaf_rn(-nf, kLn2Lo, r);
+  // z = e^x, x = max(-|y|, -104)
+  const float2 x = make_float2(fmaxf(-fabsf(y.x), -104.0f), fmaxf(-fabsf(y.y), -104.0f));
+  // n = rint(x log2 e) through the shifter, lane by lane on the scalar unit
+  const float ta = __fmaf_rn(x.x, kLog2e, kShifter), tb = __fmaf_rn(x.y, kLog2e, kShifter);
+  const float2 nf = make_float2(__fsub_rn(ta, kShifter), __fsub_rn(tb, kShifter));
+  const int na = __float_as_int(ta) - __float_as_int(kShifter);
+  const int nb = __float_as_int(tb) - __float_as_int(kShifter);
+  float2 r = __ffma2_rn(nf, f2(-kLn2Hi), x);
+  r = __ffma2_rn(nf, f2(-kLn2Lo), r);
   // 1/k! rounded to fp32, k = 7 .. 2
-  float q = 0x1.a01a02p-13f;
-  q = __fmaf_rn(q, r, 0x1.6c16c2p-10f);
-  q = __fmaf_rn(q, r, 0x1.111112p-7f);
-  q = __fmaf_rn(q, r, 0x1.555556p-5f);
-  q = __fmaf_rn(q, r, 0x1.555556p-3f);
-  q = __fmaf_rn(q, r, 0.5f);
-  q = __fmaf_rn(q, r, 1.0f);
-  q = __fmaf_rn(q, r, 1.0f);
-  const int n = __float2int_rn(nf);
-  const int n1 = n >> 1;  // arithmetic shift: floor(n / 2)
-  const int n2 = n - n1;
-  q = __fmul_rn(q, __int_as_float((n1 + 127) << 23));
-  return __fmul_rn(q, __int_as_float((n2 + 127) << 23));
+  float2 q = f2(0x1.a01a02p-13f);
+  q = __ffma2_rn(q, r, f2(0x1.6c16c2p-10f));
+  q = __ffma2_rn(q, r, f2(0x1.111112p-7f));
+  q = __ffma2_rn(q, r, f2(0x1.555556p-5f));
+  q = __ffma2_rn(q, r, f2(0x1.555556p-3f));
+  q = __ffma2_rn(q, r, f2(0.5f));
+  q = __ffma2_rn(q, r, f2(1.0f));
+  q = __ffma2_rn(q, r, f2(1.0f));
+  const int na1 = na >> 1, nb1 = nb >> 1;  // arithmetic shift: floor(n / 2)
+  q = __fmul2_rn(q, make_float2(__int_as_float((na1 + 127) << 23), __int_as_float((nb1 + 127) << 23)));
+  const float2 z =
+      __fmul2_rn(q, make_float2(__int_as_float((na - na1 + 127) << 23), __int_as_float((nb - nb1 + 127) << 23)));
+  // 1/(1+z), 1+z in [1, 2]: linear start, three Newton steps
+  const float2 d = __fadd2_rn(f2(1.0f), z);
+  const float2 dn = make_float2(-d.x, -d.y);
+  float2 rc = __ffma2_rn(f2(-0x1.e1e1e2p-2f), d, f2(0x1.69696ap+0f));
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const float2 e = __ffma2_rn(dn, rc, f2(1.0f));
+    rc = __ffma2_rn(rc, e, rc);
+  }
+  const float2 sigma = __fmul2_rn(make_float2(y.x >= 0.0f ? 1.0f : z.x, y.y >= 0.0f ? 1.0f : z.y), rc);
+  return __fmul2_rn(y, sigma);
 }
 
-__device__ __forceinline__ float silu_f32(float y) { return __fdiv_rn(y, __fadd_rn(1.0f, exp_f32(-y))); }
-
-// bf16 code of SiLU(sum_j w_j x_j) over W = 4 taps, oldest first.
-__device__ __forceinline__ uint16_t conv_silu_bf16(const float w[4], const float x[4]) {
-  float y = __fmul_rn(w[0], x[0]);
-  y = __fmaf_rn(w[1], x[1], y);
-  y = __fmaf_rn(w[2], x[2], y);
-  y = __fmaf_rn(w[3], x[3], y);
-  return f32_to_bf16(silu_f32(y));
+// bf16 codes of SiLU(sum_j w_j x_j) for two windows xa, xb of one channel
+// (W = 4 taps, oldest first): the low half holds a, the high half b.
+__device__ __forceinline__ uint32_t conv_silu_bf16x2(const float w[4], const float xa[4], const float xb[4]) {
+  float2 y = __fmul2_rn(f2(w[0]), make_float2(xa[0], xb[0]));
+  y = __ffma2_rn(f2(w[1]), make_float2(xa[1], xb[1]), y);
+  y = __ffma2_rn(f2(w[2]), make_float2(xa[2], xb[2]), y);
+  y = __ffma2_rn(f2(w[3]), make_float2(xa[3], xb[3]), y);
+  const float2 s = silu_f32x2(y);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(s.x, s.y);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 // ----------------------------------------------------------------------------

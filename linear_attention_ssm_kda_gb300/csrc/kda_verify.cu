@@ -16,26 +16,26 @@
 // never written.
 //
 // Schedule.  One persistent CTA per SM walks the (request, head) items
-// blockIdx.x + i * gridDim.x (local index i).  Two producer warps feed it
-// through mbarrier rings in shared memory:
-//   inputs (1 warp)    reads request metadata 32 items per round trip and
-//                      bulk-copies (TMA) each item's small inputs into a
-//                      ring: the 16-byte hulls of its activation and gate row
-//                      segments (rows may start anywhere), its conv taps,
-//                      conv weights and dt_bias;
-//   state (1 warp)     streams each live item's 64 KB fp32 state as eight row
-//                      chunks into a ring of chunk slots, so the HBM stream
-//                      runs ahead of the arithmetic by ~2.5 items;
-// and twelve compute warps take each item through three phases:
-//   conv   one channel per thread (3K = 384 threads): conv + SiLU (bf16,
-//          rounded from the exact value) of the window and the key record;
-//          the v-channel threads also evaluate the gates and the gate
-//          record; the rolled conv taps are written into the shared-memory
-//          copy of the item's conv state and leave by bulk stores (TMA);
-//   gates  one key channel per thread: norms and the closed-form operands
-//          X_t, Y_t, M, N (one warp reduce-scatter);
-//   gemv   eight warps, each on its own row chunk of the state: P | R, then
-//          the corrections and outputs of its rows.
+// blockIdx.x + i * gridDim.x (local index i) with four roles that meet only
+// at mbarrier rings in shared memory, so the three stages of consecutive
+// items overlap:
+//   inputs (1 warp)  reads request metadata 32 items per round trip and
+//                    bulk-copies (TMA) each item's small inputs into a ring:
+//                    the 16-byte hulls of its activation and gate row
+//                    segments (rows may start anywhere), its conv taps, conv
+//                    weights and dt_bias;
+//   state (1 warp)   streams each live item's 64 KB fp32 state as eight row
+//                    chunks into a ring of chunk slots, running ahead of the
+//                    arithmetic by two to three items;
+//   prep (4 warps)   one key channel per thread: conv + SiLU of its q, k and
+//                    v channels over the window (the bf16 codes, the key
+//                    record, the rolled conv taps, which leave by bulk
+//                    stores), the gates and gate record, the norms and the
+//                    closed-form operands X_t, Y_t, M, N, handed on through a
+//                    ring of operand slots;
+//   gemv (8 warps)   each on its own row chunk of the state: P | R with
+//                    packed fp32x2 FMAs, then the corrections and outputs of
+//                    its rows.
 // Every wait is bounded; a timeout sets KDA_DEVERR_TIMEOUT and an abort flag
 // that stops the other roles.
 #include <cuda_runtime.h>
@@ -47,13 +47,15 @@ namespace kda {
 namespace {
 
 constexpr int kConvWidth = 4;
-constexpr int kComputeWarps = 12;  // 3K channels of a K = 128 head, one per thread
-constexpr int kGemvWarps = 8;      // one state row chunk each
-constexpr int kGateWarps = 4;      // one key channel per thread (K = 128)
-constexpr int kThreads = 32 * (2 + kComputeWarps);
-constexpr int kComputeThreads = 32 * kComputeWarps;
-constexpr int kBarCompute = 1;
+constexpr int kPrepWarps = 6;  // two conv channels per thread, then one key channel per thread
+constexpr int kGemvWarps = 8;  // one state row chunk each
+constexpr int kPrepConvThreads = 32 * kPrepWarps;
+constexpr int kThreads = 32 * (2 + kPrepWarps + kGemvWarps);
+constexpr int kBarPrep = 1;
 constexpr int kSmemLimit = 227 * 1024;
+// misc ints in shared memory
+constexpr int kMiscAbort = 0;
+constexpr int kMiscPrepFail = 1;
 
 constexpr int ru(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -65,6 +67,14 @@ struct SmallMeta {
   int flags, bos, n, a;
   long long s, r;
   float A, pad;
+  float beta[QMAX];
+};
+
+// Prep -> gemv, per item (head of an operand slot).
+template <int QMAX>
+struct OpMeta {
+  int flags, bos, n, pad;
+  long long r;
   float beta[QMAX];
 };
 
@@ -83,29 +93,31 @@ struct Layout {
   static constexpr int kW = ru(kConv + 3 * KD * kLcMax * 2, 16);       // [3][KD][W] weights
   static constexpr int kDt = kW + 3 * KD * kConvWidth * 4;             // [KD] dt_bias
   static constexpr int kSmall = ru(kDt + KD * 4, 128);
-  // per-item scratch
-  static constexpr int kXs = 3 * QMAX * KD * 4;                        // [3][QMAX][KD] q | k | v
-  static constexpr int kVec = 2 * QMAX * KD * 4;                       // [2n][KD] X_t | Y_t
-  static constexpr int kEg = QMAX * KD * 4;                            // [QMAX][KD] e^g
-  static constexpr int kMN = ru(QMAX * QMAX * 4, 16);
+  // operand slot (prep -> gemv)
+  static constexpr int kOpVec = ru(int(sizeof(OpMeta<QMAX>)), 16);    // [2 QMAX][KD] X_t | Y_t
+  static constexpr int kOpV = kOpVec + 2 * QMAX * KD * 4;              // [QMAX][KD] v_t
+  static constexpr int kOpMN = kOpV + QMAX * KD * 4;                   // [QMAX][QMAX] M | N
+  static constexpr int kOp = ru(kOpMN + QMAX * QMAX * 4, 128);
+  static constexpr int kNumOp = 2;
+  // per-item scratch of the prep team
+  static constexpr int kXs = 2 * QMAX * KD * 4;                        // [2][QMAX][KD] q | k conv outputs
+  // per-warp scratch
   static constexpr int kRedPerWarp = 2 * QMAX * RW;                    // floats
-  static constexpr int kPart = ru(2 * QMAX + QMAX * QMAX, 32);         // reduced values per gate warp
-  static constexpr int kFixed = kNumSmall * kSmall + kXs + kVec + kEg + kMN + kGemvWarps * kRedPerWarp * 4 +
-                                kGateWarps * kPart * 4 + 32 + 2 * kNumSmall * 8;
+  static constexpr int kPart = ru(2 * QMAX + QMAX * QMAX, 32);         // reduced values per prep warp
+  static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kXs + kGemvWarps * kRedPerWarp * 4 +
+                                kPrepWarps * kPart * 4 + 32 + (2 * kNumSmall + 2 * kNumOp) * 8;
   static constexpr int kChunkFit = (kSmemLimit - kFixed - 64 * 2 * 8) / kChunk;
   static constexpr int kNumChunk = kChunkFit > 64 ? 64 : kChunkFit;
   // CTA layout
   static constexpr int oChunks = 0;
   static constexpr int oSmall = oChunks + kNumChunk * kChunk;
-  static constexpr int oXs = oSmall + kNumSmall * kSmall;
-  static constexpr int oVec = oXs + kXs;
-  static constexpr int oEg = oVec + kVec;
-  static constexpr int oMN = oEg + kEg;
-  static constexpr int oRed = oMN + kMN;
+  static constexpr int oOp = oSmall + kNumSmall * kSmall;
+  static constexpr int oXs = oOp + kNumOp * kOp;
+  static constexpr int oRed = oXs + kXs;
   static constexpr int oPart = oRed + kGemvWarps * kRedPerWarp * 4;
-  static constexpr int oMisc = oPart + kGateWarps * kPart * 4;  // int[8]: abort, compute ok, chunk failure
+  static constexpr int oMisc = oPart + kPrepWarps * kPart * 4;  // int[8]
   static constexpr int oBars = ru(oMisc + 32, 8);
-  static constexpr int kNumBars = 2 * kNumChunk + 2 * kNumSmall;
+  static constexpr int kNumBars = 2 * kNumChunk + 2 * kNumSmall + 2 * kNumOp;
   static constexpr int kBytes = oBars + kNumBars * 8;
   static_assert(kBytes <= kSmemLimit, "shared memory budget");
   static_assert(kNumChunk >= 2 * kGemvWarps, "at least two items of state in flight");
@@ -113,7 +125,7 @@ struct Layout {
 
 template <int KD, int QMAX>
 struct Bars {
-  uint64_t *ch_full, *ch_empty, *sm_full, *sm_empty;
+  uint64_t *ch_full, *ch_empty, *sm_full, *sm_empty, *op_full, *op_empty;
   __device__ explicit Bars(unsigned char* smem) {
     using Lay = Layout<KD, QMAX>;
     uint64_t* b = reinterpret_cast<uint64_t*>(smem + Lay::oBars);
@@ -121,6 +133,8 @@ struct Bars {
     ch_empty = b + Lay::kNumChunk;
     sm_full = b + 2 * Lay::kNumChunk;
     sm_empty = sm_full + Lay::kNumSmall;
+    op_full = sm_empty + Lay::kNumSmall;
+    op_empty = op_full + Lay::kNumOp;
   }
 };
 
@@ -360,7 +374,7 @@ __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int la
   }
 }
 
-// ---------------------------------------------------------------- compute
+// ---------------------------------------------------------------- prep team
 
 // One reduce-scatter stage over the lanes `mask` apart: each lane keeps the
 // half of its W values selected by its lane bit and adds the partner's copy.
@@ -374,186 +388,135 @@ __device__ __forceinline__ void reduce_scatter_stage(float* acc, int mask, bool 
   }
 }
 
-// Dot products of a warp's RW state rows with NCG operand vectors.  Lane =
-// 8 rs + kq covers rows 4i + rs (i < RW/4) and the float4 key chunks
-// 4kq + 32j (j < KD/32): a warp-wide LDS.128 reads 4 rows x 128 contiguous
-// bytes, and the 8 lanes of a row share a broadcast operand load.  The 8
-// partial sums of a row meet in a three-stage reduce-scatter.
-template <int KD, int NCG>
-__device__ __forceinline__ void gemv_chunk(const float* __restrict__ st, const float* __restrict__ vec,
-                                           float* __restrict__ red, int lane) {
-  constexpr int RW = KD / 8;
-  constexpr int R = RW / 4;
-  constexpr int J = KD / 32;
-  constexpr int NV = R * NCG;
-  constexpr int NVP = (NV + 7) / 8 * 8;
-  const int kq = lane & 7;
-  const int rs = lane >> 3;
-  float acc[NVP];
+// Conv + SiLU of channel k of group g (q | k | v) over the window: the bf16
+// codes of the n outputs, and the rolled taps written back into the slot's
+// copy of the conv state.
+template <int KD, int QMAX>
+__device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsigned char* sl, int g, int k, int n,
+                                             int a, int Lc, uint32_t act_lo, uint16_t (&y)[QMAX]) {
+  using Lay = Layout<KD, QMAX>;
+  uint16_t* conv = reinterpret_cast<uint16_t*>(const_cast<unsigned char*>(sl) + Lay::kConv);
+  float w[kConvWidth];
+  if (p.conv_weight_fp32) {
+    const float4 wv = reinterpret_cast<const float4*>(sl + Lay::kW)[g * KD + k];
+    w[0] = wv.x; w[1] = wv.y; w[2] = wv.z; w[3] = wv.w;
+  } else {
+    const uint2 wv = reinterpret_cast<const uint2*>(sl + Lay::kW)[g * KD + k];
+    w[0] = bf16_to_f32(wv.x & 0xffff); w[1] = bf16_to_f32(wv.x >> 16);
+    w[2] = bf16_to_f32(wv.y & 0xffff); w[3] = bf16_to_f32(wv.y >> 16);
+  }
+  uint16_t seq[kConvWidth - 1 + QMAX + 1];
+  seq[kConvWidth - 1 + QMAX] = 0;
 #pragma unroll
-  for (int i = 0; i < NVP; ++i) acc[i] = 0.0f;
-#pragma unroll 2
-  for (int j = 0; j < J; ++j) {
-    const int kk = 4 * kq + 32 * j;
-    float4 vv[NCG];
+  for (int j = 0; j < kConvWidth - 1; ++j)
+    seq[j] = p.conv_dim_first ? conv[(g * KD + k) * Lc + a - 1 + j] : conv[((a - 1 + j) * 3 + g) * KD + k];
 #pragma unroll
-    for (int c = 0; c < NCG; ++c) vv[c] = *reinterpret_cast<const float4*>(vec + c * KD + kk);
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const float4 sv = *reinterpret_cast<const float4*>(st + (4 * i + rs) * KD + kk);
-#pragma unroll
-      for (int c = 0; c < NCG; ++c) {
-        float x = acc[i * NCG + c];
-        x = fmaf(sv.x, vv[c].x, x);
-        x = fmaf(sv.y, vv[c].y, x);
-        x = fmaf(sv.z, vv[c].z, x);
-        x = fmaf(sv.w, vv[c].w, x);
-        acc[i * NCG + c] = x;
-      }
+  for (int t = 0; t < QMAX; ++t) {
+    seq[kConvWidth - 1 + t] = 0;
+    if (t < n) {
+      // the activation hull of (token t, group g) starts act_lo + 16-byte
+      // multiples before the segment: the segment's offset is its address mod 16
+      const uint32_t off = (act_lo + static_cast<uint32_t>(t) * static_cast<uint32_t>(p.qkv_stride) * 2u +
+                            static_cast<uint32_t>(g) * static_cast<uint32_t>(p.H) * KD * 2u) & 15u;
+      seq[kConvWidth - 1 + t] =
+          *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + (t * 3 + g) * Lay::kSeg + off + 2 * k);
     }
   }
-  reduce_scatter_stage<NVP>(acc, 4, (kq & 4) != 0);
-  reduce_scatter_stage<NVP / 2>(acc, 2, (kq & 2) != 0);
-  reduce_scatter_stage<NVP / 4>(acc, 1, (kq & 1) != 0);
 #pragma unroll
-  for (int i = 0; i < NVP / 8; ++i) {
-    const int v = (NVP / 8) * kq + i;
-    if (v < NV) {
-      const int row = v / NCG;
-      const int c = v - row * NCG;
-      red[c * RW + 4 * row + rs] = acc[i];
+  for (int t = 0; t < QMAX; t += 2) {  // token pairs on the packed fp32x2 unit
+    y[t] = y[t + 1] = 0;
+    if (t < n) {
+      const float xa[kConvWidth] = {bf16_to_f32(seq[t]), bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]),
+                                    bf16_to_f32(seq[t + 3])};
+      const float xb[kConvWidth] = {bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]), bf16_to_f32(seq[t + 3]),
+                                    bf16_to_f32(seq[t + 4])};
+      const uint32_t yy = conv_silu_bf16x2(w, xa, xb);
+      y[t] = static_cast<uint16_t>(yy & 0xffffu);
+      if (t + 1 < n) y[t + 1] = static_cast<uint16_t>(yy >> 16);
+    }
+  }
+  // rolled conv state: taps 0 .. W-3+n <- seq[1 .. W-2+n]
+#pragma unroll
+  for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
+    if (j < kConvWidth - 2 + n) {
+      if (p.conv_dim_first)
+        conv[(g * KD + k) * Lc + j] = seq[j + 1];
+      else
+        conv[(j * 3 + g) * KD + k] = seq[j + 1];
     }
   }
 }
 
 template <int KD, int QMAX>
-__device__ void compute(const VerifyParams& p, unsigned char* smem, int ct, volatile int* abort_flag) {
+__device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatile int* misc) {
   using Lay = Layout<KD, QMAX>;
-  constexpr int RW = Lay::RW;
   constexpr int NREDP = Lay::kPart;  // |q_t|^2, |k_t|^2, raw M / N grid, padded to 32
   constexpr int PER = NREDP / 32;
   Bars<KD, QMAX> bars(smem);
-  volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::oMisc);
-  float* xs = reinterpret_cast<float*>(smem + Lay::oXs);    // [3][QMAX][KD]
-  float* vec = reinterpret_cast<float*>(smem + Lay::oVec);  // [2n][KD]
-  float* mn = reinterpret_cast<float*>(smem + Lay::oMN);    // [QMAX][QMAX]
+  volatile int* abort_flag = misc + kMiscAbort;
   float* part = reinterpret_cast<float*>(smem + Lay::oPart);
-  const int warp = ct >> 5;
-  const int lane = ct & 31;
-  float* red = reinterpret_cast<float*>(smem + Lay::oRed) + warp * Lay::kRedPerWarp;
+  float* xs = reinterpret_cast<float*>(smem + Lay::oXs);  // [2][QMAX][KD] q | k
+  const int warp = pt >> 5;
+  const int lane = pt & 31;
   const int nloc = local_items(p.B * p.H);
   const long long HK = static_cast<long long>(p.H) * KD;
   const int Lc = p.Q + kConvWidth - 2;
   const uint32_t qkv_lo = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.mixed_qkv));
   const uint32_t gate_lo = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.raw_gate));
-  const uint32_t hk2 = static_cast<uint32_t>(HK) * 2u;
-  uint32_t live = 0;
-  bool alive = true;
   for (int i = 0; i < nloc; ++i) {
     const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
     const int h = it - (it / p.H) * p.H;
     const int slot = i % Lay::kNumSmall;
-    const uint32_t ph = (i / Lay::kNumSmall) & 1;
-    const unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
-    if (ct == 0) misc[1] = mbar_wait_or_abort(&bars.sm_full[slot], ph, abort_flag) ? 1 : 0;
-    named_barrier(kBarCompute, kComputeThreads);
-    if (!misc[1]) {
-      alive = false;
-      break;
-    }
-    if (ct != 0) mbar_acquire_seen(&bars.sm_full[slot], ph);
+    const int oslot = i % Lay::kNumOp;
+    unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
+    unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
+    const bool ok = warp_wait(&bars.sm_full[slot], (i / Lay::kNumSmall) & 1, lane, abort_flag) &&
+                    warp_wait(&bars.op_empty[oslot], ((i / Lay::kNumOp) & 1) ^ 1, lane, abort_flag);
+    if (!ok && lane == 0) misc[kMiscPrepFail] = 1;
     const SmallMeta<QMAX> m = *reinterpret_cast<const SmallMeta<QMAX>*>(sl);
+    const bool live = ok && (m.flags & kLive);
     const int n = m.n;
-    const int bos = m.bos;
     const uint32_t hoff = static_cast<uint32_t>(h) * KD * 2u;
-    if (!(m.flags & kLive)) {
-      if (m.flags & kNull) {  // null slot: zero outputs, nothing else
-        for (int e = ct; e < n * KD; e += kComputeThreads) {
-          const int t = e / KD;
-          p.out[static_cast<long long>(bos + t) * p.out_stride + static_cast<long long>(h) * KD + (e - t * KD)] = 0;
-        }
-      }
-      named_barrier(kBarCompute, kComputeThreads);
-      if (ct == 0) mbar_arrive(&bars.sm_empty[slot]);
-      continue;
-    }
     uint16_t* kg = p.key_gate + m.r * p.kg_stride + static_cast<long long>(h) * p.Q * 2 * KD;
 
-    // ---- conv: thread ct owns channel k of group g (q | k | v) ----
-    if (ct < 3 * KD) {
-      const int g = ct / KD;
-      const int k = ct - g * KD;
-      uint16_t* conv = reinterpret_cast<uint16_t*>(const_cast<unsigned char*>(sl) + Lay::kConv);
-      float w[kConvWidth];
-      if (p.conv_weight_fp32) {
-        const float4 wv = reinterpret_cast<const float4*>(sl + Lay::kW)[g * KD + k];
-        w[0] = wv.x; w[1] = wv.y; w[2] = wv.z; w[3] = wv.w;
-      } else {
-        const uint2 wv = reinterpret_cast<const uint2*>(sl + Lay::kW)[g * KD + k];
-        w[0] = bf16_to_f32(wv.x & 0xffff); w[1] = bf16_to_f32(wv.x >> 16);
-        w[2] = bf16_to_f32(wv.y & 0xffff); w[3] = bf16_to_f32(wv.y >> 16);
-      }
-      uint16_t seq[kConvWidth - 1 + QMAX + 1];
-#pragma unroll
-      for (int j = 0; j < kConvWidth - 1; ++j)
-        seq[j] = p.conv_dim_first ? conv[(g * KD + k) * Lc + m.a - 1 + j] : conv[((m.a - 1 + j) * 3 + g) * KD + k];
-#pragma unroll
-      for (int t = 0; t < QMAX + 1; ++t) {
-        seq[kConvWidth - 1 + t] = 0;
-        if (t < n) {
-          const uint32_t off =
-              (qkv_lo + static_cast<uint32_t>(bos + t) * static_cast<uint32_t>(p.qkv_stride) * 2u + g * hk2 + hoff) &
-              15u;
-          seq[kConvWidth - 1 + t] =
-              *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + (t * 3 + g) * Lay::kSeg + off + 2 * k);
-        }
-      }
-      float* xg = xs + g * QMAX * KD;
-#pragma unroll
-      for (int t = 0; t < QMAX; t += 2) {  // tokens in pairs: two independent chains
-        if (t < n) {
-          const float x0[kConvWidth] = {bf16_to_f32(seq[t]), bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]),
-                                        bf16_to_f32(seq[t + 3])};
-          const float x1[kConvWidth] = {bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]), bf16_to_f32(seq[t + 3]),
-                                        bf16_to_f32(seq[t + 4])};
-          const uint16_t y0 = conv_silu_bf16(w, x0);
-          const uint16_t y1 = conv_silu_bf16(w, x1);
-          xg[t * KD + k] = bf16_to_f32(y0);
-          if (g == 1) kg[t * 2 * KD + k] = y0;  // key record: the bf16 conv output
-          if (t + 1 < n && t + 1 < QMAX) {
-            xg[(t + 1) * KD + k] = bf16_to_f32(y1);
-            if (g == 1) kg[(t + 1) * 2 * KD + k] = y1;
-          }
-        }
-      }
-      // rolled conv state, into the slot's copy: taps 0 .. W-3+n <- seq[1 .. W-2+n]
-#pragma unroll
-      for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
-        if (j < kConvWidth - 2 + n) {
-          if (p.conv_dim_first)
-            conv[(g * KD + k) * Lc + j] = seq[j + 1];
-          else
-            conv[(j * 3 + g) * KD + k] = seq[j + 1];
-        }
-      }
-      if (g == 2) {  // gates and the gate record, on the v-channel threads
-        const float dtb = reinterpret_cast<const float*>(sl + Lay::kDt)[k];
-        float* egs = reinterpret_cast<float*>(smem + Lay::oEg);
-#pragma unroll
-        for (int t = 0; t < QMAX; ++t) {
-          if (t < n) {
-            const uint32_t goff =
-                (gate_lo + static_cast<uint32_t>(bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
-            const uint16_t rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
-            kg[t * 2 * KD + KD + k] = rg;  // gate record: bit copy
-            egs[t * KD + k] = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
-          }
-        }
+    // ---- conv: channels pt and pt + 192 of the head's 3K (q | k | v) ----
+    if (ok && (m.flags & kNull)) {  // null slot: zero outputs, nothing else
+      for (int e = pt; e < n * KD; e += kPrepConvThreads) {
+        const int t = e / KD;
+        p.out[static_cast<long long>(m.bos + t) * p.out_stride + static_cast<long long>(h) * KD + (e - t * KD)] = 0;
       }
     }
-    fence_async_shared();
-    named_barrier(kBarCompute, kComputeThreads);
-    if (ct == 0) {  // the rolled conv state leaves by bulk stores from the slot
+    if (live) {
+      const uint32_t act_lo = qkv_lo + static_cast<uint32_t>(m.bos) * static_cast<uint32_t>(p.qkv_stride) * 2u + hoff;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = pt + cc * kPrepConvThreads;
+        if (c < 3 * KD) {
+          const int g = c / KD;
+          const int k = c - g * KD;
+          uint16_t y[QMAX];
+          conv_channel<KD, QMAX>(p, sl, g, k, n, m.a, Lc, act_lo, y);
+          if (g < 2) {
+#pragma unroll
+            for (int t = 0; t < QMAX; ++t) xs[(g * QMAX + t) * KD + k] = bf16_to_f32(y[t]);
+            if (g == 1) {
+#pragma unroll
+              for (int t = 0; t < QMAX; ++t)
+                if (t < n) kg[t * 2 * KD + k] = y[t];  // key record: the bf16 conv output
+            }
+          } else {
+            float* opv = reinterpret_cast<float*>(op + Lay::kOpV);
+#pragma unroll
+            for (int t = 0; t < QMAX; ++t)
+              if (t < n) opv[t * KD + k] = bf16_to_f32(y[t]);
+          }
+        }
+      }
+      fence_async_shared();  // the rolled taps leave by bulk stores
+    }
+    named_barrier(kBarPrep, kPrepConvThreads);
+    if (misc[kMiscPrepFail]) break;  // every prep thread sees the same flag here
+    if (live && pt == 0) {  // the rolled conv state leaves by bulk stores from the slot
       uint16_t* cs = p.conv_state + m.s * p.conv_slot_stride;
       if (p.conv_dim_first) {
 #pragma unroll
@@ -569,22 +532,29 @@ __device__ void compute(const VerifyParams& p, unsigned char* smem, int ct, vola
       bulk_commit();
     }
 
-    // ---- gates, gate record, norms and closed-form scalars: key channel k = ct ----
+    // ---- gates, gate record and the per-channel partial sums: key channel k = pt ----
     float qv[QMAX], kv[QMAX], eg[QMAX];
-    if (ct < KD) {
-      const int k = ct;
-      const float* egs = reinterpret_cast<const float*>(smem + Lay::oEg);
+    if (live && pt < KD) {
+      const int k = pt;
+      const float dtb = reinterpret_cast<const float*>(sl + Lay::kDt)[k];
 #pragma unroll
       for (int t = 0; t < QMAX; ++t) {
-        qv[t] = kv[t] = eg[t] = 0.0f;
+        qv[t] = xs[t * KD + k];
+        kv[t] = xs[(QMAX + t) * KD + k];
+        eg[t] = 0.0f;
         if (t < n) {
-          qv[t] = xs[t * KD + k];
-          kv[t] = xs[QMAX * KD + t * KD + k];
-          eg[t] = egs[t * KD + k];
+          const uint32_t goff =
+              (gate_lo + static_cast<uint32_t>(m.bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
+          const uint16_t rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
+          kg[t * 2 * KD + KD + k] = rg;  // gate record: bit copy
+          eg[t] = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
+        } else {
+          qv[t] = 0.0f;
+          kv[t] = 0.0f;
         }
       }
       // vals: [t] |q_t|^2, [QMAX + t] |k_t|^2, [2QMAX + t QMAX + u] k_u D_{u+1..t} k_t (u < t),
-      //       [2QMAX + u QMAX + t] k_u D_{u+1..t} q_t (u <= t); zero past n.
+      //       [2QMAX + u QMAX + t] k_u D_{u+1..t} q_t (u <= t); zero past n (qv = kv = 0 there).
       float vals[NREDP];
 #pragma unroll
       for (int v = 0; v < NREDP; ++v) vals[v] = 0.0f;
@@ -613,8 +583,12 @@ __device__ void compute(const VerifyParams& p, unsigned char* smem, int ct, vola
 #pragma unroll
       for (int v = 0; v < PER; ++v) part[warp * NREDP + lane * PER + v] = vals[v];
     }
-    named_barrier(kBarCompute, kComputeThreads);
-    if (ct < KD) {
+    named_barrier(kBarPrep, kPrepConvThreads);
+
+    // ---- norms, the operands X_t = D_t k^_t, Y_t = D_t q^_t, M and N ----
+    if (live && pt < KD) {
+      float* vec = reinterpret_cast<float*>(op + Lay::kOpVec);
+      float* mn = reinterpret_cast<float*>(op + Lay::kOpMN);
       float rq[QMAX], rk[QMAX];
 #pragma unroll
       for (int t = 0; t < QMAX; ++t) {
@@ -632,15 +606,15 @@ __device__ void compute(const VerifyParams& p, unsigned char* smem, int ct, vola
       for (int t = 0; t < QMAX; ++t) {
         if (t < n) {
           D *= eg[t];
-          vec[t * KD + ct] = D * (kv[t] * rk[t]);        // X_t = D_t k^_t
-          vec[(n + t) * KD + ct] = D * (qv[t] * rq[t]);  // Y_t = D_t q^_t
+          vec[t * KD + pt] = D * (kv[t] * rk[t]);        // X_t
+          vec[(n + t) * KD + pt] = D * (qv[t] * rq[t]);  // Y_t
         }
       }
-      if (ct < QMAX * QMAX) {
-        const int i2 = ct / QMAX, j2 = ct - (ct / QMAX) * QMAX;
+      if (pt < QMAX * QMAX) {
+        const int i2 = pt / QMAX, j2 = pt - (pt / QMAX) * QMAX;
         float raw = 0.0f;
 #pragma unroll
-        for (int w = 0; w < KD / 32; ++w) raw += part[w * NREDP + 2 * QMAX + ct];
+        for (int w = 0; w < KD / 32; ++w) raw += part[w * NREDP + 2 * QMAX + pt];
         // i2 > j2: M = raw rk_j rk_i (t = i2, u = j2); i2 <= j2: N = raw rk_i rq_j (u = i2, t = j2)
         float ri = 0.0f, rj = 0.0f;
 #pragma unroll
@@ -648,67 +622,155 @@ __device__ void compute(const VerifyParams& p, unsigned char* smem, int ct, vola
           if (t == i2) ri = rk[t];
           if (t == j2) rj = (i2 > j2) ? rk[t] : rq[t];
         }
-        mn[ct] = raw * ri * rj;
+        mn[pt] = raw * ri * rj;
       }
     }
-    named_barrier(kBarCompute, kComputeThreads);
-    if (ct == 0) {  // the small inputs are consumed once the bulk stores have read them
-      bulk_wait_read();
+    if (pt == 0) {
+      OpMeta<QMAX>* om = reinterpret_cast<OpMeta<QMAX>*>(op);
+      om->flags = live ? kLive : 0;
+      om->bos = m.bos;
+      om->n = n;
+      om->pad = 0;
+      om->r = m.r;
+#pragma unroll
+      for (int t = 0; t < QMAX; ++t) om->beta[t] = m.beta[t];
+    }
+    named_barrier(kBarPrep, kPrepConvThreads);
+    if (pt == 0) {
+      mbar_arrive(&bars.op_full[oslot]);
+      bulk_wait_read();  // the small inputs are consumed once the bulk stores have read them
       mbar_arrive(&bars.sm_empty[slot]);
     }
+  }
+  if (pt == 0) bulk_wait_all();
+  if (misc[kMiscPrepFail] && pt == 0) {
+    report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
+    *abort_flag = 1;
+  }
+}
 
-    // ---- gemv on the warp's row chunk, then its rows' corrections and outputs ----
-    if (warp < kGemvWarps) {
-      const uint32_t pc = live * kGemvWarps + warp;
-      const int pos = pc % Lay::kNumChunk;
-      const uint32_t cph = (pc / Lay::kNumChunk) & 1;
-      if (warp_wait(&bars.ch_full[pos], cph, lane, abort_flag)) {
-        const float* st = reinterpret_cast<const float*>(smem + Lay::oChunks + pos * Lay::kChunk);
-        for (int cg = 0; cg < 2 * n; cg += 8) {
-          switch (min(8, 2 * n - cg)) {
-            case 2: gemv_chunk<KD, 2>(st, vec + cg * KD, red + cg * RW, lane); break;
-            case 4: gemv_chunk<KD, 4>(st, vec + cg * KD, red + cg * RW, lane); break;
-            case 6: gemv_chunk<KD, 6>(st, vec + cg * KD, red + cg * RW, lane); break;
-            default: gemv_chunk<KD, 8>(st, vec + cg * KD, red + cg * RW, lane); break;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-        if (lane < RW) {
-          const int row = warp * RW + lane;
-          float* corr = p.corr + m.r * p.corr_stride + static_cast<long long>(h) * p.Q * KD;
-          const float* xv = xs + 2 * QMAX * KD;
-          float cv[QMAX];
+// ---------------------------------------------------------------- gemv team
+
+// Dot products of a warp's RW state rows with NCG operand vectors.  Lane =
+// 4 rs + kq: four lanes share a row and split its K; a lane covers rows
+// rs + 8i (i < RW/8) and, at step j, the float4 key chunk 4 (j ^ (rs & 1)) + kq.
+// The xor sends rows of odd rs to the other 64-byte half of the 128-byte bank
+// window, so a warp-wide LDS.128 of 8 rows x 64 bytes is conflict-free, and
+// the operand loads stay at 8 distinct float4 (one wavefront).  Each dot
+// product runs as two interleaved halves in one packed fp32x2 FMA chain
+// (elements x, y and z, w of each float4); the halves are added, and the 4
+// partial sums of a row meet in a two-stage reduce-scatter.
+template <int KD, int NCG>
+__device__ __forceinline__ void gemv_chunk(const float* __restrict__ st, const float* __restrict__ vec,
+                                           float* __restrict__ red, int lane) {
+  constexpr int RW = KD / 8;
+  constexpr int R = RW / 8;   // rows per lane
+  constexpr int J = KD / 16;  // float4 chunks per lane and row
+  constexpr int NV = R * NCG;
+  constexpr int NVP = (NV + 3) / 4 * 4;
+  const int kq = lane & 3;
+  const int rs = lane >> 2;
+  const int flip = rs & 1;
+  float2 acc2[NV];
 #pragma unroll
-          for (int t = 0; t < QMAX; ++t) {
-            if (t < n) {
-              float x = xv[t * KD + row] - red[t * RW + lane];
+  for (int i = 0; i < NV; ++i) acc2[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-              for (int u = 0; u < t; ++u) x = fmaf(-mn[t * QMAX + u], cv[u], x);
-              const float c = x * m.beta[t];
-              cv[t] = c;
-              float o = red[(n + t) * RW + lane];
+  for (int j = 0; j < J; ++j) {
+    const int kk = 4 * (4 * (j ^ flip) + kq);
+    float4 vv[NCG];
 #pragma unroll
-              for (int u = 0; u <= t; ++u) o = fmaf(mn[u * QMAX + t], cv[u], o);
-              corr[t * KD + row] = c;
-              p.out[static_cast<long long>(bos + t) * p.out_stride + static_cast<long long>(h) * KD + row] =
-                  f32_to_bf16(o);
-            }
-          }
-        }
-      } else if (lane == 0) {
-        misc[2] = 1;
+    for (int c = 0; c < NCG; ++c) vv[c] = *reinterpret_cast<const float4*>(vec + c * KD + kk);
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const float4 sv = *reinterpret_cast<const float4*>(st + (rs + 8 * i) * KD + kk);
+#pragma unroll
+      for (int c = 0; c < NCG; ++c) {
+        acc2[i * NCG + c] = __ffma2_rn(make_float2(sv.x, sv.y), make_float2(vv[c].x, vv[c].y), acc2[i * NCG + c]);
+        acc2[i * NCG + c] = __ffma2_rn(make_float2(sv.z, sv.w), make_float2(vv[c].z, vv[c].w), acc2[i * NCG + c]);
       }
     }
-    ++live;
-    named_barrier(kBarCompute, kComputeThreads);
-    if (misc[2]) {
-      alive = false;
-      break;
+  }
+  float acc[NVP];
+#pragma unroll
+  for (int i = 0; i < NVP; ++i) acc[i] = i < NV ? acc2[i].x + acc2[i].y : 0.0f;
+  reduce_scatter_stage<NVP>(acc, 2, (kq & 2) != 0);
+  reduce_scatter_stage<NVP / 2>(acc, 1, (kq & 1) != 0);
+#pragma unroll
+  for (int i = 0; i < NVP / 4; ++i) {
+    const int v = (NVP / 4) * kq + i;
+    if (v < NV) {
+      const int row = v / NCG;
+      const int c = v - row * NCG;
+      red[c * RW + rs + 8 * row] = acc[i];
     }
   }
-  if (ct == 0) bulk_wait_all();
-  if (!alive && ct == 0) {
+}
+
+template <int KD, int QMAX>
+__device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, int lane, volatile int* misc) {
+  using Lay = Layout<KD, QMAX>;
+  constexpr int RW = Lay::RW;
+  Bars<KD, QMAX> bars(smem);
+  volatile int* abort_flag = misc + kMiscAbort;
+  float* red = reinterpret_cast<float*>(smem + Lay::oRed) + gw * Lay::kRedPerWarp;
+  const int nloc = local_items(p.B * p.H);
+  uint32_t live = 0;
+  bool ok = true;
+  for (int i = 0; i < nloc && ok; ++i) {
+    const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    const int h = it - (it / p.H) * p.H;
+    const int oslot = i % Lay::kNumOp;
+    ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag);
+    if (!ok) break;
+    const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
+    const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op);
+    if (m.flags & kLive) {
+      const int n = m.n;
+      const uint32_t pc = live * kGemvWarps + gw;
+      const int pos = pc % Lay::kNumChunk;
+      ok = warp_wait(&bars.ch_full[pos], (pc / Lay::kNumChunk) & 1, lane, abort_flag);
+      if (!ok) break;
+      const float* st = reinterpret_cast<const float*>(smem + Lay::oChunks + pos * Lay::kChunk);
+      const float* vec = reinterpret_cast<const float*>(op + Lay::kOpVec);
+      for (int cg = 0; cg < 2 * n; cg += 8) {
+        switch (min(8, 2 * n - cg)) {
+          case 2: gemv_chunk<KD, 2>(st, vec + cg * KD, red + cg * RW, lane); break;
+          case 4: gemv_chunk<KD, 4>(st, vec + cg * KD, red + cg * RW, lane); break;
+          case 6: gemv_chunk<KD, 6>(st, vec + cg * KD, red + cg * RW, lane); break;
+          default: gemv_chunk<KD, 8>(st, vec + cg * KD, red + cg * RW, lane); break;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
+      if (lane < RW) {
+        const int row = gw * RW + lane;
+        const float* mn = reinterpret_cast<const float*>(op + Lay::kOpMN);
+        const float* xv = reinterpret_cast<const float*>(op + Lay::kOpV);
+        float* corr = p.corr + m.r * p.corr_stride + static_cast<long long>(h) * p.Q * KD;
+        float cv[QMAX];
+#pragma unroll
+        for (int t = 0; t < QMAX; ++t) {
+          if (t < n) {
+            float x = xv[t * KD + row] - red[t * RW + lane];
+#pragma unroll
+            for (int u = 0; u < t; ++u) x = fmaf(-mn[t * QMAX + u], cv[u], x);
+            const float c = x * m.beta[t];
+            cv[t] = c;
+            float o = red[(n + t) * RW + lane];
+#pragma unroll
+            for (int u = 0; u <= t; ++u) o = fmaf(mn[u * QMAX + t], cv[u], o);
+            corr[t * KD + row] = c;
+            p.out[static_cast<long long>(m.bos + t) * p.out_stride + static_cast<long long>(h) * KD + row] =
+                f32_to_bf16(o);
+          }
+        }
+      }
+      ++live;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
+  }
+  if (!ok && lane == 0) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
   }
@@ -731,16 +793,22 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VerifyParams 
       mbar_init(&bars.sm_full[i], 1);
       mbar_init(&bars.sm_empty[i], 1);
     }
+    for (int i = 0; i < Lay::kNumOp; ++i) {
+      mbar_init(&bars.op_full[i], 1);
+      mbar_init(&bars.op_empty[i], kGemvWarps);
+    }
     for (int i = 0; i < 8; ++i) misc[i] = 0;
     fence_barrier_init();
   }
   __syncthreads();
   if (warp == 0) {
-    produce_inputs<KD, QMAX>(p, smem, tid & 31, misc);
+    produce_inputs<KD, QMAX>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp == 1) {
-    produce_state<KD, QMAX>(p, smem, tid & 31, misc);
+    produce_state<KD, QMAX>(p, smem, tid & 31, misc + kMiscAbort);
+  } else if (warp < 2 + kPrepWarps) {
+    prep<KD, QMAX>(p, smem, tid - 64, misc);
   } else {
-    compute<KD, QMAX>(p, smem, tid - 64, misc);
+    gemv_team<KD, QMAX>(p, smem, warp - 2 - kPrepWarps, tid & 31, misc);
   }
 }
 

@@ -103,7 +103,7 @@ def _load():
             lib.kda_oracle_bf16_round.restype = ctypes.c_uint16
             lib.kda_oracle_gate.argtypes = [ctypes.c_double] * 3 + [ctypes.c_int, ctypes.c_double]
             lib.kda_oracle_gate.restype = ctypes.c_double
-            for fn in (lib.kda_oracle_exp_f32, lib.kda_oracle_silu_f32):
+            for fn in (lib.kda_oracle_exp_neg_f32, lib.kda_oracle_silu_f32):
                 fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
                 fn.restype = None
             lib.kda_oracle_conv_silu_bf16_f32.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_int]
@@ -137,16 +137,16 @@ def gate(raw_g: float, dt_bias: float, A: float, lower_bound: float | None = Non
     return float(_load().kda_oracle_gate(raw_g, dt_bias, A, int(use_lb), float(lower_bound or 0.0)))
 
 
-def exp_f32(x) -> np.ndarray:
-    """The specified fp32 e^x of the convolution's SiLU, elementwise."""
+def exp_neg_f32(x) -> np.ndarray:
+    """The specified fp32 e^x (x <= 0) of the convolution's SiLU, elementwise."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     y = np.empty_like(x)
-    _load().kda_oracle_exp_f32(x.ctypes.data, y.ctypes.data, x.size)
+    _load().kda_oracle_exp_neg_f32(x.ctypes.data, y.ctypes.data, x.size)
     return y
 
 
 def silu_f32(x) -> np.ndarray:
-    """The specified fp32 SiLU y / (1 + exp_f32(-y)), elementwise."""
+    """The specified fp32 SiLU y sigma(y), elementwise."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     y = np.empty_like(x)
     _load().kda_oracle_silu_f32(x.ctypes.data, y.ctypes.data, x.size)

@@ -31,12 +31,13 @@
  * SiLU in fp32 and then casts to bf16, without fixing the order of the sums or
  * the exp routine.  So the oracle takes that decision in fp32 with a fully
  * specified procedure (conv_silu_bf16_f32 below): the taps are summed oldest
- * first, y = w0 x0, then y = fma(wj, xj, y); SiLU is y / (1 + exp_f32(-y))
- * with IEEE fp32 add and divide; exp_f32 is Cody-Waite argument reduction by
- * ln 2 (split in a 15-bit head and a tail) with a degree-7 Taylor polynomial
- * in Horner form and an exact scaling by 2^n; the result is rounded to bf16,
- * nearest even.  Every step is an IEEE-754 basic operation, so any conforming
- * implementation gets the same bits.  The pins check it against the exact
+ * first, y = w0 x0, then y = fma(wj, xj, y); SiLU is y sigma(y) with
+ * sigma(y) = 1/(1+z) or z/(1+z) by the sign of y and z = e^-|y| (Cody-Waite
+ * reduction by ln 2, split in a 15-bit head and a tail, and a degree-7 Taylor
+ * polynomial), the reciprocal of 1+z in [1, 2] by three Newton steps from a
+ * linear start; the result is rounded to bf16, nearest even.  Every step is
+ * an IEEE-754 fp32 add, multiply or fma, or integer arithmetic on the bits,
+ * so any conforming implementation gets the same bits.  The pins check it against the exact
  * double-precision value (within a few fp32 ulp), so it is an accurate fp32
  * evaluation and not merely a self-consistent one.
  *
@@ -110,19 +111,28 @@ static float f32_from_bits(uint32_t w) {
     return f;
 }
 
-/* e^x in fp32: x is clamped to [-104, 89] (e^-104 rounds to 0 and e^89
- * overflows, so the clamp changes no finite result); n = rint(x log2 e);
- * r = x - n ln2 with ln2 = LN2_HI + LN2_LO (LN2_HI has 15 significant bits,
- * so n LN2_HI is exact and each fma rounds once); e^r by the Taylor series
- * to r^7/7! (|r| <= 0.347: truncation below 1e-8 relative); then
- * e^x = e^r 2^n1 2^n2 with n1 = floor(n/2), n2 = n - n1, both in the normal
- * range, so the first scaling is exact and the second rounds once. */
-static float exp_f32(float x) {
+/* e^x in fp32 for x <= 0: x is clamped below at -104 (e^-104 rounds to 0,
+ * so the clamp changes no result); n = round-to-nearest-even of x log2 e,
+ * taken from the exact product by adding 1.5 * 2^23 in one fma (the sum's
+ * ulp is 1, so the rounding lands on an integer and the low mantissa bits
+ * hold n); r = x - n ln2 with ln2 = LN2_HI + LN2_LO (LN2_HI has 15
+ * significant bits, so n LN2_HI is exact and each fma rounds once); e^r by
+ * the Taylor series to r^7/7! in Horner form (|r| <= 0.347: truncation below
+ * 1e-8 relative); then e^x = e^r 2^n1 2^n2 with n1 = floor(n/2) and
+ * n2 = n - n1, both >= -75, so the first scaling is exact and the second
+ * rounds once (into the subnormal range when n < -126). */
+static float exp_neg_f32(float x) {
     const float LOG2E = 0x1.715476p+0f;
+    const float SHIFTER = 0x1.8p+23f; /* 1.5 * 2^23 */
     const float LN2_HI = 0x1.62e4p-1f;
     const float LN2_LO = 0x1.7f7d1cp-20f;
-    x = fminf(fmaxf(x, -104.0f), 89.0f);
-    const float nf = rintf(x * LOG2E);
+    x = fmaxf(x, -104.0f);
+    const float t = fmaf(x, LOG2E, SHIFTER);
+    const float nf = t - SHIFTER;
+    uint32_t tb, sb;
+    memcpy(&tb, &t, sizeof tb);
+    memcpy(&sb, &SHIFTER, sizeof sb);
+    const int n = (int)((int64_t)tb - (int64_t)sb);
     float r = fmaf(-nf, LN2_HI, x);
     r = fmaf(-nf, LN2_LO, r);
     /* 1/k! rounded to fp32, k = 7 .. 2 */
@@ -134,15 +144,32 @@ static float exp_f32(float x) {
     p = fmaf(p, r, 0.5f);
     p = fmaf(p, r, 1.0f);
     p = fmaf(p, r, 1.0f);
-    const int n = (int)nf;
     const int n1 = n >= 0 ? n / 2 : -((1 - n) / 2); /* floor(n / 2) */
     const int n2 = n - n1;
     p = p * f32_from_bits((uint32_t)(n1 + 127) << 23);
     return p * f32_from_bits((uint32_t)(n2 + 127) << 23);
 }
 
-/* SiLU in fp32: y / (1 + e^-y), IEEE add and divide. */
-static float silu_f32(float y) { return y / (1.0f + exp_f32(-y)); }
+/* 1/d for d in [1, 2]: r0 = 24/17 - (8/17) d (relative error at most 1/17),
+ * then three Newton steps e = 1 - d r, r = r + r e, each two fmas; the error
+ * squares each step, so only the fp32 rounding of the last step remains. */
+static float recip_1_2_f32(float d) {
+    float r = fmaf(-0x1.e1e1e2p-2f, d, 0x1.69696ap+0f);
+    for (int i = 0; i < 3; ++i) {
+        const float e = fmaf(-d, r, 1.0f);
+        r = fmaf(r, e, r);
+    }
+    return r;
+}
+
+/* SiLU in fp32: z = e^-|y| (never overflows), sigma(y) = 1/(1+z) for
+ * y >= 0 and z/(1+z) below, SiLU = y sigma. */
+static float silu_f32(float y) {
+    const float z = exp_neg_f32(-fabsf(y));
+    const float r = recip_1_2_f32(1.0f + z);
+    const float sigma = (y >= 0.0f ? 1.0f : z) * r;
+    return y * sigma;
+}
 
 /* fp32 -> bf16, nearest even: the fp32 value is exact in double, so one
  * rounding of it is the fp32 -> bf16 rounding. */
@@ -445,8 +472,8 @@ uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
 double kda_oracle_gate(double raw_g, double dt_bias, double A, int use_lower_bound, double lower_bound) {
     return kda_gate(raw_g, dt_bias, A, use_lower_bound, lower_bound);
 }
-void kda_oracle_exp_f32(const float *x, float *y, int64_t n) {
-    for (int64_t i = 0; i < n; ++i) y[i] = exp_f32(x[i]);
+void kda_oracle_exp_neg_f32(const float *x, float *y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = exp_neg_f32(x[i]);
 }
 void kda_oracle_silu_f32(const float *x, float *y, int64_t n) {
     for (int64_t i = 0; i < n; ++i) y[i] = silu_f32(x[i]);

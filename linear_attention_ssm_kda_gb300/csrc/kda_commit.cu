@@ -26,8 +26,8 @@ struct CommitLayout {
   static constexpr int kKd = kState + KD * KD * 4;       // float [QMAX][KD]  k^_t * prod_{u>t} e^g
   static constexpr int kDall = kKd + QMAX * KD * 4;      // float [KD]        prod_t e^g
   static constexpr int kC = kDall + KD * 4;              // float [QMAX][KD]  c_t
-  static constexpr int kNorm = kC + QMAX * KD * 4;       // float [QMAX]      |k_t|^2
-  static constexpr int kBar = (kNorm + QMAX * 4 + 7) / 8 * 8;
+  static constexpr int kNorm = kC + QMAX * KD * 4;       // float [QMAX][KD/32] per-warp parts of |k_t|^2
+  static constexpr int kBar = (kNorm + QMAX * (KD / 32) * 4 + 7) / 8 * 8;
   static constexpr int kBytes = kBar + 8;
 };
 
@@ -87,7 +87,6 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
 #pragma unroll
     for (int c = 0; c < 4; ++c) bulk_g2s(s_state + c * (KD * KD / 4), gS + c * (KD * KD / 4), KD * KD, bar);
   }
-  if (tid < QMAX) s_norm[tid] = 0.0f;
   for (int i = tid; i < m * KD; i += kThreads) s_c[i] = gc[i];
   __syncthreads();
 
@@ -103,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
         kv[t] = bf16_to_f32(gkg[t * 2 * KD + tid]);
         eg[t] = expf(kda_gate(bf16_to_f32(gkg[t * 2 * KD + KD + tid]), dtb, A, p.lower_bound_gate, p.lower_bound));
         const float kk = warp_sum(kv[t] * kv[t]);
-        if (lane == 0) atomicAdd(&s_norm[t], kk);
+        if (lane == 0) s_norm[t * (KD / 32) + (tid >> 5)] = kk;  // summed in a fixed order below
       }
     }
   }
@@ -113,7 +112,10 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
 #pragma unroll
     for (int t = QMAX - 1; t >= 0; --t) {
       if (t < m) {
-        s_kd[t * KD + tid] = kv[t] * rsqrtf(s_norm[t] + 1e-6f) * suffix;
+        float kk = 0.0f;
+#pragma unroll
+        for (int w = 0; w < KD / 32; ++w) kk += s_norm[t * (KD / 32) + w];
+        s_kd[t * KD + tid] = kv[t] * rsqrtf(kk + 1e-6f) * suffix;
         suffix *= eg[t];
       }
     }

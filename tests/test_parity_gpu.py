@@ -304,6 +304,23 @@ def test_commit_prefix_property_on_gpu():
             assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
 
 
+def test_verify_and_commit_are_bitwise_reproducible():
+    """Two runs on the same inputs write the same bits (no order-dependent
+    floating-point reductions across warps or CTAs)."""
+    runs = []
+    for _ in range(2):
+        p2 = make_problem(CONFIGS["C2"], DEV, B=48, L=2, slots=96)
+        dm = device_meta(p2.meta, DEV)
+        for l in range(p2.cfg.L):
+            verify_layer(p2, l, dm)
+        commit_all(commit_context(p2), dm)
+        torch.cuda.synchronize()
+        runs.append([t.view(torch.int16 if t.element_size() == 2 else torch.int32).cpu().numpy()
+                     for t in (p2.out, p2.corr, p2.key_gate, p2.conv_state, p2.state)])
+    for a, b in zip(*runs):
+        np.testing.assert_array_equal(a, b)
+
+
 def test_empty_and_all_null_batches():
     cfg = CONFIGS["C0"]
     prob = make_problem(cfg, DEV)

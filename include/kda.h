@@ -195,6 +195,30 @@ kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
 /* Enqueue the commit of all layers (one kernel launch). */
 kda_status kda_commit(const kda_commit_args *args, kda_stream_t stream);
 
+/* Allocation-free commit.  The pages have no counterpart to this entry point:
+ * their commit context keeps the per-layer tables in device memory it
+ * allocates once (KDARecoverSSMCommitContext.create).  It serves callers that
+ * cannot allocate device memory.
+ *
+ * args is read as for kda_commit, except that the six per-layer tables
+ * (state_base, state_slot_stride, corr_base, corr_row_stride, kg_base,
+ * kg_row_stride) are HOST arrays of L entries, read during the call.  The
+ * call copies them, in stream order, into a library-owned static device
+ * scratch of KDA_NOALLOC_MAX_LAYERS layers (6 x 64 int64 = 3 KB) and runs the
+ * kda_commit kernel on it.  It allocates nothing, on the host or the device.
+ *   - L > KDA_NOALLOC_MAX_LAYERS: KDA_ERR_UNSUPPORTED, nothing enqueued.
+ *   - The first call on a device does the set-up: it resolves the scratch's
+ *     device address (cudaGetSymbolAddress), which may load the module.  Make
+ *     that first call before any stream capture.
+ *   - Nothing in the scratch has to start at zero: each call writes every
+ *     table entry its kernel reads, before the kernel, in stream order.  The
+ *     optional workspace is the caller's and is used as for kda_commit.
+ *   - There is one scratch per device and process: calls whose copies and
+ *     kernels can overlap (different streams, or threads without a common
+ *     stream order) race on it.  Serialise them. */
+#define KDA_NOALLOC_MAX_LAYERS 64
+kda_status kda_commit_noalloc(const kda_commit_args *args, kda_stream_t stream);
+
 /* Bytes of device workspace for the error report (int32-aligned, zeroed by
  * the caller before first use; the library only ORs bits into it). */
 size_t kda_workspace_bytes(void);

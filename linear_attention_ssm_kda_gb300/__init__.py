@@ -23,6 +23,7 @@ from typing import Sequence
 import torch
 
 __all__ = [
+    "commit_noalloc",
     "KdaError", "lib_path", "load_library", "verify", "CommitContext", "workspace_bytes",
     "new_workspace", "read_device_error", "last_error",
     "DEVERR_SLOT_RANGE", "DEVERR_ROW_RANGE", "DEVERR_TOKEN_RANGE", "DEVERR_TIMEOUT", "DEVERR_MISALIGNED",
@@ -105,6 +106,8 @@ def load_library():
             lib.kda_verify.restype = ctypes.c_int
             lib.kda_commit.argtypes = [ctypes.POINTER(CommitArgs), _p]
             lib.kda_commit.restype = ctypes.c_int
+            lib.kda_commit_noalloc.argtypes = [ctypes.POINTER(CommitArgs), _p]
+            lib.kda_commit_noalloc.restype = ctypes.c_int
             lib.kda_workspace_bytes.argtypes = []
             lib.kda_workspace_bytes.restype = ctypes.c_size_t
             lib.kda_read_device_error.argtypes = [_p, _p, ctypes.POINTER(_i32)]
@@ -356,3 +359,79 @@ class CommitContext:
         a.num_accepted = num_accepted_tokens.data_ptr()
         a.workspace = _ptr(workspace)
         _check(load_library().kda_commit(ctypes.byref(a), ctypes.c_void_p(_stream_handle(dev, stream))))
+
+
+NOALLOC_MAX_LAYERS = 64  # KDA_NOALLOC_MAX_LAYERS
+
+
+def commit_noalloc(*, states: Sequence[torch.Tensor], corrections: Sequence[torch.Tensor],
+                   key_gates: Sequence[torch.Tensor], A_log: torch.Tensor, dt_bias: torch.Tensor,
+                   lower_bound: float | None, window: int, num_accepted_tokens: torch.Tensor,
+                   state_indices: torch.Tensor, query_start_loc: torch.Tensor,
+                   record_indices: torch.Tensor | None = None, null_block_id: int = 0,
+                   workspace: torch.Tensor | None = None, stream=None) -> None:
+    """The commit of ``CommitContext.commit`` through kda_commit_noalloc: the
+    per-layer tables stay on the host and the library copies them into its
+    static device scratch (at most NOALLOC_MAX_LAYERS layers), so neither this
+    function nor the library allocates device memory.  Calls that can overlap
+    on the device race on that scratch; the first call on a device does the
+    scratch set-up and belongs before any stream capture."""
+    L = len(states)
+    if L == 0 or not (L == len(corrections) == len(key_gates)):
+        raise ValueError("states, corrections and key_gates need one entry per layer")
+    ref = states[0]
+    dev = ref.device
+    slots, H, V, K = ref.shape
+    rows = corrections[0].shape[0]
+    for l in range(L):
+        _need(states[l], f"states[{l}]", torch.float32, dev, 4)
+        _need(corrections[l], f"corrections[{l}]", torch.float32, dev, 4)
+        _need(key_gates[l], f"key_gates[{l}]", torch.bfloat16, dev, 4)
+        if states[l].shape != ref.shape:
+            raise ValueError("layers need matching state shapes")
+        if corrections[l].shape != (rows, H, window, V) or key_gates[l].shape != (rows, H, window, 2 * K):
+            raise ValueError("layers need matching record shapes")
+        _inner_contiguous(states[l], f"states[{l}]", 3)
+        _inner_contiguous(corrections[l], f"corrections[{l}]", 3)
+        _inner_contiguous(key_gates[l], f"key_gates[{l}]", 3)
+    _need(A_log, "A_log", torch.float32, dev)
+    _need(dt_bias, "dt_bias", torch.float32, dev)
+    if A_log.numel() != L * H or dt_bias.numel() != L * H * K:
+        raise ValueError("A_log must be [L, H] and dt_bias [L, H*K]")
+    if not (A_log.is_contiguous() and dt_bias.is_contiguous()):
+        raise ValueError("A_log and dt_bias must be contiguous")
+    B = state_indices.shape[0]
+    for name, t in (("num_accepted_tokens", num_accepted_tokens), ("state_indices", state_indices),
+                    ("query_start_loc", query_start_loc)):
+        _need(t, name, torch.int32, dev, 1)
+        if not t.is_contiguous():
+            raise ValueError("commit metadata must be contiguous")
+    if query_start_loc.shape[0] != B + 1 or num_accepted_tokens.shape[0] < B:
+        raise ValueError("commit metadata is incompatible: query_start_loc [B+1], num_accepted [B]")
+    if record_indices is not None:
+        _need(record_indices, "record_indices", torch.int32, dev, 1)
+        if record_indices.shape[0] < B or not record_indices.is_contiguous():
+            raise ValueError("record_indices is too short")
+    if workspace is not None:
+        _need(workspace, "workspace", torch.int32, dev)
+
+    def host_table(vals):
+        return (ctypes.c_int64 * L)(*vals)
+
+    tables = [host_table([t.data_ptr() for t in states]), host_table([t.stride(0) for t in states]),
+              host_table([t.data_ptr() for t in corrections]), host_table([t.stride(0) for t in corrections]),
+              host_table([t.data_ptr() for t in key_gates]), host_table([t.stride(0) for t in key_gates])]
+    a = CommitArgs()
+    a.L, a.B, a.H, a.K, a.V, a.Q = L, B, H, K, V, window
+    a.null_block_id = null_block_id
+    a.num_slots, a.num_record_rows = slots, rows
+    a.state_base, a.state_slot_stride, a.corr_base, a.corr_row_stride, a.kg_base, a.kg_row_stride = (
+        ctypes.cast(t, ctypes.c_void_p).value for t in tables)
+    a.A_log, a.dt_bias = A_log.data_ptr(), dt_bias.data_ptr()
+    a.gate_mode = GATE_SOFTPLUS if lower_bound is None else GATE_LOWER_BOUND
+    a.lower_bound = 0.0 if lower_bound is None else float(lower_bound)
+    a.query_start_loc, a.state_indices = query_start_loc.data_ptr(), state_indices.data_ptr()
+    a.record_indices = _ptr(record_indices)
+    a.num_accepted = num_accepted_tokens.data_ptr()
+    a.workspace = _ptr(workspace)
+    _check(load_library().kda_commit_noalloc(ctypes.byref(a), ctypes.c_void_p(_stream_handle(dev, stream))))

@@ -18,6 +18,7 @@
 namespace kda {
 cudaError_t launch_verify(const VerifyParams& p, int K, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, int K, cudaStream_t stream);
+cudaError_t noalloc_tables(long long** out);
 }  // namespace kda
 
 namespace {
@@ -166,6 +167,67 @@ kda_status kda_commit(const kda_commit_args* a, kda_stream_t stream) {
   p.workspace = a->workspace;
   cudaError_t e = kda::launch_commit(p, a->K, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_commit: launch failed: %s", cudaGetErrorString(e));
+  return KDA_OK;
+}
+
+kda_status kda_commit_noalloc(const kda_commit_args* a, kda_stream_t stream) {
+  constexpr int kMax = KDA_NOALLOC_MAX_LAYERS;
+  if (a == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_commit_noalloc: args is NULL");
+  if (a->L <= 0) return fail(KDA_ERR_INVALID_ARG, "kda_commit_noalloc: needs at least one layer (L=%d)", a->L);
+  if (a->L > kMax)
+    return fail(KDA_ERR_UNSUPPORTED, "kda_commit_noalloc: L=%d layers exceed its static scratch of %d layers",
+                a->L, kMax);
+  if (a->B < 0) return fail(KDA_ERR_INVALID_ARG, "kda_commit_noalloc: negative B (%d)", a->B);
+  kda_status st = check_dims(a->H, a->K, a->V, a->Q);
+  if (st != KDA_OK) return st;
+  if (a->B == 0) return KDA_OK;
+  const void* required[] = {a->state_base, a->state_slot_stride, a->corr_base, a->corr_row_stride,
+                            a->kg_base,    a->kg_row_stride,     a->A_log,     a->dt_bias,
+                            a->query_start_loc, a->state_indices, a->num_accepted};
+  for (const void* ptr : required)
+    if (ptr == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_commit_noalloc: a required pointer is NULL");
+  if (a->gate_mode != KDA_GATE_SOFTPLUS && a->gate_mode != KDA_GATE_LOWER_BOUND)
+    return fail(KDA_ERR_INVALID_ARG, "kda_commit_noalloc: gate_mode %d", a->gate_mode);
+  if (a->gate_mode == KDA_GATE_LOWER_BOUND && !std::isfinite(a->lower_bound))
+    return fail(KDA_ERR_INVALID_ARG, "kda_commit_noalloc: lower_bound is not finite");
+  if (a->num_slots <= 0 || a->num_record_rows <= 0)
+    return fail(KDA_ERR_INVALID_ARG, "kda_commit_noalloc: num_slots and num_record_rows must be positive");
+  if (!aligned(a->A_log, 4) || !aligned(a->dt_bias, 4))
+    return fail(KDA_ERR_MISALIGNED, "kda_commit_noalloc: gate parameters must be 4-byte aligned");
+  if ((long long)a->L * a->B * a->H > 0x7fffffffLL)
+    return fail(KDA_ERR_UNSUPPORTED, "kda_commit_noalloc: L*B*H too large");
+
+  long long* tables = nullptr;
+  cudaError_t e = kda::noalloc_tables(&tables);
+  if (e != cudaSuccess)
+    return fail(KDA_ERR_CUDA, "kda_commit_noalloc: scratch set-up failed: %s", cudaGetErrorString(e));
+  // host staging on the stack: table j of layer l at [j * kMax + l]
+  long long host[6 * kMax];
+  const int64_t* src[6] = {a->state_base, a->state_slot_stride, a->corr_base,
+                           a->corr_row_stride, a->kg_base, a->kg_row_stride};
+  for (int j = 0; j < 6; ++j)
+    for (int l = 0; l < kMax; ++l) host[j * kMax + l] = l < a->L ? static_cast<long long>(src[j][l]) : 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  e = cudaMemcpyAsync(tables, host, sizeof host, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess)
+    return fail(KDA_ERR_CUDA, "kda_commit_noalloc: table copy failed: %s", cudaGetErrorString(e));
+
+  kda::CommitParams p{};
+  p.L = a->L; p.B = a->B; p.H = a->H; p.Q = a->Q; p.null_block_id = a->null_block_id;
+  p.num_slots = a->num_slots; p.num_record_rows = a->num_record_rows;
+  p.state_base = tables + 0 * kMax;
+  p.state_stride = tables + 1 * kMax;
+  p.corr_base = tables + 2 * kMax;
+  p.corr_stride = tables + 3 * kMax;
+  p.kg_base = tables + 4 * kMax;
+  p.kg_stride = tables + 5 * kMax;
+  p.A_log = a->A_log; p.dt_bias = a->dt_bias;
+  p.lower_bound_gate = a->gate_mode == KDA_GATE_LOWER_BOUND; p.lower_bound = a->lower_bound;
+  p.qsl = a->query_start_loc; p.state_indices = a->state_indices;
+  p.record_indices = a->record_indices; p.num_accepted = a->num_accepted;
+  p.workspace = a->workspace;
+  e = kda::launch_commit(p, a->K, s);
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_commit_noalloc: launch failed: %s", cudaGetErrorString(e));
   return KDA_OK;
 }
 

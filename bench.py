@@ -82,17 +82,20 @@ def kernel_source_hash(kind: str) -> str:
 
 
 def profiled_traffic(kind: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from the committed ncu summary
+    (``profiles/traffic.txt``: kernel, source hash, workload, bytes per launch),
+    if it was taken on the current source of the kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
-            rec = json.load(f)[kind]
-    except Exception:
+            for line in f:
+                parts = line.split("#", 1)[0].split()
+                if len(parts) >= 4 and parts[0] == kind:
+                    if parts[1] == kernel_source_hash(kind) and parts[2] == workload:
+                        return int(parts[3])
+    except (OSError, ValueError):
         return None
-    if rec.get("source_sha") != kernel_source_hash(kind) or rec.get("workload") != workload:
-        return None
-    return rec.get("dram_bytes_per_launch")
+    return None
 
 
 # --------------------------------------------------------------------------- clocks
@@ -200,6 +203,21 @@ def shard_seed(base_seed: int, rank: int) -> int:
     return base_seed + 1000 * rank
 
 
+def workload_config(c, acct) -> dict:
+    """The ``config`` object of the JSON line (both arms)."""
+    return {
+        "workload": (f"{c.name}: verify then commit, B={c.B} requests, H={c.H} heads, K=V={c.K}, "
+                     f"window Q={c.Q}, conv width {c.W}, {c.L} layers, {c.slots}-slot fp32 state pools, "
+                     f"{'dim' if c.conv_dim_first else 'seq'}-first conv state, "
+                     f"{'fp32' if c.conv_weight_fp32 else 'bf16'} conv weight, "
+                     f"{'lower_bound' if c.lower_bound is not None else 'softplus'} gate"),
+        "tokens_per_step": acct["tokens"],
+        "algorithmic_bytes_per_step": acct["step_bytes"],
+        "l2": "inputs larger than L2 (each step streams every layer's live state, ~GBs)",
+        "activations": "bf16", "state": "fp32",
+    }
+
+
 # --------------------------------------------------------------------------- oracle timing (CPU)
 
 def time_oracle(cfg_name: str, steps: int, warmup: int, sample_layers: int = 1, threads: int | None = None):
@@ -235,7 +253,7 @@ def time_oracle(cfg_name: str, steps: int, warmup: int, sample_layers: int = 1, 
     per_full_step = dt * cfg.L / sample_layers
     sample = (f"{cfg_name} request batch (B={cfg.B}, H={cfg.H}) over {sample_layers} of {cfg.L} layers, "
               f"verify + commit, {steps} steps; scaled to {cfg.L} layers")
-    return acct["tokens"] / per_full_step, per_full_step, sample, threads
+    return acct["tokens"] / per_full_step, per_full_step, sample, threads, acct
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -374,10 +392,9 @@ def run_gpu(args, rank, local, world):
     traffic = profiled_traffic("verify" if dom == "kda_verify" else "commit", workload)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cv, cstep, sample, threads = time_oracle(args.config, steps=args.cpu_steps, warmup=1)
+        cv, cstep, sample, threads, _ = time_oracle(args.config, steps=args.cpu_steps, warmup=1)
         cpu = {"value": cv, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample,
                "s_per_full_step": cstep}
-    c = cfg
     line = {
         "metric": METRIC,
         "value": value,
@@ -391,17 +408,7 @@ def run_gpu(args, rank, local, world):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded; inputs resident in HBM)",
-        "config": {
-            "workload": (f"{args.config}: verify then commit, B={c.B} requests, H={c.H} heads, K=V={c.K}, "
-                         f"window Q={c.Q}, conv width {c.W}, {c.L} layers, {c.slots}-slot fp32 state pools, "
-                         f"{'dim' if c.conv_dim_first else 'seq'}-first conv state, "
-                         f"{'fp32' if c.conv_weight_fp32 else 'bf16'} conv weight, "
-                         f"{'lower_bound' if c.lower_bound is not None else 'softplus'} gate"),
-            "tokens_per_step": acct["tokens"],
-            "algorithmic_bytes_per_step": acct["step_bytes"],
-            "l2": "inputs larger than L2 (each step streams every layer's live state, ~GBs)",
-            "activations": "bf16", "state": "fp32",
-        },
+        "config": workload_config(cfg, acct),
         "achieved_hbm_gbs": achieved,
         "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * achieved / peak,
@@ -431,22 +438,23 @@ def run_reference(args, rank, world):
     oracle.build()
     from workloads import CONFIGS
     cfg = CONFIGS[args.config]
-    value, per_step, sample, threads = time_oracle(args.config, steps=args.steps, warmup=args.warmup)
+    steps = min(args.steps, args.cpu_steps)  # each oracle step is a bounded sample (one layer)
+    value, per_step, sample, threads, acct = time_oracle(args.config, steps=steps, warmup=min(args.warmup, 3))
     return {
         "impl": "reference",
         "metric": METRIC,
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+        "steps": steps,
+        "warmup": min(args.warmup, 3),
         "ms_per_step": per_step * 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": f"{args.config}: B={cfg.B}, H={cfg.H}, K=V={cfg.K}, Q={cfg.Q}, {cfg.L} layers"},
+        "config": workload_config(cfg, acct),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -455,12 +463,12 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default="C2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-steps", type=int, default=40)
+    ap.add_argument("--cpu-steps", type=int, default=200)
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (small cases for profiling; not a bench line)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -48,7 +48,7 @@ namespace {
 
 constexpr int kConvWidth = 4;
 constexpr int kPrepWarps = 6;  // two conv channels per thread, then one key channel per thread
-constexpr int kGemvWarps = 8;  // one state row chunk each
+constexpr int kGemvWarps = 8;  // one state row chunk (16 rows at K = 128) each
 constexpr int kPrepConvThreads = 32 * kPrepWarps;
 constexpr int kThreads = 32 * (2 + kPrepWarps + kGemvWarps);
 constexpr int kBarPrep = 1;
@@ -81,7 +81,7 @@ struct OpMeta {
 template <int KD, int QMAX>
 struct Layout {
   static_assert(7 * QMAX + 10 <= 96, "small-input copies per item exceed three per lane");
-  static constexpr int RW = KD / 8;           // state rows per gemv warp (one chunk)
+  static constexpr int RW = KD / kGemvWarps;  // state rows per gemv warp (one chunk)
   static constexpr int kChunk = RW * KD * 4;  // bytes per state chunk
   static constexpr int kLcMax = QMAX + kConvWidth - 2;
   static constexpr int kSeg = KD * 2 + 16;    // hull of one row segment
@@ -209,7 +209,7 @@ __device__ __forceinline__ int hull_offset(const void* src) {
 // order: 3n activation row segments (token t, group g), n gate row segments,
 // the head's conv taps (3 blocks dim-first, 3 (Q+W-2) rows seq-first), three
 // conv-weight blocks and dt_bias.  Returns false past the last copy.
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool DF>
 __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, int bos, long long s, int h,
                                            unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
   using Lay = Layout<KD, QMAX>;
@@ -231,10 +231,10 @@ __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, 
     len = KD * 2;
   } else {
     q -= 4 * n;
-    const int nconv = p.conv_dim_first ? 3 : 3 * Lc;
+    const int nconv = DF ? 3 : 3 * Lc;
     const uint16_t* cs = p.conv_state + s * p.conv_slot_stride;
     if (q < nconv) {
-      if (p.conv_dim_first) {
+      if (DF) {
         ptr = reinterpret_cast<const unsigned char*>(cs + (q * HK + static_cast<long long>(h) * KD) * Lc);
         *dst = sl + Lay::kConv + q * KD * Lc * 2;
         len = KD * Lc * 2;
@@ -266,7 +266,7 @@ __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, 
 
 // ---------------------------------------------------------------- inputs warp
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool DF>
 __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
   using Lay = Layout<KD, QMAX>;
   Bars<KD, QMAX> bars(smem);
@@ -312,7 +312,7 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
         uint32_t mine = 0;
 #pragma unroll
         for (int c = 0; c < 3; ++c) {
-          if (!small_copy<KD, QMAX>(p, lane + 32 * c, mj.n, mj.bos, mj.s, jh, sl, &src[c], &dst[c], &bytes[c]))
+          if (!small_copy<KD, QMAX, DF>(p, lane + 32 * c, mj.n, mj.bos, mj.s, jh, sl, &src[c], &dst[c], &bytes[c]))
             bytes[c] = 0;
           mine += bytes[c];
         }
@@ -391,7 +391,7 @@ __device__ __forceinline__ void reduce_scatter_stage(float* acc, int mask, bool 
 // Conv + SiLU of channel k of group g (q | k | v) over the window: the bf16
 // codes of the n outputs, and the rolled taps written back into the slot's
 // copy of the conv state.
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool DF>
 __device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsigned char* sl, int g, int k, int n,
                                              int a, int Lc, uint32_t act_lo, uint16_t (&y)[QMAX]) {
   using Lay = Layout<KD, QMAX>;
@@ -409,7 +409,7 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsign
   seq[kConvWidth - 1 + QMAX] = 0;
 #pragma unroll
   for (int j = 0; j < kConvWidth - 1; ++j)
-    seq[j] = p.conv_dim_first ? conv[(g * KD + k) * Lc + a - 1 + j] : conv[((a - 1 + j) * 3 + g) * KD + k];
+    seq[j] = DF ? conv[(g * KD + k) * Lc + a - 1 + j] : conv[((a - 1 + j) * 3 + g) * KD + k];
 #pragma unroll
   for (int t = 0; t < QMAX; ++t) {
     seq[kConvWidth - 1 + t] = 0;
@@ -439,7 +439,7 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsign
 #pragma unroll
   for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
     if (j < kConvWidth - 2 + n) {
-      if (p.conv_dim_first)
+      if (DF)
         conv[(g * KD + k) * Lc + j] = seq[j + 1];
       else
         conv[(j * 3 + g) * KD + k] = seq[j + 1];
@@ -447,7 +447,7 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsign
   }
 }
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool DF>
 __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatile int* misc) {
   using Lay = Layout<KD, QMAX>;
   constexpr int NREDP = Lay::kPart;  // |q_t|^2, |k_t|^2, raw M / N grid, padded to 32
@@ -495,7 +495,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
           const int g = c / KD;
           const int k = c - g * KD;
           uint16_t y[QMAX];
-          conv_channel<KD, QMAX>(p, sl, g, k, n, m.a, Lc, act_lo, y);
+          conv_channel<KD, QMAX, DF>(p, sl, g, k, n, m.a, Lc, act_lo, y);
           if (g < 2) {
 #pragma unroll
             for (int t = 0; t < QMAX; ++t) xs[(g * QMAX + t) * KD + k] = bf16_to_f32(y[t]);
@@ -518,7 +518,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
     if (misc[kMiscPrepFail]) break;  // every prep thread sees the same flag here
     if (live && pt == 0) {  // the rolled conv state leaves by bulk stores from the slot
       uint16_t* cs = p.conv_state + m.s * p.conv_slot_stride;
-      if (p.conv_dim_first) {
+      if (DF) {
 #pragma unroll
         for (int g = 0; g < 3; ++g)
           bulk_s2g(cs + (g * HK + static_cast<long long>(h) * KD) * Lc, sl + Lay::kConv + g * KD * Lc * 2, KD * Lc * 2);
@@ -660,10 +660,10 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
 // product runs as two interleaved halves in one packed fp32x2 FMA chain
 // (elements x, y and z, w of each float4); the halves are added, and the 4
 // partial sums of a row meet in a two-stage reduce-scatter.
-template <int KD, int NCG>
+template <int KD, int NCG, bool kToRed>
 __device__ __forceinline__ void gemv_chunk(const float* __restrict__ st, const float* __restrict__ vec,
-                                           float* __restrict__ red, int lane) {
-  constexpr int RW = KD / 8;
+                                           float* __restrict__ red, int lane, float (&mine)[8]) {
+  constexpr int RW = KD / kGemvWarps;
   constexpr int R = RW / 8;   // rows per lane
   constexpr int J = KD / 16;  // float4 chunks per lane and row
   constexpr int NV = R * NCG;
@@ -695,14 +695,64 @@ __device__ __forceinline__ void gemv_chunk(const float* __restrict__ st, const f
   for (int i = 0; i < NVP; ++i) acc[i] = i < NV ? acc2[i].x + acc2[i].y : 0.0f;
   reduce_scatter_stage<NVP>(acc, 2, (kq & 2) != 0);
   reduce_scatter_stage<NVP / 2>(acc, 1, (kq & 1) != 0);
+  // lane kq now holds values v = (NVP/4) kq + i: row v / NCG, vector v % NCG
+  if constexpr (kToRed) {
 #pragma unroll
-  for (int i = 0; i < NVP / 4; ++i) {
-    const int v = (NVP / 4) * kq + i;
-    if (v < NV) {
-      const int row = v / NCG;
-      const int c = v - row * NCG;
-      red[c * RW + rs + 8 * row] = acc[i];
+    for (int i = 0; i < NVP / 4; ++i) {
+      const int v = (NVP / 4) * kq + i;
+      if (v < NV) {
+        const int row = v / NCG;
+        const int c = v - row * NCG;
+        red[c * RW + rs + 8 * row] = acc[i];
+      }
     }
+  } else {
+    static_assert(NVP / 4 <= 8, "at most eight values per lane stay in registers");
+#pragma unroll
+    for (int i = 0; i < NVP / 4; ++i) mine[i] = acc[i];
+  }
+}
+
+// The row-local solve with P | R in registers (K = 128, 16 rows per warp,
+// 2N <= 8 vectors in one group): after gemv_chunk<128, 2N, false> lane
+// (rs, kq) holds, for row rs + 8 (kq >> 1) of its chunk, P_0..P_{N-1} if kq is
+// even and R_0..R_{N-1} if kq is odd.  The two lanes of a row swap their
+// halves and both run the recurrence; the even lane stores the corrections,
+// the odd lane the outputs.
+template <int KD, int QMAX, int N>
+__device__ __forceinline__ void solve_regs(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op,
+                                           int h, int gw, int lane, const float (&mine)[8]) {
+  using Lay = Layout<KD, QMAX>;
+  static_assert(Lay::RW == 16, "two lanes per row: 16 rows per gemv warp");
+  const int kq = lane & 3;
+  const int row = gw * Lay::RW + (lane >> 2) + 8 * (kq >> 1);
+  const bool xlane = (kq & 1) == 0;
+  const float* mn = reinterpret_cast<const float*>(op + Lay::kOpMN);
+  const float* xv = reinterpret_cast<const float*>(op + Lay::kOpV);
+  float P[N], R[N];
+#pragma unroll
+  for (int t = 0; t < N; ++t) {
+    const float other = __shfl_xor_sync(0xffffffffu, mine[t], 1);
+    P[t] = xlane ? mine[t] : other;
+    R[t] = xlane ? other : mine[t];
+  }
+  float* corr = p.corr + m.r * p.corr_stride + static_cast<long long>(h) * p.Q * KD + row;
+  uint16_t* out = p.out + static_cast<long long>(m.bos) * p.out_stride + static_cast<long long>(h) * KD + row;
+  float cv[N];
+#pragma unroll
+  for (int t = 0; t < N; ++t) {
+    float x = xv[t * KD + row] - P[t];
+#pragma unroll
+    for (int u = 0; u < t; ++u) x = fmaf(-mn[t * QMAX + u], cv[u], x);
+    const float c = x * m.beta[t];
+    cv[t] = c;
+    float o = R[t];
+#pragma unroll
+    for (int u = 0; u <= t; ++u) o = fmaf(mn[u * QMAX + t], cv[u], o);
+    if (xlane)
+      corr[t * KD] = c;
+    else
+      out[static_cast<long long>(t) * p.out_stride] = f32_to_bf16(o);
   }
 }
 
@@ -732,12 +782,47 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
       if (!ok) break;
       const float* st = reinterpret_cast<const float*>(smem + Lay::oChunks + pos * Lay::kChunk);
       const float* vec = reinterpret_cast<const float*>(op + Lay::kOpVec);
+      float mine[8];
+      if (KD == 128 && n <= 4) {  // one vector group: P | R stay in registers
+        if constexpr (KD == 128) {
+          switch (n) {
+            case 1:
+              gemv_chunk<KD, 2, false>(st, vec, red, lane, mine);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
+              solve_regs<KD, QMAX, 1>(p, m, op, h, gw, lane, mine);
+              break;
+            case 2:
+              gemv_chunk<KD, 4, false>(st, vec, red, lane, mine);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
+              solve_regs<KD, QMAX, 2>(p, m, op, h, gw, lane, mine);
+              break;
+            case 3:
+              gemv_chunk<KD, 6, false>(st, vec, red, lane, mine);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
+              solve_regs<KD, QMAX, 3>(p, m, op, h, gw, lane, mine);
+              break;
+            default:
+              gemv_chunk<KD, 8, false>(st, vec, red, lane, mine);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
+              solve_regs<KD, QMAX, 4>(p, m, op, h, gw, lane, mine);
+              break;
+          }
+        }
+        ++live;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
+        continue;
+      }
       for (int cg = 0; cg < 2 * n; cg += 8) {
         switch (min(8, 2 * n - cg)) {
-          case 2: gemv_chunk<KD, 2>(st, vec + cg * KD, red + cg * RW, lane); break;
-          case 4: gemv_chunk<KD, 4>(st, vec + cg * KD, red + cg * RW, lane); break;
-          case 6: gemv_chunk<KD, 6>(st, vec + cg * KD, red + cg * RW, lane); break;
-          default: gemv_chunk<KD, 8>(st, vec + cg * KD, red + cg * RW, lane); break;
+          case 2: gemv_chunk<KD, 2, true>(st, vec + cg * KD, red + cg * RW, lane, mine); break;
+          case 4: gemv_chunk<KD, 4, true>(st, vec + cg * KD, red + cg * RW, lane, mine); break;
+          case 6: gemv_chunk<KD, 6, true>(st, vec + cg * KD, red + cg * RW, lane, mine); break;
+          default: gemv_chunk<KD, 8, true>(st, vec + cg * KD, red + cg * RW, lane, mine); break;
         }
       }
       __syncwarp();
@@ -776,7 +861,7 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
   }
 }
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool DF>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VerifyParams p) {
   using Lay = Layout<KD, QMAX>;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -802,11 +887,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VerifyParams 
   }
   __syncthreads();
   if (warp == 0) {
-    produce_inputs<KD, QMAX>(p, smem, tid & 31, misc + kMiscAbort);
+    produce_inputs<KD, QMAX, DF>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp == 1) {
     produce_state<KD, QMAX>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp < 2 + kPrepWarps) {
-    prep<KD, QMAX>(p, smem, tid - 64, misc);
+    prep<KD, QMAX, DF>(p, smem, tid - 64, misc);
   } else {
     gemv_team<KD, QMAX>(p, smem, warp - 2 - kPrepWarps, tid & 31, misc);
   }
@@ -824,22 +909,27 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool DF>
 cudaError_t launch(const VerifyParams& p, cudaStream_t stream) {
   constexpr int bytes = Layout<KD, QMAX>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, DF>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const int items = p.B * p.H;
   const int grid = items < sm_count() ? items : sm_count();
-  verify_kernel<KD, QMAX><<<grid, kThreads, bytes, stream>>>(p);
+  verify_kernel<KD, QMAX, DF><<<grid, kThreads, bytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_verify(const VerifyParams& p, int K, cudaStream_t stream) {
-  if (K == 128) return p.Q <= 4 ? launch<128, 4>(p, stream) : launch<128, 8>(p, stream);
-  return p.Q <= 4 ? launch<64, 4>(p, stream) : launch<64, 8>(p, stream);
+  // the conv-state layout is a template parameter: straight-line tap addressing
+  if (p.conv_dim_first) {
+    if (K == 128) return p.Q <= 4 ? launch<128, 4, true>(p, stream) : launch<128, 8, true>(p, stream);
+    return p.Q <= 4 ? launch<64, 4, true>(p, stream) : launch<64, 8, true>(p, stream);
+  }
+  if (K == 128) return p.Q <= 4 ? launch<128, 4, false>(p, stream) : launch<128, 8, false>(p, stream);
+  return p.Q <= 4 ? launch<64, 4, false>(p, stream) : launch<64, 8, false>(p, stream);
 }
 
 }  // namespace kda

@@ -98,7 +98,7 @@ struct Layout {
   static constexpr int kOpV = kOpVec + 2 * QMAX * KD * 4;              // [QMAX][KD] v_t
   static constexpr int kOpMN = kOpV + QMAX * KD * 4;                   // [QMAX][QMAX] M | N
   static constexpr int kOp = ru(kOpMN + QMAX * QMAX * 4, 128);
-  static constexpr int kNumOp = 2;
+  static constexpr int kNumOp = QMAX <= 4 ? 3 : 2;  // prep runs up to two items ahead of the gemv team
   // per-item scratch of the prep team
   static constexpr int kXs = 2 * QMAX * KD * 4;                        // [2][QMAX][KD] q | k conv outputs
   // per-warp scratch

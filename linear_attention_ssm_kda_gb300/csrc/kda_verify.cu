@@ -264,6 +264,51 @@ __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, 
   return true;
 }
 
+// The same copies for the dim-first conv layout when they fit one per lane
+// (4n + 7 <= 32): every lane computes its copy without branches, by
+// selecting a base, a row, a row stride and a column per kind of copy.
+// Kinds by lane q: activation (t = q / 3, g = q % 3) for q < 3n, gate
+// (t = q - 3n) for q < 4n, conv taps of group q - 4n, conv weights of group
+// q - 4n - 3, dt_bias at q = 4n + 6.  Returns false for lanes past the last copy.
+template <int KD, int QMAX>
+__device__ __forceinline__ bool small_copy_lane(const VerifyParams& p, int q, int n, int bos, long long s, int h,
+                                                unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
+  using Lay = Layout<KD, QMAX>;
+  const long long HK = static_cast<long long>(p.H) * KD;
+  const int Lc = p.Q + kConvWidth - 2;
+  const int wb = p.conv_weight_fp32 ? 4 : 2;
+  const int n3 = 3 * n, n4 = 4 * n;
+  const bool is_act = q < n3, is_gate = !is_act && q < n4, is_conv = q >= n4 && q < n4 + 3;
+  const bool is_w = q >= n4 + 3 && q < n4 + 6, is_dt = q == n4 + 6;
+  const int t_act = q / 3;
+  const int g = is_act ? q - 3 * t_act : (is_conv ? q - n4 : q - n4 - 3);
+  const long long hk = static_cast<long long>(h) * KD;
+  const unsigned char* base = is_act    ? reinterpret_cast<const unsigned char*>(p.mixed_qkv)
+                              : is_gate ? reinterpret_cast<const unsigned char*>(p.raw_gate)
+                              : is_conv ? reinterpret_cast<const unsigned char*>(p.conv_state)
+                              : is_w    ? static_cast<const unsigned char*>(p.conv_weight)
+                                        : reinterpret_cast<const unsigned char*>(p.dt_bias);
+  const long long row = is_act ? bos + t_act : (is_gate ? bos + q - n3 : (is_conv ? s : 0));
+  const long long row_bytes = is_act ? p.qkv_stride * 2 : (is_gate ? p.gate_stride * 2 : (is_conv ? p.conv_slot_stride * 2 : 0));
+  const long long col = is_act ? (g * HK + hk) * 2
+                      : is_gate ? hk * 2
+                      : is_conv ? (g * HK + hk) * Lc * 2
+                      : is_w    ? (g * HK + hk) * kConvWidth * wb
+                                : hk * 4;
+  const int dst_off = is_act    ? Lay::kAct + q * Lay::kSeg
+                      : is_gate ? Lay::kGate + (q - n3) * Lay::kSeg
+                      : is_conv ? Lay::kConv + g * KD * Lc * 2
+                      : is_w    ? Lay::kW + g * KD * kConvWidth * wb
+                                : Lay::kDt;
+  const int len = (is_act || is_gate) ? KD * 2 : (is_conv ? KD * Lc * 2 : (is_w ? KD * kConvWidth * wb : KD * 4));
+  const unsigned char* ptr = base + row * row_bytes + col;
+  const int off = hull_offset(ptr);
+  *src = ptr - off;
+  *dst = sl + dst_off;
+  *bytes = static_cast<uint32_t>((off + len + 15) & ~15);
+  return is_act || is_gate || is_conv || is_w || is_dt;
+}
+
 // ---------------------------------------------------------------- inputs warp
 
 template <int KD, int QMAX, bool DF>
@@ -308,13 +353,19 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
         // byte before the first copy can land
         const void* src[3];
         void* dst[3];
-        uint32_t bytes[3];
+        uint32_t bytes[3] = {0, 0, 0};
         uint32_t mine = 0;
+        if (DF && 4 * QMAX + 7 <= 32) {  // one copy per lane, computed without branches
+          if (!small_copy_lane<KD, QMAX>(p, lane, mj.n, mj.bos, mj.s, jh, sl, &src[0], &dst[0], &bytes[0]))
+            bytes[0] = 0;
+          mine = bytes[0];
+        } else {
 #pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          if (!small_copy<KD, QMAX, DF>(p, lane + 32 * c, mj.n, mj.bos, mj.s, jh, sl, &src[c], &dst[c], &bytes[c]))
-            bytes[c] = 0;
-          mine += bytes[c];
+          for (int c = 0; c < 3; ++c) {
+            if (!small_copy<KD, QMAX, DF>(p, lane + 32 * c, mj.n, mj.bos, mj.s, jh, sl, &src[c], &dst[c], &bytes[c]))
+              bytes[c] = 0;
+            mine += bytes[c];
+          }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);

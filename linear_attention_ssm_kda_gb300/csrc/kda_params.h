@@ -2,6 +2,7 @@
 // structs of device pointers, built by the host API from the C-ABI arguments.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <stdint.h>
 
 namespace kda {
@@ -24,6 +25,13 @@ struct VerifyParams {
   const int* qsl; const int* state_indices; const int* record_indices; const int* num_accepted_prev;
   int* workspace;
   float k_scale;  // K^-1/2
+  // Small-input copies of the verify.  act_mode 0: one bulk copy per 16-byte
+  // hull of each row segment (any 2-byte alignment).  Otherwise tensor copies
+  // (TMA tiles) fetch an item's q | k | v rows (1: with the gate rows, which
+  // then follow v in the same rows; 2: gate rows by tm_gate), its conv taps
+  // (tm_conv) and conv weights (tm_w), built by the host for this call.
+  int act_mode;
+  CUtensorMap tm_act, tm_gate, tm_conv, tm_w;
 };
 
 struct CommitParams {

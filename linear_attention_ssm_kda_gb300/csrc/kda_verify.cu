@@ -38,7 +38,10 @@
 //                    its rows.
 // Every wait is bounded; a timeout sets KDA_DEVERR_TIMEOUT and an abort flag
 // that stops the other roles.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "kda_device.cuh"
 
@@ -88,10 +91,10 @@ struct Layout {
   static constexpr int kNumSmall = QMAX <= 4 ? 3 : 2;  // small-input ring
   // small slot
   static constexpr int kAct = ru(int(sizeof(SmallMeta<QMAX>)), 128);  // [QMAX][3] hulls
-  static constexpr int kGate = kAct + QMAX * 3 * kSeg;                 // [QMAX] hulls
-  static constexpr int kConv = ru(kGate + QMAX * kSeg, 16);            // the head's conv taps
-  static constexpr int kW = ru(kConv + 3 * KD * kLcMax * 2, 16);       // [3][KD][W] weights
-  static constexpr int kDt = kW + 3 * KD * kConvWidth * 4;             // [KD] dt_bias
+  static constexpr int kGate = ru(kAct + QMAX * 3 * kSeg, 128);       // [QMAX] hulls
+  static constexpr int kConv = ru(kGate + QMAX * kSeg, 128);           // the head's conv taps
+  static constexpr int kW = ru(kConv + 3 * KD * kLcMax * 2, 128);      // [3][KD][W] weights
+  static constexpr int kDt = ru(kW + 3 * KD * kConvWidth * 4, 128);    // [KD] dt_bias
   static constexpr int kSmall = ru(kDt + KD * 4, 128);
   // operand slot (prep -> gemv)
   static constexpr int kOpVec = ru(int(sizeof(OpMeta<QMAX>)), 16);    // [2 QMAX][KD] X_t | Y_t
@@ -152,7 +155,7 @@ __device__ __forceinline__ long long shfl_ll(long long v, int src) {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane, const volatile int* abort_flag) {
   bool ok = true;
   if (lane == 0) ok = mbar_wait_or_abort(bar, parity, abort_flag);
-  ok = __shfl_sync(0xffffffffu, ok, 0);
+  ok = __all_sync(0xffffffffu, ok);
   if (ok && lane != 0) mbar_acquire_seen(bar, parity);
   return ok;
 }
@@ -328,27 +331,53 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
       beta[t] = (im.flags == kLive && t < im.n)
                     ? sigmoid_fast(bf16_to_f32(p.raw_beta[static_cast<long long>(im.bos + t) * p.beta_stride + im.h]))
                     : 0.0f;
+    // lane j's own item: the per-item header the prep team reads
+    SmallMeta<QMAX> own;
+    own.flags = im.flags;
+    own.bos = im.bos;
+    own.n = im.n;
+    own.a = im.a;
+    own.s = im.s;
+    own.r = im.r;
+    own.A = A;
+    own.pad = 0.0f;
+#pragma unroll
+    for (int t = 0; t < QMAX; ++t) own.beta[t] = beta[t];
     const int count = min(32, nloc - i0);
     for (int j = 0; j < count && ok; ++j) {
       const int i = i0 + j;
-      SmallMeta<QMAX> mj;
-      mj.flags = __shfl_sync(0xffffffffu, im.flags, j);
-      mj.bos = __shfl_sync(0xffffffffu, im.bos, j);
-      mj.n = __shfl_sync(0xffffffffu, im.n, j);
-      mj.a = __shfl_sync(0xffffffffu, im.a, j);
-      mj.s = shfl_ll(im.s, j);
-      mj.r = shfl_ll(im.r, j);
-      mj.A = __shfl_sync(0xffffffffu, A, j);
-      mj.pad = 0.0f;
-#pragma unroll
-      for (int t = 0; t < QMAX; ++t) mj.beta[t] = __shfl_sync(0xffffffffu, beta[t], j);
+      const int jflags = __shfl_sync(0xffffffffu, im.flags, j);
+      const int jbos = __shfl_sync(0xffffffffu, im.bos, j);
+      const int jn = __shfl_sync(0xffffffffu, im.n, j);
+      const long long js = shfl_ll(im.s, j);
       const int jh = __shfl_sync(0xffffffffu, im.h, j);
       const int slot = i % Lay::kNumSmall;
       ok = warp_wait(&bars.sm_empty[slot], ((i / Lay::kNumSmall) & 1) ^ 1, lane, abort_flag);
       if (!ok) break;
       unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
-      if (lane == 0) *reinterpret_cast<SmallMeta<QMAX>*>(sl) = mj;
-      if (mj.flags & kLive) {
+      if (lane == j) *reinterpret_cast<SmallMeta<QMAX>*>(sl) = own;
+      __syncwarp();  // orders lane j's header before lane 0's arrival on sm_full
+      if ((jflags & kLive) && p.act_mode != 0) {
+        // four or five tensor / bulk copies, all from lane 0
+        if (lane == 0) {
+          const int Lc = p.Q + kConvWidth - 2;
+          const int wb = p.conv_weight_fp32 ? 4 : 2;
+          const int G = p.act_mode == 1 ? 4 : 3;
+          const uint32_t total = KD * G * p.Q * 2 + (p.act_mode == 2 ? KD * p.Q * 2 : 0) + 3 * KD * Lc * 2 +
+                                 3 * KD * kConvWidth * wb + KD * 4;
+          uint64_t* bar = &bars.sm_full[slot];
+          mbar_arrive_expect_tx(bar, total);
+          tma_load_3d(sl + Lay::kAct, &p.tm_act, jh * KD, 0, jbos, bar);
+          if (p.act_mode == 2) tma_load_2d(sl + Lay::kGate, &p.tm_gate, jh * KD, jbos, bar);
+          if (DF)
+            tma_load_4d(sl + Lay::kConv, &p.tm_conv, 0, jh * KD * Lc / 128, 0, static_cast<int>(js), bar);
+          else
+            tma_load_4d(sl + Lay::kConv, &p.tm_conv, jh * KD, 0, 0, static_cast<int>(js), bar);
+          tma_load_3d(sl + Lay::kW, &p.tm_w, 0, jh * KD * kConvWidth / 128, 0, bar);
+          bulk_g2s(sl + Lay::kDt, p.dt_bias + static_cast<long long>(jh) * KD, KD * 4, bar);
+        }
+        __syncwarp();
+      } else if (jflags & kLive) {
         // at most 7 QMAX + 10 copies, three per lane; the barrier expects every
         // byte before the first copy can land
         const void* src[3];
@@ -356,19 +385,18 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
         uint32_t bytes[3] = {0, 0, 0};
         uint32_t mine = 0;
         if (DF && 4 * QMAX + 7 <= 32) {  // one copy per lane, computed without branches
-          if (!small_copy_lane<KD, QMAX>(p, lane, mj.n, mj.bos, mj.s, jh, sl, &src[0], &dst[0], &bytes[0]))
+          if (!small_copy_lane<KD, QMAX>(p, lane, jn, jbos, js, jh, sl, &src[0], &dst[0], &bytes[0]))
             bytes[0] = 0;
           mine = bytes[0];
         } else {
 #pragma unroll
           for (int c = 0; c < 3; ++c) {
-            if (!small_copy<KD, QMAX, DF>(p, lane + 32 * c, mj.n, mj.bos, mj.s, jh, sl, &src[c], &dst[c], &bytes[c]))
+            if (!small_copy<KD, QMAX, DF>(p, lane + 32 * c, jn, jbos, js, jh, sl, &src[c], &dst[c], &bytes[c]))
               bytes[c] = 0;
             mine += bytes[c];
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        mine = __reduce_add_sync(0xffffffffu, mine);
         if (lane == 0) mbar_arrive_expect_tx(&bars.sm_full[slot], mine);
         __syncwarp();
 #pragma unroll
@@ -444,9 +472,10 @@ __device__ __forceinline__ void reduce_scatter_stage(float* acc, int mask, bool 
 // copy of the conv state.
 template <int KD, int QMAX, bool DF>
 __device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsigned char* sl, int g, int k, int n,
-                                             int a, int Lc, uint32_t act_lo, uint16_t (&y)[QMAX]) {
+                                             int a, int Lc, uint32_t act_lo, uint16_t* gconv, long long hk,
+                                             uint16_t (&y)[QMAX]) {
   using Lay = Layout<KD, QMAX>;
-  uint16_t* conv = reinterpret_cast<uint16_t*>(const_cast<unsigned char*>(sl) + Lay::kConv);
+  const uint16_t* conv = reinterpret_cast<const uint16_t*>(sl + Lay::kConv);
   float w[kConvWidth];
   if (p.conv_weight_fp32) {
     const float4 wv = reinterpret_cast<const float4*>(sl + Lay::kW)[g * KD + k];
@@ -465,12 +494,17 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsign
   for (int t = 0; t < QMAX; ++t) {
     seq[kConvWidth - 1 + t] = 0;
     if (t < n) {
-      // the activation hull of (token t, group g) starts act_lo + 16-byte
-      // multiples before the segment: the segment's offset is its address mod 16
-      const uint32_t off = (act_lo + static_cast<uint32_t>(t) * static_cast<uint32_t>(p.qkv_stride) * 2u +
-                            static_cast<uint32_t>(g) * static_cast<uint32_t>(p.H) * KD * 2u) & 15u;
-      seq[kConvWidth - 1 + t] =
-          *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + (t * 3 + g) * Lay::kSeg + off + 2 * k);
+      if (p.act_mode == 0) {
+        // the activation hull of (token t, group g) starts act_lo + 16-byte
+        // multiples before the segment: the segment's offset is its address mod 16
+        const uint32_t off = (act_lo + static_cast<uint32_t>(t) * static_cast<uint32_t>(p.qkv_stride) * 2u +
+                              static_cast<uint32_t>(g) * static_cast<uint32_t>(p.H) * KD * 2u) & 15u;
+        seq[kConvWidth - 1 + t] =
+            *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + (t * 3 + g) * Lay::kSeg + off + 2 * k);
+      } else {  // tensor tile [t][q | k | v (| gate)][K]
+        const int G = p.act_mode == 1 ? 4 : 3;
+        seq[kConvWidth - 1 + t] = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * G + g) * KD + k) * 2);
+      }
     }
   }
 #pragma unroll
@@ -486,14 +520,17 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsign
       if (t + 1 < n) y[t + 1] = static_cast<uint16_t>(yy >> 16);
     }
   }
-  // rolled conv state: taps 0 .. W-3+n <- seq[1 .. W-2+n]
+  // rolled conv state, straight to the slot in global memory:
+  // taps 0 .. W-3+n <- seq[1 .. W-2+n]; later taps are left as they are
+  const long long HK = static_cast<long long>(p.H) * KD;
+  const long long c = g * HK + hk + k;
 #pragma unroll
   for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
     if (j < kConvWidth - 2 + n) {
       if (DF)
-        conv[(g * KD + k) * Lc + j] = seq[j + 1];
+        gconv[c * Lc + j] = seq[j + 1];
       else
-        conv[(j * 3 + g) * KD + k] = seq[j + 1];
+        gconv[j * 3 * HK + c] = seq[j + 1];
     }
   }
 }
@@ -539,6 +576,8 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
     }
     if (live) {
       const uint32_t act_lo = qkv_lo + static_cast<uint32_t>(m.bos) * static_cast<uint32_t>(p.qkv_stride) * 2u + hoff;
+      uint16_t* gconv = p.conv_state + m.s * p.conv_slot_stride;
+      const long long hk = static_cast<long long>(h) * KD;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = pt + cc * kPrepConvThreads;
@@ -546,7 +585,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
           const int g = c / KD;
           const int k = c - g * KD;
           uint16_t y[QMAX];
-          conv_channel<KD, QMAX, DF>(p, sl, g, k, n, m.a, Lc, act_lo, y);
+          conv_channel<KD, QMAX, DF>(p, sl, g, k, n, m.a, Lc, act_lo, gconv, hk, y);
           if (g < 2) {
 #pragma unroll
             for (int t = 0; t < QMAX; ++t) xs[(g * QMAX + t) * KD + k] = bf16_to_f32(y[t]);
@@ -563,25 +602,9 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
           }
         }
       }
-      fence_async_shared();  // the rolled taps leave by bulk stores
     }
     named_barrier(kBarPrep, kPrepConvThreads);
     if (misc[kMiscPrepFail]) break;  // every prep thread sees the same flag here
-    if (live && pt == 0) {  // the rolled conv state leaves by bulk stores from the slot
-      uint16_t* cs = p.conv_state + m.s * p.conv_slot_stride;
-      if (DF) {
-#pragma unroll
-        for (int g = 0; g < 3; ++g)
-          bulk_s2g(cs + (g * HK + static_cast<long long>(h) * KD) * Lc, sl + Lay::kConv + g * KD * Lc * 2, KD * Lc * 2);
-      } else {
-        for (int j = 0; j < kConvWidth - 2 + n; ++j)
-#pragma unroll
-          for (int g = 0; g < 3; ++g)
-            bulk_s2g(cs + j * 3 * HK + g * HK + static_cast<long long>(h) * KD, sl + Lay::kConv + (j * 3 + g) * KD * 2,
-                     KD * 2);
-      }
-      bulk_commit();
-    }
 
     // ---- gates, gate record and the per-channel partial sums: key channel k = pt ----
     float qv[QMAX], kv[QMAX], eg[QMAX];
@@ -594,9 +617,16 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
         kv[t] = xs[(QMAX + t) * KD + k];
         eg[t] = 0.0f;
         if (t < n) {
-          const uint32_t goff =
-              (gate_lo + static_cast<uint32_t>(m.bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
-          const uint16_t rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
+          uint16_t rg;
+          if (p.act_mode == 0) {
+            const uint32_t goff =
+                (gate_lo + static_cast<uint32_t>(m.bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
+            rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
+          } else if (p.act_mode == 1) {  // gate rows follow v in the q | k | v | gate tile
+            rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * 4 + 3) * KD + k) * 2);
+          } else {
+            rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + (t * KD + k) * 2);
+          }
           kg[t * 2 * KD + KD + k] = rg;  // gate record: bit copy
           eg[t] = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
         } else {
@@ -635,6 +665,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       for (int v = 0; v < PER; ++v) part[warp * NREDP + lane * PER + v] = vals[v];
     }
     named_barrier(kBarPrep, kPrepConvThreads);
+    if (pt == 0) mbar_arrive(&bars.sm_empty[slot]);  // the small inputs are consumed
 
     // ---- norms, the operands X_t = D_t k^_t, Y_t = D_t q^_t, M and N ----
     if (live && pt < KD) {
@@ -687,13 +718,8 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       for (int t = 0; t < QMAX; ++t) om->beta[t] = m.beta[t];
     }
     named_barrier(kBarPrep, kPrepConvThreads);
-    if (pt == 0) {
-      mbar_arrive(&bars.op_full[oslot]);
-      bulk_wait_read();  // the small inputs are consumed once the bulk stores have read them
-      mbar_arrive(&bars.sm_empty[slot]);
-    }
+    if (pt == 0) mbar_arrive(&bars.op_full[oslot]);
   }
-  if (pt == 0) bulk_wait_all();
   if (misc[kMiscPrepFail] && pt == 0) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
@@ -913,7 +939,7 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
 }
 
 template <int KD, int QMAX, bool DF>
-__global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kThreads, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
   using Lay = Layout<KD, QMAX>;
   extern __shared__ __align__(1024) unsigned char smem[];
   volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::oMisc);
@@ -948,6 +974,103 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const VerifyParams 
   }
 }
 
+// ---------------------------------------------------------------- tensor maps (host)
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).
+EncodeTiledFn tensor_map_encoder() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const cuuint64_t* dims,
+                const cuuint64_t* strides, const cuuint32_t* box) {
+  const EncodeTiledFn fn = tensor_map_encoder();
+  if (fn == nullptr) return false;
+  const cuuint32_t unit[5] = {1, 1, 1, 1, 1};
+  return fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, unit,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps for the small inputs when every start and stride they need is
+// 16-byte aligned; otherwise act_mode stays 0 (per-segment hull copies).
+//   q | k | v (| gate): dims {HK, 3 or 4 groups, T}, box {K, groups, Q}, at
+//     {h K, 0, bos}; rows past T arrive as zeros;
+//   gate (separate): dims {HK, T}, box {K, Q}, at {h K, bos};
+//   conv taps, dim-first [slots][3HK][Lc]: dims {128, HK Lc / 128, 3, slots},
+//     box {128, K Lc / 128, 3, 1}, at {0, h K Lc / 128, 0, s};
+//     seq-first [slots][Lc][3HK]: dims {HK, 3, Lc, slots}, box {K, 3, Lc, 1},
+//     at {h K, 0, 0, s};
+//   conv weights [3HK][W]: dims {128, HK W / 128, 3}, box {128, K W / 128, 3},
+//     at {0, h K W / 128, 0}.
+// Every box lands in the layout the hull copies would give, except q | k | v
+// (| gate), which lands as [t][group][K].
+void build_tensor_maps(VerifyParams& p, int KD) {
+  p.act_mode = 0;
+  const cuuint64_t H = static_cast<cuuint64_t>(p.H), K = static_cast<cuuint64_t>(KD), HK = H * K;
+  const cuuint64_t T = static_cast<cuuint64_t>(p.T), Q = static_cast<cuuint64_t>(p.Q);
+  const cuuint64_t Lc = Q + kConvWidth - 2, W = kConvWidth;
+  const cuuint64_t wb = p.conv_weight_fp32 ? 4 : 2;
+  auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+  if (!al16(p.mixed_qkv) || (p.qkv_stride * 2) % 16 != 0) return;
+  int mode;
+  if (p.raw_gate == p.mixed_qkv + 3 * HK && p.gate_stride == p.qkv_stride &&
+      static_cast<cuuint64_t>(p.qkv_stride) >= 4 * HK)
+    mode = 1;
+  else if (al16(p.raw_gate) && (p.gate_stride * 2) % 16 == 0)
+    mode = 2;
+  else
+    return;
+  if (p.conv_dim_first && (K * Lc) % 128 != 0) return;
+  if ((K * W) % 128 != 0 || !al16(p.conv_state) || (p.conv_slot_stride * 2) % 16 != 0 || !al16(p.conv_weight)) return;
+  const cuuint64_t groups = mode == 1 ? 4 : 3;
+  {
+    const cuuint64_t dims[3] = {HK, groups, T};
+    const cuuint64_t strides[2] = {HK * 2, static_cast<cuuint64_t>(p.qkv_stride) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(K), static_cast<cuuint32_t>(groups), static_cast<cuuint32_t>(Q)};
+    if (!encode_map(&p.tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.mixed_qkv, dims, strides, box)) return;
+  }
+  if (mode == 2) {
+    const cuuint64_t dims[2] = {HK, T};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.gate_stride) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(K), static_cast<cuuint32_t>(Q)};
+    if (!encode_map(&p.tm_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.raw_gate, dims, strides, box)) return;
+  }
+  const cuuint64_t slots = static_cast<cuuint64_t>(p.num_slots);
+  if (p.conv_dim_first) {
+    const cuuint64_t dims[4] = {128, HK * Lc / 128, 3, slots};
+    const cuuint64_t strides[3] = {256, HK * Lc * 2, static_cast<cuuint64_t>(p.conv_slot_stride) * 2};
+    const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(K * Lc / 128), 3, 1};
+    if (!encode_map(&p.tm_conv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.conv_state, dims, strides, box)) return;
+  } else {
+    const cuuint64_t dims[4] = {HK, 3, Lc, slots};
+    const cuuint64_t strides[3] = {HK * 2, 3 * HK * 2, static_cast<cuuint64_t>(p.conv_slot_stride) * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(K), 3, static_cast<cuuint32_t>(Lc), 1};
+    if (!encode_map(&p.tm_conv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.conv_state, dims, strides, box)) return;
+  }
+  {
+    const cuuint64_t dims[3] = {128, HK * W / 128, 3};
+    const cuuint64_t strides[2] = {128 * wb, HK * W * wb};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(K * W / 128), 3};
+    const CUtensorMapDataType dt = p.conv_weight_fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_map(&p.tm_w, dt, 3, p.conv_weight, dims, strides, box)) return;
+  }
+  p.act_mode = mode;
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -973,7 +1096,9 @@ cudaError_t launch(const VerifyParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_verify(const VerifyParams& p, int K, cudaStream_t stream) {
+cudaError_t launch_verify(const VerifyParams& params, int K, cudaStream_t stream) {
+  VerifyParams p = params;
+  build_tensor_maps(p, K);
   // the conv-state layout is a template parameter: straight-line tap addressing
   if (p.conv_dim_first) {
     if (K == 128) return p.Q <= 4 ? launch<128, 4, true>(p, stream) : launch<128, 8, true>(p, stream);

@@ -467,71 +467,111 @@ __device__ __forceinline__ void reduce_scatter_stage(float* acc, int mask, bool 
   }
 }
 
-// Conv + SiLU of channel k of group g (q | k | v) over the window: the bf16
-// codes of the n outputs, and the rolled taps written back into the slot's
-// copy of the conv state.
+// Conv + SiLU of one channel (group g of q | k | v, key index k) over the
+// window, in three steps so that a thread's channels run interleaved:
+// conv_load reads the weights, the W - 1 stored taps and the window inputs
+// (zero past n); conv_pairs evaluates NP token pairs on the packed fp32x2 unit
+// without branches; conv_roll stores the rolled taps to the slot in global
+// memory (taps 0 .. W-3+n <- seq[1 .. W-2+n]; later taps are left as they are).
+template <int QMAX>
+struct ConvIn {
+  float w[kConvWidth];
+  uint16_t seq[kConvWidth - 1 + QMAX + 1];
+};
+
 template <int KD, int QMAX, bool DF>
-__device__ __forceinline__ void conv_channel(const VerifyParams& p, const unsigned char* sl, int g, int k, int n,
-                                             int a, int Lc, uint32_t act_lo, uint16_t* gconv, long long hk,
-                                             uint16_t (&y)[QMAX]) {
+__device__ __forceinline__ void conv_load(const VerifyParams& p, const unsigned char* sl, int g, int k, int n, int a,
+                                          int Lc, uint32_t act_lo, ConvIn<QMAX>& in) {
   using Lay = Layout<KD, QMAX>;
   const uint16_t* conv = reinterpret_cast<const uint16_t*>(sl + Lay::kConv);
-  float w[kConvWidth];
   if (p.conv_weight_fp32) {
     const float4 wv = reinterpret_cast<const float4*>(sl + Lay::kW)[g * KD + k];
-    w[0] = wv.x; w[1] = wv.y; w[2] = wv.z; w[3] = wv.w;
+    in.w[0] = wv.x; in.w[1] = wv.y; in.w[2] = wv.z; in.w[3] = wv.w;
   } else {
     const uint2 wv = reinterpret_cast<const uint2*>(sl + Lay::kW)[g * KD + k];
-    w[0] = bf16_to_f32(wv.x & 0xffff); w[1] = bf16_to_f32(wv.x >> 16);
-    w[2] = bf16_to_f32(wv.y & 0xffff); w[3] = bf16_to_f32(wv.y >> 16);
+    in.w[0] = bf16_to_f32(wv.x & 0xffff); in.w[1] = bf16_to_f32(wv.x >> 16);
+    in.w[2] = bf16_to_f32(wv.y & 0xffff); in.w[3] = bf16_to_f32(wv.y >> 16);
   }
-  uint16_t seq[kConvWidth - 1 + QMAX + 1];
-  seq[kConvWidth - 1 + QMAX] = 0;
+  in.seq[kConvWidth - 1 + QMAX] = 0;
 #pragma unroll
   for (int j = 0; j < kConvWidth - 1; ++j)
-    seq[j] = DF ? conv[(g * KD + k) * Lc + a - 1 + j] : conv[((a - 1 + j) * 3 + g) * KD + k];
+    in.seq[j] = DF ? conv[(g * KD + k) * Lc + a - 1 + j] : conv[((a - 1 + j) * 3 + g) * KD + k];
 #pragma unroll
   for (int t = 0; t < QMAX; ++t) {
-    seq[kConvWidth - 1 + t] = 0;
-    if (t < n) {
-      if (p.act_mode == 0) {
-        // the activation hull of (token t, group g) starts act_lo + 16-byte
-        // multiples before the segment: the segment's offset is its address mod 16
-        const uint32_t off = (act_lo + static_cast<uint32_t>(t) * static_cast<uint32_t>(p.qkv_stride) * 2u +
-                              static_cast<uint32_t>(g) * static_cast<uint32_t>(p.H) * KD * 2u) & 15u;
-        seq[kConvWidth - 1 + t] =
-            *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + (t * 3 + g) * Lay::kSeg + off + 2 * k);
-      } else {  // tensor tile [t][q | k | v (| gate)][K]
-        const int G = p.act_mode == 1 ? 4 : 3;
-        seq[kConvWidth - 1 + t] = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * G + g) * KD + k) * 2);
-      }
+    uint16_t x;
+    if (p.act_mode == 0) {
+      // the activation hull of (token t, group g) starts act_lo + 16-byte
+      // multiples before the segment: the segment's offset is its address mod 16
+      const uint32_t off = (act_lo + static_cast<uint32_t>(t) * static_cast<uint32_t>(p.qkv_stride) * 2u +
+                            static_cast<uint32_t>(g) * static_cast<uint32_t>(p.H) * KD * 2u) & 15u;
+      x = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + (t * 3 + g) * Lay::kSeg + off + 2 * k);
+    } else {  // tensor tile [t][q | k | v (| gate)][K]
+      const int G = p.act_mode == 1 ? 4 : 3;
+      x = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * G + g) * KD + k) * 2);
     }
+    in.seq[kConvWidth - 1 + t] = t < n ? x : static_cast<uint16_t>(0);  // slots past n hold no token
   }
+}
+
+template <int NP, int QMAX>
+__device__ __forceinline__ void conv_pairs(const ConvIn<QMAX>& in, uint16_t (&y)[QMAX]) {
 #pragma unroll
-  for (int t = 0; t < QMAX; t += 2) {  // token pairs on the packed fp32x2 unit
-    y[t] = y[t + 1] = 0;
-    if (t < n) {
-      const float xa[kConvWidth] = {bf16_to_f32(seq[t]), bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]),
-                                    bf16_to_f32(seq[t + 3])};
-      const float xb[kConvWidth] = {bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]), bf16_to_f32(seq[t + 3]),
-                                    bf16_to_f32(seq[t + 4])};
-      const uint32_t yy = conv_silu_bf16x2(w, xa, xb);
-      y[t] = static_cast<uint16_t>(yy & 0xffffu);
-      if (t + 1 < n) y[t + 1] = static_cast<uint16_t>(yy >> 16);
-    }
+  for (int t = 0; t < QMAX; ++t) y[t] = 0;
+#pragma unroll
+  for (int pr = 0; pr < NP; ++pr) {
+    const int t = 2 * pr;
+    const float xa[kConvWidth] = {bf16_to_f32(in.seq[t]), bf16_to_f32(in.seq[t + 1]), bf16_to_f32(in.seq[t + 2]),
+                                  bf16_to_f32(in.seq[t + 3])};
+    const float xb[kConvWidth] = {bf16_to_f32(in.seq[t + 1]), bf16_to_f32(in.seq[t + 2]),
+                                  bf16_to_f32(in.seq[t + 3]), bf16_to_f32(in.seq[t + 4])};
+    const uint32_t yy = conv_silu_bf16x2(in.w, xa, xb);
+    y[t] = static_cast<uint16_t>(yy & 0xffffu);
+    y[t + 1] = static_cast<uint16_t>(yy >> 16);
   }
-  // rolled conv state, straight to the slot in global memory:
-  // taps 0 .. W-3+n <- seq[1 .. W-2+n]; later taps are left as they are
+}
+
+template <int KD, int QMAX, bool DF>
+__device__ __forceinline__ void conv_roll(const VerifyParams& p, const ConvIn<QMAX>& in, int g, int k, int n, int Lc,
+                                          uint16_t* gconv, long long hk) {
   const long long HK = static_cast<long long>(p.H) * KD;
   const long long c = g * HK + hk + k;
 #pragma unroll
   for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
     if (j < kConvWidth - 2 + n) {
       if (DF)
-        gconv[c * Lc + j] = seq[j + 1];
+        gconv[c * Lc + j] = in.seq[j + 1];
       else
-        gconv[j * 3 * HK + c] = seq[j + 1];
+        gconv[j * 3 * HK + c] = in.seq[j + 1];
     }
+  }
+}
+
+// Both channels of a prep thread, their pairs interleaved: np = ceil(n / 2)
+// pairs each, the codes of tokens past n zeroed.
+template <int QMAX>
+__device__ __forceinline__ void conv_two(const ConvIn<QMAX>& in0, const ConvIn<QMAX>& in1, int n,
+                                         uint16_t (&y0)[QMAX], uint16_t (&y1)[QMAX]) {
+  const int np = (n + 1) >> 1;
+  if (QMAX <= 4) {
+    if (np <= 1) {
+      conv_pairs<1, QMAX>(in0, y0);
+      conv_pairs<1, QMAX>(in1, y1);
+    } else {
+      conv_pairs<(QMAX + 1) / 2, QMAX>(in0, y0);
+      conv_pairs<(QMAX + 1) / 2, QMAX>(in1, y1);
+    }
+  } else {
+    switch (np) {
+      case 1: conv_pairs<1, QMAX>(in0, y0); conv_pairs<1, QMAX>(in1, y1); break;
+      case 2: conv_pairs<2, QMAX>(in0, y0); conv_pairs<2, QMAX>(in1, y1); break;
+      case 3: conv_pairs<3, QMAX>(in0, y0); conv_pairs<3, QMAX>(in1, y1); break;
+      default: conv_pairs<(QMAX + 1) / 2, QMAX>(in0, y0); conv_pairs<(QMAX + 1) / 2, QMAX>(in1, y1); break;
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < QMAX; ++t) {
+    y0[t] = t < n ? y0[t] : static_cast<uint16_t>(0);
+    y1[t] = t < n ? y1[t] : static_cast<uint16_t>(0);
   }
 }
 
@@ -578,28 +618,44 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       const uint32_t act_lo = qkv_lo + static_cast<uint32_t>(m.bos) * static_cast<uint32_t>(p.qkv_stride) * 2u + hoff;
       uint16_t* gconv = p.conv_state + m.s * p.conv_slot_stride;
       const long long hk = static_cast<long long>(h) * KD;
+      // channels c0 = pt and c1 = pt + 192 of the head's 3K (q | k | v)
+      const int c0 = pt, c1 = pt + kPrepConvThreads;
+      const bool has1 = c1 < 3 * KD;
+      const int g0 = c0 / KD, k0 = c0 - g0 * KD;
+      const int g1 = c1 / KD, k1 = c1 - g1 * KD;
+      ConvIn<QMAX> in0, in1;
+      conv_load<KD, QMAX, DF>(p, sl, g0, k0, n, m.a, Lc, act_lo, in0);
+      if (has1) {
+        conv_load<KD, QMAX, DF>(p, sl, g1, k1, n, m.a, Lc, act_lo, in1);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kConvWidth; ++j) in1.w[j] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kConvWidth + QMAX; ++j) in1.seq[j] = 0;
+      }
+      uint16_t y0[QMAX], y1[QMAX];
+      conv_two<QMAX>(in0, in1, n, y0, y1);
+      conv_roll<KD, QMAX, DF>(p, in0, g0, k0, n, Lc, gconv, hk);
+      if (has1) conv_roll<KD, QMAX, DF>(p, in1, g1, k1, n, Lc, gconv, hk);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int c = pt + cc * kPrepConvThreads;
-        if (c < 3 * KD) {
-          const int g = c / KD;
-          const int k = c - g * KD;
-          uint16_t y[QMAX];
-          conv_channel<KD, QMAX, DF>(p, sl, g, k, n, m.a, Lc, act_lo, gconv, hk, y);
-          if (g < 2) {
+        if (cc == 1 && !has1) break;
+        const int g = cc == 0 ? g0 : g1;
+        const int k = cc == 0 ? k0 : k1;
+        const uint16_t(&y)[QMAX] = cc == 0 ? y0 : y1;
+        if (g < 2) {
 #pragma unroll
-            for (int t = 0; t < QMAX; ++t) xs[(g * QMAX + t) * KD + k] = bf16_to_f32(y[t]);
-            if (g == 1) {
-#pragma unroll
-              for (int t = 0; t < QMAX; ++t)
-                if (t < n) kg[t * 2 * KD + k] = y[t];  // key record: the bf16 conv output
-            }
-          } else {
-            float* opv = reinterpret_cast<float*>(op + Lay::kOpV);
+          for (int t = 0; t < QMAX; ++t) xs[(g * QMAX + t) * KD + k] = bf16_to_f32(y[t]);
+          if (g == 1) {
 #pragma unroll
             for (int t = 0; t < QMAX; ++t)
-              if (t < n) opv[t * KD + k] = bf16_to_f32(y[t]);
+              if (t < n) kg[t * 2 * KD + k] = y[t];  // key record: the bf16 conv output
           }
+        } else {
+          float* opv = reinterpret_cast<float*>(op + Lay::kOpV);
+#pragma unroll
+          for (int t = 0; t < QMAX; ++t)
+            if (t < n) opv[t * KD + k] = bf16_to_f32(y[t]);
         }
       }
     }
@@ -613,26 +669,24 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       const float dtb = reinterpret_cast<const float*>(sl + Lay::kDt)[k];
 #pragma unroll
       for (int t = 0; t < QMAX; ++t) {
-        qv[t] = xs[t * KD + k];
+        qv[t] = xs[t * KD + k];  // zero past n
         kv[t] = xs[(QMAX + t) * KD + k];
-        eg[t] = 0.0f;
-        if (t < n) {
-          uint16_t rg;
-          if (p.act_mode == 0) {
-            const uint32_t goff =
-                (gate_lo + static_cast<uint32_t>(m.bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
-            rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
-          } else if (p.act_mode == 1) {  // gate rows follow v in the q | k | v | gate tile
-            rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * 4 + 3) * KD + k) * 2);
-          } else {
-            rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + (t * KD + k) * 2);
-          }
-          kg[t * 2 * KD + KD + k] = rg;  // gate record: bit copy
-          eg[t] = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
+        // every slot of the window is read (rows past n hold other tokens,
+        // zeros or stale bytes) and the gate of a missing token is discarded,
+        // so the QMAX gates evaluate side by side without branches
+        uint16_t rg;
+        if (p.act_mode == 0) {
+          const uint32_t goff =
+              (gate_lo + static_cast<uint32_t>(m.bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
+          rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
+        } else if (p.act_mode == 1) {  // gate rows follow v in the q | k | v | gate tile
+          rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * 4 + 3) * KD + k) * 2);
         } else {
-          qv[t] = 0.0f;
-          kv[t] = 0.0f;
+          rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + (t * KD + k) * 2);
         }
+        const float e = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
+        eg[t] = t < n ? e : 0.0f;
+        if (t < n) kg[t * 2 * KD + KD + k] = rg;  // gate record: bit copy
       }
       // vals: [t] |q_t|^2, [QMAX + t] |k_t|^2, [2QMAX + t QMAX + u] k_u D_{u+1..t} k_t (u < t),
       //       [2QMAX + u QMAX + t] k_u D_{u+1..t} q_t (u <= t); zero past n (qv = kv = 0 there).

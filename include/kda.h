@@ -189,7 +189,11 @@ typedef struct kda_commit_args {
     int32_t *workspace;               /* zeroed kda_workspace_bytes(), or NULL     */
 } kda_commit_args;
 
-/* Enqueue the verify of one layer.  Returns before the kernel runs. */
+/* Enqueue the verify of one layer.  Returns before the kernel runs.
+ * With the environment variable KDA_VERIFY_TCGEN05=1 at the call, K == 128
+ * and Q <= 4, the products S0 [X | Y] run on tcgen05 tensor cores (tf32 with
+ * a hi/lo split of the state, same tolerances); the default is the CUDA-core
+ * kernel, which is faster on GB300. */
 kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
 
 /* Enqueue the commit of all layers (one kernel launch). */

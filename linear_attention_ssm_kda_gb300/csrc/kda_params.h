@@ -32,6 +32,9 @@ struct VerifyParams {
   // (tm_conv) and conv weights (tm_w), built by the host for this call.
   int act_mode;
   CUtensorMap tm_act, tm_gate, tm_conv, tm_w;
+  // fp32 state pool [slots][H V][K] in K-slices of 32 (128-byte swizzle), for
+  // the tensor-core path of the verify
+  CUtensorMap tm_state;
 };
 
 struct CommitParams {

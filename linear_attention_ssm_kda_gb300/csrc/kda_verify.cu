@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "kda_device.cuh"
@@ -53,12 +54,14 @@ constexpr int kConvWidth = 4;
 constexpr int kPrepWarps = 6;  // two conv channels per thread, then one key channel per thread
 constexpr int kGemvWarps = 8;  // one state row chunk (16 rows at K = 128) each
 constexpr int kPrepConvThreads = 32 * kPrepWarps;
-constexpr int kThreads = 32 * (2 + kPrepWarps + kGemvWarps);
 constexpr int kBarPrep = 1;
 constexpr int kSmemLimit = 227 * 1024;
 // misc ints in shared memory
 constexpr int kMiscAbort = 0;
 constexpr int kMiscPrepFail = 1;
+constexpr int kMiscTaddr = 4;  // tensor-memory base of the tensor-core path
+constexpr int kSplitWarps = 4;  // tensor-core path: warps 8 .. 11 form the low parts and read out the products
+constexpr int kMmaWarp = 2 + kPrepWarps + kSplitWarps;  // warp 12 issues the MMAs
 
 constexpr int ru(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -81,11 +84,17 @@ struct OpMeta {
   float beta[QMAX];
 };
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool TC>
 struct Layout {
   static_assert(7 * QMAX + 10 <= 96, "small-input copies per item exceed three per lane");
+  // Tensor-core instantiation (K = 128, windows up to 4 tokens): the state
+  // streams as K-slices of 32 (128 rows x 128 bytes, 128-byte swizzle) and the
+  // products S0 [X | Y] come from tcgen05 MMAs; otherwise CUDA-core gemv warps.
+  static_assert(!TC || (KD == 128 && QMAX == 4), "the tensor-core path covers K = 128, windows up to 4");
+  static constexpr bool kTC = TC;
+  static constexpr int kThreads = 32 * (kTC ? kMmaWarp + 1 : 2 + kPrepWarps + kGemvWarps);
   static constexpr int RW = KD / kGemvWarps;  // state rows per gemv warp (one chunk)
-  static constexpr int kChunk = RW * KD * 4;  // bytes per state chunk
+  static constexpr int kChunk = kTC ? 128 * 32 * 4 : RW * KD * 4;  // bytes per state unit (chunk or K-slice)
   static constexpr int kLcMax = QMAX + kConvWidth - 2;
   static constexpr int kSeg = KD * 2 + 16;    // hull of one row segment
   static constexpr int kNumSmall = QMAX <= 4 ? 3 : 2;  // small-input ring
@@ -96,41 +105,48 @@ struct Layout {
   static constexpr int kW = ru(kConv + 3 * KD * kLcMax * 2, 128);      // [3][KD][W] weights
   static constexpr int kDt = ru(kW + 3 * KD * kConvWidth * 4, 128);    // [KD] dt_bias
   static constexpr int kSmall = ru(kDt + KD * 4, 128);
-  // operand slot (prep -> gemv)
-  static constexpr int kOpVec = ru(int(sizeof(OpMeta<QMAX>)), 16);    // [2 QMAX][KD] X_t | Y_t
-  static constexpr int kOpV = kOpVec + 2 * QMAX * KD * 4;              // [QMAX][KD] v_t
-  static constexpr int kOpMN = kOpV + QMAX * KD * 4;                   // [QMAX][QMAX] M | N
-  static constexpr int kOp = ru(kOpMN + QMAX * QMAX * 4, 128);
-  static constexpr int kNumOp = QMAX <= 4 ? 3 : 2;  // prep runs up to two items ahead of the gemv team
+  // operand slot (prep -> gemv).  Tensor-core path: first the MMA's B operand,
+  // [X | Y]_hi rows 0..7 and [X | Y]_lo rows 8..15, as four K-slices of
+  // [16][32] fp32 with the 128-byte swizzle (8 KB), then the rest.
+  static constexpr int kOpMeta = kTC ? 4 * 2048 : 0;
+  static constexpr int kOpVec = ru(kOpMeta + int(sizeof(OpMeta<QMAX>)), 16);  // [2 QMAX][KD] X_t | Y_t
+  static constexpr int kOpV = kTC ? kOpVec : kOpVec + 2 * QMAX * KD * 4;        // [QMAX][KD] v_t
+  static constexpr int kOpMN = kOpV + QMAX * KD * 4;                            // [QMAX][QMAX] M | N
+  static constexpr int kOp = ru(kOpMN + QMAX * QMAX * 4, kTC ? 1024 : 128);
+  // prep runs up to two items ahead of the gemv team; on the tensor-core path
+  // an item's slot is also held until its readout, one item later
+  static constexpr int kNumOp = kTC ? 4 : QMAX <= 4 ? 3 : 2;
   // per-item scratch of the prep team
   static constexpr int kXs = 2 * QMAX * KD * 4;                        // [2][QMAX][KD] q | k conv outputs
   // per-warp scratch
-  static constexpr int kRedPerWarp = 2 * QMAX * RW;                    // floats
+  static constexpr int kRedPerWarp = kTC ? 0 : 2 * QMAX * RW;         // floats
   static constexpr int kPart = ru(2 * QMAX + QMAX * QMAX, 32);         // reduced values per prep warp
   static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kXs + kGemvWarps * kRedPerWarp * 4 +
-                                kPrepWarps * kPart * 4 + 32 + (2 * kNumSmall + 2 * kNumOp) * 8;
-  static constexpr int kChunkFit = (kSmemLimit - kFixed - 64 * 2 * 8) / kChunk;
+                                kPrepWarps * kPart * 4 + 32 + (2 * kNumSmall + 2 * kNumOp + 4) * 8 +
+                                (kTC ? 1024 : 0);
+  static constexpr int kBarsPerChunk = kTC ? 4 : 2;
+  static constexpr int kChunkFit = (kSmemLimit - kFixed - 64 * kBarsPerChunk * 8) / kChunk;
   static constexpr int kNumChunk = kChunkFit > 64 ? 64 : kChunkFit;
   // CTA layout
   static constexpr int oChunks = 0;
   static constexpr int oSmall = oChunks + kNumChunk * kChunk;
-  static constexpr int oOp = oSmall + kNumSmall * kSmall;
+  static constexpr int oOp = ru(oSmall + kNumSmall * kSmall, kTC ? 1024 : 128);
   static constexpr int oXs = oOp + kNumOp * kOp;
   static constexpr int oRed = oXs + kXs;
   static constexpr int oPart = oRed + kGemvWarps * kRedPerWarp * 4;
   static constexpr int oMisc = oPart + kPrepWarps * kPart * 4;  // int[8]
   static constexpr int oBars = ru(oMisc + 32, 8);
-  static constexpr int kNumBars = 2 * kNumChunk + 2 * kNumSmall + 2 * kNumOp;
+  static constexpr int kNumBars = kBarsPerChunk * kNumChunk + 2 * kNumSmall + 2 * kNumOp + 4;
   static constexpr int kBytes = oBars + kNumBars * 8;
   static_assert(kBytes <= kSmemLimit, "shared memory budget");
-  static_assert(kNumChunk >= 2 * kGemvWarps, "at least two items of state in flight");
+  static_assert(kTC ? kNumChunk >= 6 : kNumChunk >= 2 * kGemvWarps, "state in flight");
 };
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool TC>
 struct Bars {
-  uint64_t *ch_full, *ch_empty, *sm_full, *sm_empty, *op_full, *op_empty;
+  uint64_t *ch_full, *ch_empty, *sm_full, *sm_empty, *op_full, *op_empty, *d_full, *d_empty, *hi_done, *lo_full;
   __device__ explicit Bars(unsigned char* smem) {
-    using Lay = Layout<KD, QMAX>;
+    using Lay = Layout<KD, QMAX, TC>;
     uint64_t* b = reinterpret_cast<uint64_t*>(smem + Lay::oBars);
     ch_full = b;
     ch_empty = b + Lay::kNumChunk;
@@ -138,6 +154,10 @@ struct Bars {
     sm_empty = sm_full + Lay::kNumSmall;
     op_full = sm_empty + Lay::kNumSmall;
     op_empty = op_full + Lay::kNumOp;
+    d_full = op_empty + Lay::kNumOp;   // [2] tensor-core path
+    d_empty = d_full + 2;              // [2]
+    hi_done = d_empty + 2;             // [kNumChunk]
+    lo_full = hi_done + Lay::kNumChunk;  // [kNumChunk]
   }
 };
 
@@ -212,10 +232,10 @@ __device__ __forceinline__ int hull_offset(const void* src) {
 // order: 3n activation row segments (token t, group g), n gate row segments,
 // the head's conv taps (3 blocks dim-first, 3 (Q+W-2) rows seq-first), three
 // conv-weight blocks and dt_bias.  Returns false past the last copy.
-template <int KD, int QMAX, bool DF>
+template <int KD, int QMAX, bool DF, bool TC>
 __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, int bos, long long s, int h,
                                            unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
-  using Lay = Layout<KD, QMAX>;
+  using Lay = Layout<KD, QMAX, TC>;
   const long long HK = static_cast<long long>(p.H) * KD;
   const int Lc = p.Q + kConvWidth - 2;
   const unsigned char* ptr;
@@ -273,10 +293,10 @@ __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, 
 // Kinds by lane q: activation (t = q / 3, g = q % 3) for q < 3n, gate
 // (t = q - 3n) for q < 4n, conv taps of group q - 4n, conv weights of group
 // q - 4n - 3, dt_bias at q = 4n + 6.  Returns false for lanes past the last copy.
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool TC>
 __device__ __forceinline__ bool small_copy_lane(const VerifyParams& p, int q, int n, int bos, long long s, int h,
                                                 unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
-  using Lay = Layout<KD, QMAX>;
+  using Lay = Layout<KD, QMAX, TC>;
   const long long HK = static_cast<long long>(p.H) * KD;
   const int Lc = p.Q + kConvWidth - 2;
   const int wb = p.conv_weight_fp32 ? 4 : 2;
@@ -314,10 +334,10 @@ __device__ __forceinline__ bool small_copy_lane(const VerifyParams& p, int q, in
 
 // ---------------------------------------------------------------- inputs warp
 
-template <int KD, int QMAX, bool DF>
+template <int KD, int QMAX, bool DF, bool TC>
 __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
-  using Lay = Layout<KD, QMAX>;
-  Bars<KD, QMAX> bars(smem);
+  using Lay = Layout<KD, QMAX, TC>;
+  Bars<KD, QMAX, TC> bars(smem);
   const int nloc = local_items(p.B * p.H);
   bool ok = true;
   for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
@@ -385,13 +405,13 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
         uint32_t bytes[3] = {0, 0, 0};
         uint32_t mine = 0;
         if (DF && 4 * QMAX + 7 <= 32) {  // one copy per lane, computed without branches
-          if (!small_copy_lane<KD, QMAX>(p, lane, jn, jbos, js, jh, sl, &src[0], &dst[0], &bytes[0]))
+          if (!small_copy_lane<KD, QMAX, TC>(p, lane, jn, jbos, js, jh, sl, &src[0], &dst[0], &bytes[0]))
             bytes[0] = 0;
           mine = bytes[0];
         } else {
 #pragma unroll
           for (int c = 0; c < 3; ++c) {
-            if (!small_copy<KD, QMAX, DF>(p, lane + 32 * c, jn, jbos, js, jh, sl, &src[c], &dst[c], &bytes[c]))
+            if (!small_copy<KD, QMAX, DF, TC>(p, lane + 32 * c, jn, jbos, js, jh, sl, &src[c], &dst[c], &bytes[c]))
               bytes[c] = 0;
             mine += bytes[c];
           }
@@ -416,10 +436,10 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
 
 // ---------------------------------------------------------------- state warp
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool TC>
 __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
-  using Lay = Layout<KD, QMAX>;
-  Bars<KD, QMAX> bars(smem);
+  using Lay = Layout<KD, QMAX, TC>;
+  Bars<KD, QMAX, TC> bars(smem);
   const int nloc = local_items(p.B * p.H);
   uint32_t ch_cnt = 0;
   bool ok = true;
@@ -479,10 +499,10 @@ struct ConvIn {
   uint16_t seq[kConvWidth - 1 + QMAX + 1];
 };
 
-template <int KD, int QMAX, bool DF>
+template <int KD, int QMAX, bool DF, bool TC>
 __device__ __forceinline__ void conv_load(const VerifyParams& p, const unsigned char* sl, int g, int k, int n, int a,
                                           int Lc, uint32_t act_lo, ConvIn<QMAX>& in) {
-  using Lay = Layout<KD, QMAX>;
+  using Lay = Layout<KD, QMAX, TC>;
   const uint16_t* conv = reinterpret_cast<const uint16_t*>(sl + Lay::kConv);
   if (p.conv_weight_fp32) {
     const float4 wv = reinterpret_cast<const float4*>(sl + Lay::kW)[g * KD + k];
@@ -530,7 +550,7 @@ __device__ __forceinline__ void conv_pairs(const ConvIn<QMAX>& in, uint16_t (&y)
   }
 }
 
-template <int KD, int QMAX, bool DF>
+template <int KD, int QMAX, bool DF, bool TC>
 __device__ __forceinline__ void conv_roll(const VerifyParams& p, const ConvIn<QMAX>& in, int g, int k, int n, int Lc,
                                           uint16_t* gconv, long long hk) {
   const long long HK = static_cast<long long>(p.H) * KD;
@@ -575,12 +595,12 @@ __device__ __forceinline__ void conv_two(const ConvIn<QMAX>& in0, const ConvIn<Q
   }
 }
 
-template <int KD, int QMAX, bool DF>
+template <int KD, int QMAX, bool DF, bool TC>
 __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatile int* misc) {
-  using Lay = Layout<KD, QMAX>;
+  using Lay = Layout<KD, QMAX, TC>;
   constexpr int NREDP = Lay::kPart;  // |q_t|^2, |k_t|^2, raw M / N grid, padded to 32
   constexpr int PER = NREDP / 32;
-  Bars<KD, QMAX> bars(smem);
+  Bars<KD, QMAX, TC> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   float* part = reinterpret_cast<float*>(smem + Lay::oPart);
   float* xs = reinterpret_cast<float*>(smem + Lay::oXs);  // [2][QMAX][KD] q | k
@@ -624,9 +644,9 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       const int g0 = c0 / KD, k0 = c0 - g0 * KD;
       const int g1 = c1 / KD, k1 = c1 - g1 * KD;
       ConvIn<QMAX> in0, in1;
-      conv_load<KD, QMAX, DF>(p, sl, g0, k0, n, m.a, Lc, act_lo, in0);
+      conv_load<KD, QMAX, DF, TC>(p, sl, g0, k0, n, m.a, Lc, act_lo, in0);
       if (has1) {
-        conv_load<KD, QMAX, DF>(p, sl, g1, k1, n, m.a, Lc, act_lo, in1);
+        conv_load<KD, QMAX, DF, TC>(p, sl, g1, k1, n, m.a, Lc, act_lo, in1);
       } else {
 #pragma unroll
         for (int j = 0; j < kConvWidth; ++j) in1.w[j] = 0.0f;
@@ -635,8 +655,8 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       }
       uint16_t y0[QMAX], y1[QMAX];
       conv_two<QMAX>(in0, in1, n, y0, y1);
-      conv_roll<KD, QMAX, DF>(p, in0, g0, k0, n, Lc, gconv, hk);
-      if (has1) conv_roll<KD, QMAX, DF>(p, in1, g1, k1, n, Lc, gconv, hk);
+      conv_roll<KD, QMAX, DF, TC>(p, in0, g0, k0, n, Lc, gconv, hk);
+      if (has1) conv_roll<KD, QMAX, DF, TC>(p, in1, g1, k1, n, Lc, gconv, hk);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         if (cc == 1 && !has1) break;
@@ -737,13 +757,38 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
         rq[t] = rsqrtf(qq + 1e-6f) * p.k_scale;  // q^ = q rsqrt(|q|^2 + eps) K^-1/2
         rk[t] = rsqrtf(kk + 1e-6f);              // k^ = k rsqrt(|k|^2 + eps)
       }
-      float D = 1.0f;
+      if constexpr (Lay::kTC) {
+        // the MMA's B operand: vector c (X_0..X_{n-1}, Y_0..Y_{n-1}, then
+        // zeros) split as hi = the value with its low 13 mantissa bits cleared
+        // (exact in tf32) in row c and lo = value - hi in row 8 + c
+        unsigned char* bt = op + (pt >> 5) * 2048;
+        const int kk = pt & 31;
+        auto put = [&](int c, float v) {
+          const float hi = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+          *reinterpret_cast<float*>(bt + sw128_offset(c, kk)) = hi;
+          *reinterpret_cast<float*>(bt + sw128_offset(8 + c, kk)) = v - hi;
+        };
+        float D = 1.0f;
 #pragma unroll
-      for (int t = 0; t < QMAX; ++t) {
-        if (t < n) {
-          D *= eg[t];
-          vec[t * KD + pt] = D * (kv[t] * rk[t]);        // X_t
-          vec[(n + t) * KD + pt] = D * (qv[t] * rq[t]);  // Y_t
+        for (int t = 0; t < QMAX; ++t) {
+          if (t < n) {
+            D *= eg[t];
+            put(t, D * (kv[t] * rk[t]));      // X_t
+            put(n + t, D * (qv[t] * rq[t]));  // Y_t
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 2 * QMAX; ++c)
+          if (c >= 2 * n) put(c, 0.0f);
+      } else {
+        float D = 1.0f;
+#pragma unroll
+        for (int t = 0; t < QMAX; ++t) {
+          if (t < n) {
+            D *= eg[t];
+            vec[t * KD + pt] = D * (kv[t] * rk[t]);        // X_t
+            vec[(n + t) * KD + pt] = D * (qv[t] * rq[t]);  // Y_t
+          }
         }
       }
       if (pt < QMAX * QMAX) {
@@ -762,7 +807,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       }
     }
     if (pt == 0) {
-      OpMeta<QMAX>* om = reinterpret_cast<OpMeta<QMAX>*>(op);
+      OpMeta<QMAX>* om = reinterpret_cast<OpMeta<QMAX>*>(op + Lay::kOpMeta);
       om->flags = live ? kLive : 0;
       om->bos = m.bos;
       om->n = n;
@@ -771,6 +816,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
 #pragma unroll
       for (int t = 0; t < QMAX; ++t) om->beta[t] = m.beta[t];
     }
+    if constexpr (Lay::kTC) fence_async_shared();  // the B operand is read by the tensor cores
     named_barrier(kBarPrep, kPrepConvThreads);
     if (pt == 0) mbar_arrive(&bars.op_full[oslot]);
   }
@@ -850,10 +896,10 @@ __device__ __forceinline__ void gemv_chunk(const float* __restrict__ st, const f
 // even and R_0..R_{N-1} if kq is odd.  The two lanes of a row swap their
 // halves and both run the recurrence; the even lane stores the corrections,
 // the odd lane the outputs.
-template <int KD, int QMAX, int N>
+template <int KD, int QMAX, int N, bool TC>
 __device__ __forceinline__ void solve_regs(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op,
                                            int h, int gw, int lane, const float (&mine)[8]) {
-  using Lay = Layout<KD, QMAX>;
+  using Lay = Layout<KD, QMAX, TC>;
   static_assert(Lay::RW == 16, "two lanes per row: 16 rows per gemv warp");
   const int kq = lane & 3;
   const int row = gw * Lay::RW + (lane >> 2) + 8 * (kq >> 1);
@@ -887,11 +933,11 @@ __device__ __forceinline__ void solve_regs(const VerifyParams& p, const OpMeta<Q
   }
 }
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool TC>
 __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, int lane, volatile int* misc) {
-  using Lay = Layout<KD, QMAX>;
+  using Lay = Layout<KD, QMAX, TC>;
   constexpr int RW = Lay::RW;
-  Bars<KD, QMAX> bars(smem);
+  Bars<KD, QMAX, TC> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   float* red = reinterpret_cast<float*>(smem + Lay::oRed) + gw * Lay::kRedPerWarp;
   const int nloc = local_items(p.B * p.H);
@@ -904,7 +950,7 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
     ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag);
     if (!ok) break;
     const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
-    const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op);
+    const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta);
     if (m.flags & kLive) {
       const int n = m.n;
       const uint32_t pc = live * kGemvWarps + gw;
@@ -921,25 +967,25 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
               gemv_chunk<KD, 2, false>(st, vec, red, lane, mine);
               __syncwarp();
               if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 1>(p, m, op, h, gw, lane, mine);
+              solve_regs<KD, QMAX, 1, TC>(p, m, op, h, gw, lane, mine);
               break;
             case 2:
               gemv_chunk<KD, 4, false>(st, vec, red, lane, mine);
               __syncwarp();
               if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 2>(p, m, op, h, gw, lane, mine);
+              solve_regs<KD, QMAX, 2, TC>(p, m, op, h, gw, lane, mine);
               break;
             case 3:
               gemv_chunk<KD, 6, false>(st, vec, red, lane, mine);
               __syncwarp();
               if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 3>(p, m, op, h, gw, lane, mine);
+              solve_regs<KD, QMAX, 3, TC>(p, m, op, h, gw, lane, mine);
               break;
             default:
               gemv_chunk<KD, 8, false>(st, vec, red, lane, mine);
               __syncwarp();
               if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 4>(p, m, op, h, gw, lane, mine);
+              solve_regs<KD, QMAX, 4, TC>(p, m, op, h, gw, lane, mine);
               break;
           }
         }
@@ -992,15 +1038,279 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
   }
 }
 
-template <int KD, int QMAX, bool DF>
-__global__ void __launch_bounds__(kThreads, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
-  using Lay = Layout<KD, QMAX>;
+// ---------------------------------------------------------------- tensor-core path (K = 128, Q <= 4)
+//
+// The products P | R = S0 [X_0..X_{n-1} | Y_0..Y_{n-1}] of an item come from
+// tcgen05 MMAs: D[128 x 16] in tensor memory = S0 [128 x 128] times B^T, B =
+// [hi rows 0..7 | lo rows 8..15] of the 2n <= 8 operand vectors.  fp32
+// accuracy from tf32 inputs: S0 = S_hi + S_lo with S_hi the value with its
+// low 13 mantissa bits cleared (exact in tf32) and S_lo = S0 - S_hi (exact in
+// fp32, at most 11 significant bits, rounded to tf32 within 2^-21 of S0);
+// likewise for B.  Two MMAs per K step, S_hi B^T + S_lo B^T, accumulate
+// column c < 8 = S0 v_c,hi and column 8 + c = S0 v_c,lo, whose sum is S0 v_c.
+
+// State producer: each live item's state as four K-slices (TMA tiles of 128
+// rows x 32 fp32 with the 128-byte swizzle) into the ring of slice slots.
+template <int KD, int QMAX, bool TC>
+__device__ void tc_produce_state(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
+  using Lay = Layout<KD, QMAX, TC>;
+  Bars<KD, QMAX, TC> bars(smem);
+  const int nloc = local_items(p.B * p.H);
+  uint32_t g = 0;  // slices issued
+  bool ok = true;
+  for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
+    const int it = static_cast<int>(blockIdx.x) + (i0 + lane) * static_cast<int>(gridDim.x);
+    const ItemMeta<QMAX> im = decode_item<QMAX>(p, it, i0 + lane < nloc, false);
+    const int count = min(32, nloc - i0);
+    for (int j = 0; j < count && ok; ++j) {
+      if (!(__shfl_sync(0xffffffffu, im.flags, j) & kLive)) continue;
+      const int jh = __shfl_sync(0xffffffffu, im.h, j);
+      const int js = static_cast<int>(shfl_ll(im.s, j));
+      for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
+        const int pos = static_cast<int>(g % Lay::kNumChunk);
+        if (lane == 0) {
+          ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((g / Lay::kNumChunk) & 1) ^ 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
+            tma_load_3d(smem + Lay::oChunks + pos * Lay::kChunk, &p.tm_state, kb * 32, jh * KD, js, &bars.ch_full[pos]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+    }
+  }
+  if (!ok && lane == 0) {
+    report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
+    *abort_flag = 1;
+  }
+  // the slots are released by MMA completion: see every release land before
+  // the CTA (and its shared memory) goes away
+  if (lane == 0) {
+    for (uint32_t e = 0; e < static_cast<uint32_t>(Lay::kNumChunk); ++e, ++g)
+      (void)mbar_wait_bounded(&bars.ch_empty[g % Lay::kNumChunk], ((g / Lay::kNumChunk) & 1) ^ 1);
+  }
+}
+
+// MMA issuer (one thread).  Per K-slice of a live item: the 4 K-steps of
+// S_hi B^T as soon as the slice has landed (committed to hi_done, after which
+// the split team overwrites the slice with its low part), then, one slice
+// later, the 4 K-steps of S_lo B^T once the low part is complete (committed
+// to the slot's release and, after an item's last slice, to its D buffer).
+// Issuing the next slice's S_hi before the previous slice's S_lo keeps the
+// split team fed while the tensor cores work.
+struct LoPending {
+  bool valid, last;
+  int pos, oslot;
+  uint32_t g, db;
+  uint64_t bk;
+};
+
+template <int KD, int QMAX, bool TC>
+__device__ __forceinline__ bool tc_issue_lo(unsigned char* smem, uint32_t taddr, LoPending& lp,
+                                            const volatile int* abort_flag) {
+  using Lay = Layout<KD, QMAX, TC>;
+  constexpr uint32_t kIdesc = umma_idesc_tf32(128, 16);
+  Bars<KD, QMAX, TC> bars(smem);
+  if (!lp.valid) return true;
+  lp.valid = false;
+  if (!mbar_wait_or_abort(&bars.lo_full[lp.pos], (lp.g / Lay::kNumChunk) & 1, abort_flag)) return false;
+  tmem_fence_after();
+  const uint64_t a = umma_desc_sw128(smem + Lay::oChunks + lp.pos * Lay::kChunk);
+  const uint32_t d = taddr + lp.db * 16;
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) umma_tf32(d, a + 2 * ks, lp.bk + 2 * ks, kIdesc, true);
+  umma_commit(&bars.ch_empty[lp.pos]);
+  if (lp.last) {
+    umma_commit(&bars.d_full[lp.db]);
+    mbar_arrive(&bars.op_empty[lp.oslot]);
+  }
+  return true;
+}
+
+template <int KD, int QMAX, bool TC>
+__device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int* misc) {
+  using Lay = Layout<KD, QMAX, TC>;
+  constexpr uint32_t kIdesc = umma_idesc_tf32(128, 16);
+  Bars<KD, QMAX, TC> bars(smem);
+  volatile int* abort_flag = misc + kMiscAbort;
+  const int nloc = local_items(p.B * p.H);
+  const uint32_t taddr = static_cast<uint32_t>(misc[kMiscTaddr]);
+  uint32_t g = 0, live = 0;
+  LoPending lp{false, false, 0, 0, 0, 0, 0};
+  bool ok = true;
+  for (int i = 0; i < nloc && ok; ++i) {
+    const int oslot = i % Lay::kNumOp;
+    const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
+    ok = mbar_wait_or_abort(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, abort_flag);
+    if (!ok) break;
+    if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
+      // finish the previous item first: its operand slot may be the next one
+      // the prep team needs
+      ok = tc_issue_lo<KD, QMAX, TC>(smem, taddr, lp, abort_flag);
+      mbar_arrive(&bars.op_empty[oslot]);
+      continue;
+    }
+    const uint32_t db = live & 1;
+    ok = mbar_wait_or_abort(&bars.d_empty[db], ((live >> 1) & 1) ^ 1, abort_flag);
+    const uint64_t b = umma_desc_sw128(op);
+    const uint32_t d = taddr + db * 16;
+    for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
+      const int pos = static_cast<int>(g % Lay::kNumChunk);
+      ok = mbar_wait_or_abort(&bars.ch_full[pos], (g / Lay::kNumChunk) & 1, abort_flag);
+      if (!ok) break;
+      tmem_fence_after();
+      const uint64_t a = umma_desc_sw128(smem + Lay::oChunks + pos * Lay::kChunk);
+      const uint64_t bk = b + static_cast<uint64_t>(kb) * (2048 >> 4);  // B slice kb: 2 KB further
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) umma_tf32(d, a + 2 * ks, bk + 2 * ks, kIdesc, kb > 0 || ks > 0);
+      umma_commit(&bars.hi_done[pos]);
+      ok = tc_issue_lo<KD, QMAX, TC>(smem, taddr, lp, abort_flag);
+      lp = LoPending{true, kb == 3, pos, oslot, g, db, bk};
+    }
+    ++live;
+  }
+  if (ok) ok = tc_issue_lo<KD, QMAX, TC>(smem, taddr, lp, abort_flag);
+  if (!ok) {
+    report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
+    *abort_flag = 1;
+  }
+}
+
+// Readout team (4 warps, warp q of the CTA's last warpgroup reads tensor-memory
+// lanes 32 q .. 32 q + 31): each lane owns one state row; it sums the hi and
+// lo columns into P_t | R_t and runs the row's solve.
+template <int KD, int QMAX, int N, bool TC>
+__device__ __forceinline__ void tc_solve(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op, int h,
+                                         int row, const float (&d)[16]) {
+  using Lay = Layout<KD, QMAX, TC>;
+  const float* mn = reinterpret_cast<const float*>(op + Lay::kOpMN);
+  const float* xv = reinterpret_cast<const float*>(op + Lay::kOpV);
+  float* corr = p.corr + m.r * p.corr_stride + static_cast<long long>(h) * p.Q * KD + row;
+  uint16_t* out = p.out + static_cast<long long>(m.bos) * p.out_stride + static_cast<long long>(h) * KD + row;
+  float cv[N];
+#pragma unroll
+  for (int t = 0; t < N; ++t) {
+    float x = xv[t * KD + row] - (d[t] + d[8 + t]);
+#pragma unroll
+    for (int u = 0; u < t; ++u) x = fmaf(-mn[t * QMAX + u], cv[u], x);
+    const float c = x * m.beta[t];
+    cv[t] = c;
+    float o = d[N + t] + d[8 + N + t];
+#pragma unroll
+    for (int u = 0; u <= t; ++u) o = fmaf(mn[u * QMAX + t], cv[u], o);
+    corr[t * KD] = c;
+    out[static_cast<long long>(t) * p.out_stride] = f32_to_bf16(o);
+  }
+}
+
+// Readout of a live item's products, in the split warp that owns tensor-memory
+// lanes 32 wq .. 32 wq + 31 (one state row per lane): P_t | R_t = hi column +
+// lo column, then the row's solve.  Releases the D buffer and the operand slot.
+template <int KD, int QMAX, bool TC>
+__device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char* smem, int i, uint32_t live, int wq,
+                                           int lane, uint32_t taddr, const volatile int* abort_flag) {
+  using Lay = Layout<KD, QMAX, TC>;
+  Bars<KD, QMAX, TC> bars(smem);
+  const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+  const int h = it - (it / p.H) * p.H;
+  const int oslot = i % Lay::kNumOp;
+  const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
+  const uint32_t db = live & 1;
+  if (!warp_wait(&bars.d_full[db], (live >> 1) & 1, lane, abort_flag)) return false;
+  tmem_fence_after();
+  float d[16];
+  tmem_ld16(taddr + db * 16 + (static_cast<uint32_t>(wq * 32) << 16), d);
+  tmem_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars.d_empty[db]);
+  const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta);
+  const int row = wq * 32 + lane;
+  switch (m.n) {
+    case 1: tc_solve<KD, QMAX, 1, TC>(p, m, op, h, row, d); break;
+    case 2: tc_solve<KD, QMAX, 2, TC>(p, m, op, h, row, d); break;
+    case 3: tc_solve<KD, QMAX, 3, TC>(p, m, op, h, row, d); break;
+    default: tc_solve<KD, QMAX, 4, TC>(p, m, op, h, row, d); break;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
+  return true;
+}
+
+// Split team (4 warps, each on its own).  A tf32 MMA reads an fp32 operand
+// with its low 13 mantissa bits ignored, so a K-slice as loaded is S_hi to the
+// tensor cores.  Once its S_hi products are done, the warps overwrite the
+// slice in place with its low part S - S_hi for the S_lo products.
+// Two slices into an item, the warp reads out the previous live item, whose
+// MMAs have completed by then.
+template <int KD, int QMAX, bool TC>
+__device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, volatile int* misc) {
+  using Lay = Layout<KD, QMAX, TC>;
+  Bars<KD, QMAX, TC> bars(smem);
+  volatile int* abort_flag = misc + kMiscAbort;
+  const int lane = st & 31;
+  const int wq = st >> 5;
+  const int nloc = local_items(p.B * p.H);
+  const uint32_t taddr = static_cast<uint32_t>(misc[kMiscTaddr]);
+  uint32_t g = 0, live = 0;
+  int pending = -1;  // live item awaiting readout
+  bool ok = true;
+  for (int i = 0; i < nloc && ok; ++i) {
+    const int oslot = i % Lay::kNumOp;
+    const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
+    ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag);
+    if (!ok) break;
+    if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
+      // read the pending item out now: with no live item to follow soon, its
+      // operand slot would be missing when the prep team comes round to it
+      if (pending >= 0) ok = tc_readout<KD, QMAX, TC>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
+      pending = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
+      continue;
+    }
+    for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
+      const int pos = static_cast<int>(g % Lay::kNumChunk);
+      ok = warp_wait(&bars.ch_full[pos], (g / Lay::kNumChunk) & 1, lane, abort_flag) &&
+           warp_wait(&bars.hi_done[pos], (g / Lay::kNumChunk) & 1, lane, abort_flag);
+      if (!ok) break;
+      float4* s4 = reinterpret_cast<float4*>(smem + Lay::oChunks + pos * Lay::kChunk);
+#pragma unroll 4
+      for (int e = st; e < Lay::kChunk / 16; e += 32 * kSplitWarps) {
+        const float4 x = s4[e];
+        float4 l;
+        l.x = x.x - __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+        l.y = x.y - __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+        l.z = x.z - __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+        l.w = x.w - __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+        s4[e] = l;
+      }
+      fence_async_shared();  // the low parts are read by the tensor cores
+      mbar_arrive(&bars.lo_full[pos]);
+      if (kb == 1 && pending >= 0) {  // the pending item's MMAs are done by now
+        ok = tc_readout<KD, QMAX, TC>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
+        pending = -1;
+      }
+    }
+    if (!ok) break;
+    pending = i;
+    ++live;
+  }
+  if (ok && pending >= 0) ok = tc_readout<KD, QMAX, TC>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
+  if (!ok && lane == 0) {
+    report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
+    *abort_flag = 1;
+  }
+}
+
+template <int KD, int QMAX, bool DF, bool TC>
+__global__ void __launch_bounds__(Layout<KD, QMAX, TC>::kThreads, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
+  using Lay = Layout<KD, QMAX, TC>;
   extern __shared__ __align__(1024) unsigned char smem[];
   volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::oMisc);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   if (tid == 0) {
-    Bars<KD, QMAX> bars(smem);
+    Bars<KD, QMAX, TC> bars(smem);
     for (int i = 0; i < Lay::kNumChunk; ++i) {
       mbar_init(&bars.ch_full[i], 1);
       mbar_init(&bars.ch_empty[i], 1);
@@ -1011,20 +1321,62 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const __grid_consta
     }
     for (int i = 0; i < Lay::kNumOp; ++i) {
       mbar_init(&bars.op_full[i], 1);
-      mbar_init(&bars.op_empty[i], kGemvWarps);
+      // released by the gemv warps, or by the readout warps and the MMA issuer
+      mbar_init(&bars.op_empty[i], Lay::kTC ? kSplitWarps + 1 : kGemvWarps);
     }
-    for (int i = 0; i < 8; ++i) misc[i] = 0;
+    if constexpr (Lay::kTC) {
+      for (int i = 0; i < Lay::kNumChunk; ++i) {
+        mbar_init(&bars.hi_done[i], 1);
+        mbar_init(&bars.lo_full[i], 32 * kSplitWarps);
+      }
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.d_full[i], 1);
+      mbar_init(&bars.d_empty[i], kSplitWarps);
+    }
+    for (int i = 0; i < 8; ++i)
+      if (i != kMiscTaddr) misc[i] = 0;  // the tensor-memory base is written by the allocating warp
     fence_barrier_init();
   }
+  if constexpr (Lay::kTC) {
+    // the 128-byte swizzle of the MMA operands is anchored at 1024-byte boundaries
+    if (smem_u32(smem) & 1023u) {
+      if (tid == 0) report(p.workspace, KDA_DEVERR_MISALIGNED, blockIdx.x);
+      return;
+    }
+    // tensor memory for two D buffers of 16 fp32 columns, owned by the MMA warp
+    if (warp == kMmaWarp)
+      tmem_alloc(reinterpret_cast<uint32_t*>(const_cast<int*>(misc) + kMiscTaddr), 32);
+    tmem_fence_before();
+  }
   __syncthreads();
+  if constexpr (Lay::kTC) tmem_fence_after();
   if (warp == 0) {
-    produce_inputs<KD, QMAX, DF>(p, smem, tid & 31, misc + kMiscAbort);
+    produce_inputs<KD, QMAX, DF, TC>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp == 1) {
-    produce_state<KD, QMAX>(p, smem, tid & 31, misc + kMiscAbort);
+    if constexpr (Lay::kTC)
+      tc_produce_state<KD, QMAX, TC>(p, smem, tid & 31, misc + kMiscAbort);
+    else
+      produce_state<KD, QMAX, TC>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp < 2 + kPrepWarps) {
-    prep<KD, QMAX, DF>(p, smem, tid - 64, misc);
+    prep<KD, QMAX, DF, TC>(p, smem, tid - 64, misc);
+  } else if constexpr (Lay::kTC) {
+    if (warp < kMmaWarp)
+      tc_split<KD, QMAX, TC>(p, smem, tid - 32 * (2 + kPrepWarps), misc);
+    else if ((tid & 31) == 0)
+      tc_mma<KD, QMAX, TC>(p, smem, misc);
   } else {
-    gemv_team<KD, QMAX>(p, smem, warp - 2 - kPrepWarps, tid & 31, misc);
+    gemv_team<KD, QMAX, TC>(p, smem, warp - 2 - kPrepWarps, tid & 31, misc);
+  }
+  if constexpr (Lay::kTC) {
+    // every role is done and the MMA issuer has seen its last MMAs complete:
+    // release the tensor memory
+    tmem_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+      tmem_fence_after();
+      tmem_dealloc(static_cast<uint32_t>(misc[kMiscTaddr]), 32);
+    }
   }
 }
 
@@ -1050,12 +1402,13 @@ EncodeTiledFn tensor_map_encoder() {
 }
 
 bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const cuuint64_t* dims,
-                const cuuint64_t* strides, const cuuint32_t* box) {
+                const cuuint64_t* strides, const cuuint32_t* box,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   const EncodeTiledFn fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint32_t unit[5] = {1, 1, 1, 1, 1};
   return fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, unit,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1072,6 +1425,18 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
 //     at {0, h K W / 128, 0}.
 // Every box lands in the layout the hull copies would give, except q | k | v
 // (| gate), which lands as [t][group][K].
+// The fp32 state pool for the tensor-core path, [slots][H K][K] with the slot
+// stride given: dims {K, H K, slots}, box {32, 128, 1} with the 128-byte
+// swizzle, at {32 kb, h K, s}: K-slice kb of head h's state.
+bool build_state_map(VerifyParams& p, int KD) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(KD), static_cast<cuuint64_t>(p.H) * KD,
+                              static_cast<cuuint64_t>(p.num_slots)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(KD) * 4, static_cast<cuuint64_t>(p.state_slot_stride) * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
+  return encode_map(&p.tm_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.state, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 void build_tensor_maps(VerifyParams& p, int KD) {
   p.act_mode = 0;
   const cuuint64_t H = static_cast<cuuint64_t>(p.H), K = static_cast<cuuint64_t>(KD), HK = H * K;
@@ -1125,6 +1490,16 @@ void build_tensor_maps(VerifyParams& p, int KD) {
   p.act_mode = mode;
 }
 
+// The tensor-core verify (K = 128, windows up to 4) is opt-in: set
+// KDA_VERIFY_TCGEN05=1.  It matches the CUDA-core gemv within the same
+// tolerances but runs slower on GB300: an M = 128 tf32 MMA costs about the
+// same whatever N is, so the 2n <= 8 operand vectors use a few percent of the
+// tensor core, and fp32 accuracy takes a second (low-part) pass.
+bool tcgen05_requested() {
+  const char* v = std::getenv("KDA_VERIFY_TCGEN05");
+  return v != nullptr && v[0] == '1' && v[1] == '\0';
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -1137,14 +1512,14 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int KD, int QMAX, bool DF>
+template <int KD, int QMAX, bool DF, bool TC>
 cudaError_t launch(const VerifyParams& p, cudaStream_t stream) {
-  constexpr int bytes = Layout<KD, QMAX>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, DF>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  constexpr int bytes = Layout<KD, QMAX, TC>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, DF, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const int items = p.B * p.H;
   const int grid = items < sm_count() ? items : sm_count();
-  verify_kernel<KD, QMAX, DF><<<grid, kThreads, bytes, stream>>>(p);
+  verify_kernel<KD, QMAX, DF, TC><<<grid, Layout<KD, QMAX, TC>::kThreads, bytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1154,12 +1529,15 @@ cudaError_t launch_verify(const VerifyParams& params, int K, cudaStream_t stream
   VerifyParams p = params;
   build_tensor_maps(p, K);
   // the conv-state layout is a template parameter: straight-line tap addressing
+  const bool q4 = p.Q <= 4;
+  if (K == 128 && q4 && tcgen05_requested() && build_state_map(p, K))
+    return p.conv_dim_first ? launch<128, 4, true, true>(p, stream) : launch<128, 4, false, true>(p, stream);
   if (p.conv_dim_first) {
-    if (K == 128) return p.Q <= 4 ? launch<128, 4, true>(p, stream) : launch<128, 8, true>(p, stream);
-    return p.Q <= 4 ? launch<64, 4, true>(p, stream) : launch<64, 8, true>(p, stream);
+    if (K == 128) return q4 ? launch<128, 4, true, false>(p, stream) : launch<128, 8, true, false>(p, stream);
+    return q4 ? launch<64, 4, true, false>(p, stream) : launch<64, 8, true, false>(p, stream);
   }
-  if (K == 128) return p.Q <= 4 ? launch<128, 4, false>(p, stream) : launch<128, 8, false>(p, stream);
-  return p.Q <= 4 ? launch<64, 4, false>(p, stream) : launch<64, 8, false>(p, stream);
+  if (K == 128) return q4 ? launch<128, 4, false, false>(p, stream) : launch<128, 8, false, false>(p, stream);
+  return q4 ? launch<64, 4, false, false>(p, stream) : launch<64, 8, false, false>(p, stream);
 }
 
 }  // namespace kda

@@ -1,0 +1,58 @@
+"""The opt-in tensor-core verify (KDA_VERIFY_TCGEN05=1: K = 128, windows up to
+4 tokens, P | R from tcgen05 tf32 MMAs with a hi/lo split of the state) against
+the oracle, under the same comparison rules as the CUDA-core path."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_ssm_kda_gb300 as kda
+from linear_attention_ssm_kda_gb300 import _build
+from test_parity_gpu import run_and_check
+from workloads import CONFIGS, make_problem
+from workloads.drive import device_meta, verify_layer
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _tcgen05(monkeypatch):
+    _build.build()
+    kda.load_library()
+    monkeypatch.setenv("KDA_VERIFY_TCGEN05", "1")
+
+
+def test_c1_full_size_with_null_slots():
+    prob = make_problem(CONFIGS["C1"], DEV)
+    assert (prob.meta.state_indices <= 0).sum() == 4
+    run_and_check(prob)
+
+
+def test_c2_verify_then_commit_reduced():
+    prob = make_problem(CONFIGS["C2"], DEV, B=40, L=3, slots=64)
+    run_and_check(prob)
+
+
+def test_c4_null_slots_and_misaligned_rows_reduced():
+    prob = make_problem(CONFIGS["C4"], DEV, B=96, L=2, slots=256)
+    assert (prob.meta.state_indices <= 0).sum() > 0
+    run_and_check(prob)
+
+
+def test_differs_from_the_cuda_core_path_only_by_rounding(monkeypatch):
+    """Both instantiations run on the same inputs; the outputs agree to the
+    verify tolerance but not bit for bit, so the tensor-core kernel did run."""
+    got = {}
+    for flag in ("1", "0"):
+        monkeypatch.setenv("KDA_VERIFY_TCGEN05", flag)
+        prob = make_problem(CONFIGS["C2"], DEV, B=48, L=1, slots=96)
+        dm = device_meta(prob.meta, DEV)
+        verify_layer(prob, 0, dm)
+        torch.cuda.synchronize()
+        got[flag] = prob.corr[0].cpu().numpy()
+    a, b = got["1"], got["0"]
+    live = np.isfinite(a) & np.isfinite(b)
+    assert not np.array_equal(a[live].view(np.uint32), b[live].view(np.uint32))
+    assert np.abs(a[live] - b[live]).max() <= 1e-4 * np.abs(b[live]).max()

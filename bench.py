@@ -258,31 +258,24 @@ def time_oracle(cfg_name: str, steps: int, warmup: int, sample_layers: int = 1, 
 
 # --------------------------------------------------------------------------- GPU arm
 
-def run_e2e(args, prob, dm, step, stream, dev, world):
+def run_e2e(args, prob, ctx, stream, dev, world):
     """End to end through the public API with host buffers: every step copies
-    its inputs from pinned host memory, runs, and reads its outputs back."""
-    meta = prob.meta
+    its inputs from pinned host memory, runs, and reads its outputs back
+    (``workloads.drive.HostPipeline``: each layer's copies overlap the other
+    layers' kernels)."""
+    from workloads.drive import HostPipeline, pinned_meta
+
     host_fused = torch.empty(prob.fused.shape, dtype=prob.fused.dtype, pin_memory=True)
     host_fused.copy_(prob.fused)
-    host_meta = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
-                 for k, v in (("qsl", meta.query_start_loc), ("si", meta.state_indices),
-                              ("prev", meta.num_accepted_prev), ("acc", meta.num_accepted)) if v is not None}
+    host_meta = pinned_meta(prob.meta)
     host_out = torch.empty(prob.out.shape, dtype=prob.out.dtype, pin_memory=True)
     h2d = host_fused.numel() * 2 + sum(t.numel() * 4 for t in host_meta.values())
     d2h = host_out.numel() * 2
-
-    def e2e_step():
-        prob.fused.copy_(host_fused, non_blocking=True)
-        dm.query_start_loc.copy_(host_meta["qsl"], non_blocking=True)
-        dm.state_indices.copy_(host_meta["si"], non_blocking=True)
-        if "prev" in host_meta:
-            dm.num_accepted_prev.copy_(host_meta["prev"], non_blocking=True)
-        dm.num_accepted.copy_(host_meta["acc"], non_blocking=True)
-        step()
-        host_out.copy_(prob.out, non_blocking=True)
+    pipe = HostPipeline(prob, ctx, stream)
 
     for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
+        pipe.step(host_fused, host_meta, host_out)
+    pipe.drain()
     torch.cuda.synchronize(dev)
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
@@ -290,11 +283,11 @@ def run_e2e(args, prob, dm, step, stream, dev, world):
     barrier(world)
     e_start.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        pipe.step(host_fused, host_meta, host_out)
+    pipe.drain()
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e_start.elapsed_time(e_end)
-
     return e2e_ms, e2e_steps, h2d, d2h
 
 
@@ -365,7 +358,7 @@ def run_gpu(args, rank, local, world):
 
     e2e_ms, e2e_steps, h2d, d2h = None, 0, 0, 0
     if not args.no_e2e:
-        e2e_ms, e2e_steps, h2d, d2h = run_e2e(args, prob, dm, step, stream, dev, world)
+        e2e_ms, e2e_steps, h2d, d2h = run_e2e(args, prob, ctx, stream, dev, world)
 
     # aggregate over ranks: units of all ranks / the slowest rank's time
     t_max = max_over_ranks(elapsed_ms, world)
@@ -423,7 +416,8 @@ def run_gpu(args, rank, local, world):
         },
         "e2e": None if e_max is None else {
             "value": tokens_e2e / (e_max / 1e3), "unit": "tokens/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+            "copies": "per layer on two copy streams, overlapping the other layers' kernels"},
         "gpu_launches": args.steps * (L + 1),
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -65,3 +65,73 @@ def commit_all(ctx: kda.CommitContext, dm: DeviceMeta, *, num_accepted=None, wor
                stream=None) -> None:
     ctx.commit(dm.num_accepted if num_accepted is None else num_accepted, dm.state_indices,
                dm.query_start_loc, record_indices=dm.record_indices, workspace=workspace, stream=stream)
+
+
+def pinned_meta(meta: Metadata) -> dict:
+    """The step's request metadata as pinned host int32 tensors."""
+    return {k: torch.from_numpy(np.ascontiguousarray(v, dtype=np.int32)).pin_memory()
+            for k, v in (("qsl", meta.query_start_loc), ("si", meta.state_indices),
+                         ("prev", meta.num_accepted_prev), ("acc", meta.num_accepted)) if v is not None}
+
+
+class HostPipeline:
+    """Decode steps (verify of every layer, then the commit) fed from pinned
+    host memory, with the copies of one layer overlapping the kernels of its
+    neighbours.  Layer l's activations go up on one copy stream while earlier
+    layers run; its outputs come back on another while later layers run.
+    Events order every reuse of a device buffer: a layer's activations are
+    overwritten only after the previous step's verify of that layer, its
+    outputs only after they were read back, and the request metadata
+    alternates between two device sets."""
+
+    def __init__(self, prob: Problem, ctx: kda.CommitContext, stream: torch.cuda.Stream):
+        self.prob, self.ctx, self.stream = prob, ctx, stream
+        dev = prob.fused.device
+        L = prob.cfg.L
+        self.dms = [device_meta(prob.meta, dev), device_meta(prob.meta, dev)]
+        self.up = torch.cuda.Stream(dev)
+        self.down = torch.cuda.Stream(dev)
+        self.in_ready = [torch.cuda.Event() for _ in range(L)]
+        self.verified = [torch.cuda.Event() for _ in range(L)]
+        self.read_back = [torch.cuda.Event() for _ in range(L)]
+        self.meta_ready = torch.cuda.Event()
+        self.meta_free = [torch.cuda.Event(), torch.cuda.Event()]
+        self.count = 0
+
+    def step(self, host_fused: torch.Tensor, host_meta: dict, host_out: torch.Tensor) -> None:
+        """Enqueue one step: ``host_fused`` [L, T, F] and ``host_meta`` (from
+        ``pinned_meta``) in, ``host_out`` [L, T, H K] back, all pinned."""
+        prob, stream, up, down = self.prob, self.stream, self.up, self.down
+        L = prob.cfg.L
+        d = self.dms[self.count % 2]
+        with torch.cuda.stream(up):
+            up.wait_event(self.meta_free[self.count % 2])  # the step two back is done with this set
+            d.query_start_loc.copy_(host_meta["qsl"], non_blocking=True)
+            d.state_indices.copy_(host_meta["si"], non_blocking=True)
+            if "prev" in host_meta:
+                d.num_accepted_prev.copy_(host_meta["prev"], non_blocking=True)
+            d.num_accepted.copy_(host_meta["acc"], non_blocking=True)
+            self.meta_ready.record(up)
+            for l in range(L):
+                up.wait_event(self.verified[l])  # the previous step's verify has read these activations
+                prob.fused[l].copy_(host_fused[l], non_blocking=True)
+                self.in_ready[l].record(up)
+        stream.wait_event(self.meta_ready)
+        for l in range(L):
+            stream.wait_event(self.in_ready[l])
+            stream.wait_event(self.read_back[l])  # the previous step's outputs of this layer are home
+            verify_layer(prob, l, d, stream=stream)
+            self.verified[l].record(stream)
+        commit_all(self.ctx, d, stream=stream)
+        self.meta_free[self.count % 2].record(stream)
+        with torch.cuda.stream(down):
+            for l in range(L):
+                down.wait_event(self.verified[l])
+                host_out[l].copy_(prob.out[l], non_blocking=True)
+                self.read_back[l].record(down)
+        self.count += 1
+
+    def drain(self) -> None:
+        """Make the compute stream wait for every copy enqueued so far."""
+        self.stream.wait_stream(self.up)
+        self.stream.wait_stream(self.down)

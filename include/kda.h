@@ -88,8 +88,10 @@ enum {
  *      a = clamp(num_accepted_prev[b], 1, Q) (a = 1 when the pointer is NULL);
  *      seq = history followed by mixed_qkv[bos..bos+n, c];
  *      y_t = bf16_rne(silu(sum_j w[c,j] * seq[t+j])), w[c,W-1] on the newest
- *      input, rounded from the exact sum (a result the device cannot round
- *      with certainty in fp32 is recomputed in fp64);
+ *      input, evaluated by one fixed fp32 procedure (taps summed oldest first
+ *      with fma, e^-|y| by a Cody-Waite reduction and a degree-7 Taylor
+ *      polynomial, 1/(1+z) by three Newton steps), so the code is
+ *      reproducible bit for bit on any IEEE-754 machine;
  *      the slot then stores seq[1 .. W-2+n] at taps 0 .. W-3+n (in place;
  *      later taps are left as they were).
  *   2. q^ = q * rsqrt(|q|^2 + 1e-6) * K^-1/2, k^ = k * rsqrt(|k|^2 + 1e-6),
@@ -188,6 +190,38 @@ typedef struct kda_commit_args {
     const int32_t *num_accepted;      /* [B]                                       */
     int32_t *workspace;               /* zeroed kda_workspace_bytes(), or NULL     */
 } kda_commit_args;
+
+/*
+ * kda_verify_fold -- the pending commit of the previous step fused into this
+ * step's verify of one layer.  This is the deferred form of the hot path
+ * ("vllm.models.kimi_k3.nvidia.specialized_decode.recoverssm.state",
+ * deferred_recoverssm_verify: the last step's accepted tokens are folded into
+ * the checkpoints before the verify; the pages run that fold as a separate
+ * commit of all layers).  For each request b with a live slot
+ * s = state_indices[b]:
+ *   m = min(max(fold->num_accepted[b], 0), n'),
+ *   n' = min(fold->query_start_loc[b+1] - fold->query_start_loc[b], Q),
+ * and the records of row r' = fold->record_indices ? fold->record_indices[b]
+ * : s, tokens t < m, are folded exactly as kda_commit folds them (this
+ * layer's A_log, dt_bias and gate mode), the folded state is written back to
+ * state[s] (so args->state is WRITTEN by this call), and the verify of this
+ * step then runs on it as kda_verify does.  The pending records are read
+ * before this step's records are written, so r' may equal this step's record
+ * row.  A request with n = 0 and m > 0 is folded only.  The result equals
+ * kda_commit with the fold arguments followed by kda_verify, up to fp32
+ * rounding.  The fold pointers are device arrays ([B+1], [B], [B] or NULL);
+ * fold == NULL or fold->query_start_loc == NULL runs the plain verify.
+ * Supported: Q <= 4 (KDA_ERR_UNSUPPORTED otherwise); the other arguments and
+ * errors are those of kda_verify; a pending record row out of range is a
+ * device error (KDA_DEVERR_ROW_RANGE) that skips the item.
+ */
+typedef struct kda_fold_args {
+    const int32_t *query_start_loc;  /* [B+1] of the step whose records are pending */
+    const int32_t *num_accepted;     /* [B] its accepted tokens                      */
+    const int32_t *record_indices;   /* [B] its record rows, or NULL (the state slot) */
+} kda_fold_args;
+
+kda_status kda_verify_fold(const kda_verify_args *args, const kda_fold_args *fold, kda_stream_t stream);
 
 /* Enqueue the verify of one layer.  Returns before the kernel runs.
  * With the environment variable KDA_VERIFY_TCGEN05=1 at the call, K == 128

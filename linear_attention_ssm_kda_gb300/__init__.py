@@ -71,6 +71,11 @@ class VerifyArgs(ctypes.Structure):
     ]
 
 
+class FoldArgs(ctypes.Structure):
+    """Mirror of ``kda_fold_args``."""
+    _fields_ = [("query_start_loc", _p), ("num_accepted", _p), ("record_indices", _p)]
+
+
 class CommitArgs(ctypes.Structure):
     """Mirror of ``kda_commit_args``."""
     _fields_ = [
@@ -104,6 +109,8 @@ def load_library():
             lib = ctypes.CDLL(_LIB_PATH)
             lib.kda_verify.argtypes = [ctypes.POINTER(VerifyArgs), _p]
             lib.kda_verify.restype = ctypes.c_int
+            lib.kda_verify_fold.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(FoldArgs), _p]
+            lib.kda_verify_fold.restype = ctypes.c_int
             lib.kda_commit.argtypes = [ctypes.POINTER(CommitArgs), _p]
             lib.kda_commit.restype = ctypes.c_int
             lib.kda_commit_noalloc.argtypes = [ctypes.POINTER(CommitArgs), _p]
@@ -182,7 +189,8 @@ def _ptr(t):
 def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state, correction,
            key_gate, query_start_loc, state_indices, conv_state, conv_weight, out, window,
            num_accepted_tokens=None, record_indices=None, conv_dim_first=True, null_block_id=0,
-           workspace=None, stream=None) -> None:
+           workspace=None, stream=None, fold_query_start_loc=None, fold_num_accepted=None,
+           fold_record_indices=None) -> None:
     """Verify ``state_indices.shape[0]`` requests of one KDA layer.
 
     ``mixed_qkv`` [T, 3HK] is the raw projection (before the convolution),
@@ -193,7 +201,13 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
     ``conv_state`` bf16 [slots, 3HK, window+2] (dim first) or
     [slots, window+2, 3HK], ``conv_weight`` bf16 or fp32 [3HK, 4].
     ``lower_bound`` None selects the softplus gate, a float the bounded one.
-    Asynchronous on ``stream`` (default: the current stream)."""
+    Asynchronous on ``stream`` (default: the current stream).
+
+    With ``fold_query_start_loc`` and ``fold_num_accepted`` (the previous
+    step's query_start_loc [B+1] and accepted counts [B], and optionally its
+    record rows ``fold_record_indices``) this is ``kda_verify_fold``: each
+    request's pending records are first folded into its checkpoint, which is
+    written back, and the verify runs on the folded state (windows up to 4)."""
     dev = state.device
     if dev.type != "cuda":
         raise ValueError("verify runs on a CUDA device; state is on " + str(dev))
@@ -244,6 +258,22 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
                 raise ValueError(f"{name} must be contiguous with at least B entries")
     if workspace is not None:
         _need(workspace, "workspace", torch.int32, dev)
+    fold = None
+    if fold_query_start_loc is not None:
+        if fold_num_accepted is None:
+            raise ValueError("fold_num_accepted is required with fold_query_start_loc")
+        _need(fold_query_start_loc, "fold_query_start_loc", torch.int32, dev, 1)
+        if fold_query_start_loc.shape[0] != B + 1 or not fold_query_start_loc.is_contiguous():
+            raise ValueError("fold_query_start_loc must be contiguous [B+1]")
+        for name, t in (("fold_num_accepted", fold_num_accepted), ("fold_record_indices", fold_record_indices)):
+            if t is not None:
+                _need(t, name, torch.int32, dev, 1)
+                if t.shape[0] < B or not t.is_contiguous():
+                    raise ValueError(f"{name} must be contiguous with at least B entries")
+        fold = FoldArgs()
+        fold.query_start_loc = fold_query_start_loc.data_ptr()
+        fold.num_accepted = fold_num_accepted.data_ptr()
+        fold.record_indices = _ptr(fold_record_indices)
 
     a = VerifyArgs()
     a.B, a.H, a.K, a.V, a.Q, a.W, a.T = B, H, K, V, window, 4, T
@@ -266,7 +296,11 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
     a.query_start_loc, a.state_indices = query_start_loc.data_ptr(), state_indices.data_ptr()
     a.record_indices, a.num_accepted_prev = _ptr(record_indices), _ptr(num_accepted_tokens)
     a.workspace = _ptr(workspace)
-    _check(load_library().kda_verify(ctypes.byref(a), ctypes.c_void_p(_stream_handle(dev, stream))))
+    handle = ctypes.c_void_p(_stream_handle(dev, stream))
+    if fold is None:
+        _check(load_library().kda_verify(ctypes.byref(a), handle))
+    else:
+        _check(load_library().kda_verify_fold(ctypes.byref(a), ctypes.byref(fold), handle))
 
 
 class CommitContext:

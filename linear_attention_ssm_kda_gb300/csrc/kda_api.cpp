@@ -57,7 +57,14 @@ size_t kda_workspace_bytes(void) { return 16; }
 
 const char* kda_last_error(void) { return g_error; }
 
-kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks the verify arguments and fills the launch parameters; *noop is set
+// when there is nothing to launch.
+kda_status verify_params(const kda_verify_args* a, bool fold, kda::VerifyParams& p, bool* noop) {
+  *noop = false;
   if (a == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify: args is NULL");
   if (a->B < 0 || a->T < 0) return fail(KDA_ERR_INVALID_ARG, "kda_verify: negative B (%d) or T (%d)", a->B, a->T);
   kda_status st = check_dims(a->H, a->K, a->V, a->Q);
@@ -65,7 +72,11 @@ kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
   if (a->W != kConvWidth) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: conv width %d, supported %d", a->W, kConvWidth);
   if ((long long)a->T > (long long)a->B * a->Q)
     return fail(KDA_ERR_INVALID_ARG, "kda_verify: %d token rows exceed B*Q = %lld", a->T, (long long)a->B * a->Q);
-  if (a->B == 0 || a->T == 0) return KDA_OK;
+  // the fold still has work when no token row is left
+  if (a->B == 0 || (a->T == 0 && !fold)) {
+    *noop = true;
+    return KDA_OK;
+  }
   const void* required[] = {a->mixed_qkv, a->raw_gate,  a->raw_beta, a->out,   a->A_log,
                             a->dt_bias,   a->conv_weight, a->conv_state, a->state, a->corr,
                             a->key_gate,  a->query_start_loc, a->state_indices};
@@ -104,7 +115,7 @@ kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
   if (!aligned(a->mixed_qkv, 2) || !aligned(a->raw_gate, 2) || !aligned(a->raw_beta, 2) || !aligned(a->out, 2))
     return fail(KDA_ERR_MISALIGNED, "kda_verify: bf16 activations must be 2-byte aligned");
 
-  kda::VerifyParams p{};
+  p = kda::VerifyParams{};
   p.B = a->B; p.H = a->H; p.Q = a->Q; p.T = a->T; p.null_block_id = a->null_block_id;
   p.num_slots = a->num_slots; p.num_record_rows = a->num_record_rows;
   p.mixed_qkv = static_cast<const uint16_t*>(a->mixed_qkv); p.qkv_stride = a->qkv_row_stride;
@@ -124,8 +135,37 @@ kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
   p.workspace = a->workspace;
   p.k_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(K)));
   if ((long long)p.B * p.H > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: B*H too large");
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
+  kda::VerifyParams p;
+  bool noop = false;
+  const kda_status st = verify_params(a, false, p, &noop);
+  if (st != KDA_OK || noop) return st;
   cudaError_t e = kda::launch_verify(p, a->K, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify: launch failed: %s", cudaGetErrorString(e));
+  return KDA_OK;
+}
+
+kda_status kda_verify_fold(const kda_verify_args* a, const kda_fold_args* f, kda_stream_t stream) {
+  if (f == nullptr || f->query_start_loc == nullptr) return kda_verify(a, stream);
+  if (f->num_accepted == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify_fold: num_accepted is NULL");
+  if (a != nullptr && a->Q > 4)
+    return fail(KDA_ERR_UNSUPPORTED, "kda_verify_fold: windows up to 4 tokens (Q = %d)", a->Q);
+  kda::VerifyParams p;
+  bool noop = false;
+  const kda_status st = verify_params(a, true, p, &noop);
+  if (st != KDA_OK || noop) return st;
+  p.fold_qsl = f->query_start_loc;
+  p.fold_num_accepted = f->num_accepted;
+  p.fold_record_indices = f->record_indices;
+  cudaError_t e = kda::launch_verify(p, a->K, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify_fold: launch failed: %s", cudaGetErrorString(e));
   return KDA_OK;
 }
 

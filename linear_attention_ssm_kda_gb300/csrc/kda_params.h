@@ -35,6 +35,10 @@ struct VerifyParams {
   // fp32 state pool [slots][H V][K] in K-slices of 32 (128-byte swizzle), for
   // the tensor-core path of the verify
   CUtensorMap tm_state;
+  // kda_verify_fold: each request's pending records of the previous step
+  // (query_start_loc, accepted counts, record rows or NULL for the state slot)
+  // folded into its checkpoint first; fold_qsl == nullptr: plain verify
+  const int* fold_qsl; const int* fold_num_accepted; const int* fold_record_indices;
 };
 
 struct CommitParams {

@@ -65,6 +65,11 @@ constexpr int kMmaWarp = 2 + kPrepWarps + kSplitWarps;  // warp 12 issues the MM
 
 constexpr int ru(int x, int a) { return (x + a - 1) / a * a; }
 
+// Kernel variants: the CUDA-core verify, the tcgen05 verify (opt-in), and the
+// CUDA-core verify that first folds each request's pending records of the
+// previous step into its checkpoint.
+enum : int { kVarPlain = 0, kVarTcgen05 = 1, kVarFold = 2 };
+
 enum : int { kLive = 1, kNull = 2 };
 
 // Inputs warp -> prep, per item.
@@ -74,6 +79,8 @@ struct SmallMeta {
   long long s, r;
   float A, pad;
   float beta[QMAX];
+  int fold_m, pad2;  // fold variant: pending records to fold, their row
+  long long fold_r;
 };
 
 // Prep -> gemv, per item (head of an operand slot).
@@ -82,16 +89,21 @@ struct OpMeta {
   int flags, bos, n, pad;
   long long r;
   float beta[QMAX];
+  int fold_m, pad2;   // fold variant: pending records folded into the chunk,
+  long long s;        // the slot the folded state goes back to,
+  float rkf[QMAX];    // and 1 / |k_u| (with the eps) of each pending key
 };
 
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 struct Layout {
   static_assert(7 * QMAX + 10 <= 96, "small-input copies per item exceed three per lane");
   // Tensor-core instantiation (K = 128, windows up to 4 tokens): the state
   // streams as K-slices of 32 (128 rows x 128 bytes, 128-byte swizzle) and the
   // products S0 [X | Y] come from tcgen05 MMAs; otherwise CUDA-core gemv warps.
-  static_assert(!TC || (KD == 128 && QMAX == 4), "the tensor-core path covers K = 128, windows up to 4");
-  static constexpr bool kTC = TC;
+  static_assert(VAR != kVarTcgen05 || (KD == 128 && QMAX == 4), "the tensor-core path covers K = 128, windows up to 4");
+  static_assert(VAR != kVarFold || QMAX <= 4, "the fold variant covers windows up to 4");
+  static constexpr bool kTC = VAR == kVarTcgen05;
+  static constexpr bool kFold = VAR == kVarFold;
   static constexpr int kThreads = 32 * (kTC ? kMmaWarp + 1 : 2 + kPrepWarps + kGemvWarps);
   static constexpr int RW = KD / kGemvWarps;  // state rows per gemv warp (one chunk)
   static constexpr int kChunk = kTC ? 128 * 32 * 4 : RW * KD * 4;  // bytes per state unit (chunk or K-slice)
@@ -104,7 +116,11 @@ struct Layout {
   static constexpr int kConv = ru(kGate + QMAX * kSeg, 128);           // the head's conv taps
   static constexpr int kW = ru(kConv + 3 * KD * kLcMax * 2, 128);      // [3][KD][W] weights
   static constexpr int kDt = ru(kW + 3 * KD * kConvWidth * 4, 128);    // [KD] dt_bias
-  static constexpr int kSmall = ru(kDt + KD * 4, 128);
+  // fold variant: the pending records of the item, [QMAX][2K] bf16 key/gate
+  // and [QMAX][V] fp32 corrections (V == K)
+  static constexpr int kFoldKg = ru(kDt + KD * 4, 128);
+  static constexpr int kFoldC = kFoldKg + (kFold ? QMAX * 2 * KD * 2 : 0);
+  static constexpr int kSmall = ru(kFoldC + (kFold ? QMAX * KD * 4 : 0), 128);
   // operand slot (prep -> gemv).  Tensor-core path: first the MMA's B operand,
   // [X | Y]_hi rows 0..7 and [X | Y]_lo rows 8..15, as four K-slices of
   // [16][32] fp32 with the 128-byte swizzle (8 KB), then the rest.
@@ -112,7 +128,12 @@ struct Layout {
   static constexpr int kOpVec = ru(kOpMeta + int(sizeof(OpMeta<QMAX>)), 16);  // [2 QMAX][KD] X_t | Y_t
   static constexpr int kOpV = kTC ? kOpVec : kOpVec + 2 * QMAX * KD * 4;        // [QMAX][KD] v_t
   static constexpr int kOpMN = kOpV + QMAX * KD * 4;                            // [QMAX][QMAX] M | N
-  static constexpr int kOp = ru(kOpMN + QMAX * QMAX * 4, kTC ? 1024 : 128);
+  // fold variant: prod_u e^{g_u} [K], the pending k_u prod_{w>u} e^{g_w}
+  // (unnormalised) [QMAX][K] and the pending corrections [QMAX][V]
+  static constexpr int kOpDall = ru(kOpMN + QMAX * QMAX * 4, 16);
+  static constexpr int kOpKd = kOpDall + (kFold ? KD * 4 : 0);
+  static constexpr int kOpFc = kOpKd + (kFold ? QMAX * KD * 4 : 0);
+  static constexpr int kOp = ru(kOpFc + (kFold ? QMAX * KD * 4 : 0), kTC ? 1024 : 128);
   // prep runs up to two items ahead of the gemv team; on the tensor-core path
   // an item's slot is also held until its readout, one item later
   static constexpr int kNumOp = kTC ? 4 : QMAX <= 4 ? 3 : 2;
@@ -120,7 +141,8 @@ struct Layout {
   static constexpr int kXs = 2 * QMAX * KD * 4;                        // [2][QMAX][KD] q | k conv outputs
   // per-warp scratch
   static constexpr int kRedPerWarp = kTC ? 0 : 2 * QMAX * RW;         // floats
-  static constexpr int kPart = ru(2 * QMAX + QMAX * QMAX, 32);         // reduced values per prep warp
+  static constexpr int kFoldIdx = 2 * QMAX + QMAX * QMAX;  // fold variant: |k_u|^2 of the pending keys
+  static constexpr int kPart = ru(kFoldIdx + (kFold ? QMAX : 0), 32);         // reduced values per prep warp
   static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kXs + kGemvWarps * kRedPerWarp * 4 +
                                 kPrepWarps * kPart * 4 + 32 + (2 * kNumSmall + 2 * kNumOp + 4) * 8 +
                                 (kTC ? 1024 : 0);
@@ -139,14 +161,16 @@ struct Layout {
   static constexpr int kNumBars = kBarsPerChunk * kNumChunk + 2 * kNumSmall + 2 * kNumOp + 4;
   static constexpr int kBytes = oBars + kNumBars * 8;
   static_assert(kBytes <= kSmemLimit, "shared memory budget");
-  static_assert(kTC ? kNumChunk >= 6 : kNumChunk >= 2 * kGemvWarps, "state in flight");
+  // at least six K-slices (tensor cores), 1.5 items of chunks (fold variant,
+  // whose slots carry the pending records) or two items of chunks in flight
+  static_assert(kNumChunk >= (kTC ? 6 : kFold ? 3 * kGemvWarps / 2 : 2 * kGemvWarps), "state in flight");
 };
 
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 struct Bars {
   uint64_t *ch_full, *ch_empty, *sm_full, *sm_empty, *op_full, *op_empty, *d_full, *d_empty, *hi_done, *lo_full;
   __device__ explicit Bars(unsigned char* smem) {
-    using Lay = Layout<KD, QMAX, TC>;
+    using Lay = Layout<KD, QMAX, VAR>;
     uint64_t* b = reinterpret_cast<uint64_t*>(smem + Lay::oBars);
     ch_full = b;
     ch_empty = b + Lay::kNumChunk;
@@ -192,11 +216,13 @@ template <int QMAX>
 struct ItemMeta {
   int flags, h, bos, n, a;
   long long s, r;
+  int fold_m;
+  long long fold_r;
 };
 
 template <int QMAX>
 __device__ __forceinline__ ItemMeta<QMAX> decode_item(const VerifyParams& p, int it, bool valid, bool report_errors) {
-  ItemMeta<QMAX> m{0, 0, 0, 0, 1, 0, 0};
+  ItemMeta<QMAX> m{0, 0, 0, 0, 1, 0, 0, 0, 0};
   if (!valid) return m;
   const int b = it / p.H;
   m.h = it - b * p.H;
@@ -206,14 +232,20 @@ __device__ __forceinline__ ItemMeta<QMAX> decode_item(const VerifyParams& p, int
   m.r = p.record_indices ? static_cast<long long>(p.record_indices[b]) : m.s;
   m.a = p.num_accepted_prev ? min(max(p.num_accepted_prev[b], 1), p.Q) : 1;
   m.n = min(max(len, 0), p.Q);
+  if (p.fold_qsl != nullptr) {  // the previous step's pending records, folded first
+    const int plen = p.fold_qsl[b + 1] - p.fold_qsl[b];
+    m.fold_m = min(max(p.fold_num_accepted[b], 0), min(max(plen, 0), p.Q));
+    m.fold_r = p.fold_record_indices ? static_cast<long long>(p.fold_record_indices[b]) : m.s;
+  }
   if (len < 0 || (m.n > 0 && (m.bos < 0 || m.bos + m.n > p.T))) {
     if (report_errors) report(p.workspace, KDA_DEVERR_TOKEN_RANGE, it);
-  } else if (m.n > 0) {
+  } else if (m.n > 0 || m.fold_m > 0) {
     if (m.s <= p.null_block_id) {
-      m.flags = kNull;
+      m.flags = m.n > 0 ? kNull : 0;
     } else if (m.s < 0 || m.s >= p.num_slots) {
       if (report_errors) report(p.workspace, KDA_DEVERR_SLOT_RANGE, it);
-    } else if (m.r < 0 || m.r >= p.num_record_rows) {
+    } else if ((m.n > 0 && (m.r < 0 || m.r >= p.num_record_rows)) ||
+               (m.fold_m > 0 && (m.fold_r < 0 || m.fold_r >= p.num_record_rows))) {
       if (report_errors) report(p.workspace, KDA_DEVERR_ROW_RANGE, it);
     } else {
       m.flags = kLive;
@@ -232,10 +264,10 @@ __device__ __forceinline__ int hull_offset(const void* src) {
 // order: 3n activation row segments (token t, group g), n gate row segments,
 // the head's conv taps (3 blocks dim-first, 3 (Q+W-2) rows seq-first), three
 // conv-weight blocks and dt_bias.  Returns false past the last copy.
-template <int KD, int QMAX, bool DF, bool TC>
+template <int KD, int QMAX, bool DF, int VAR>
 __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, int bos, long long s, int h,
                                            unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   const long long HK = static_cast<long long>(p.H) * KD;
   const int Lc = p.Q + kConvWidth - 2;
   const unsigned char* ptr;
@@ -293,10 +325,10 @@ __device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, 
 // Kinds by lane q: activation (t = q / 3, g = q % 3) for q < 3n, gate
 // (t = q - 3n) for q < 4n, conv taps of group q - 4n, conv weights of group
 // q - 4n - 3, dt_bias at q = 4n + 6.  Returns false for lanes past the last copy.
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 __device__ __forceinline__ bool small_copy_lane(const VerifyParams& p, int q, int n, int bos, long long s, int h,
                                                 unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   const long long HK = static_cast<long long>(p.H) * KD;
   const int Lc = p.Q + kConvWidth - 2;
   const int wb = p.conv_weight_fp32 ? 4 : 2;
@@ -334,10 +366,23 @@ __device__ __forceinline__ bool small_copy_lane(const VerifyParams& p, int q, in
 
 // ---------------------------------------------------------------- inputs warp
 
-template <int KD, int QMAX, bool DF, bool TC>
+// Fold variant: bulk copies of an item's pending records (the first m tokens'
+// key/gate rows and corrections of head h in record row r) into its
+// small-input slot; the barrier's expected bytes already count them.
+template <int KD, int QMAX, int VAR>
+__device__ __forceinline__ void fold_copies(const VerifyParams& p, unsigned char* sl, int h, int m, long long r,
+                                            uint64_t* bar) {
+  using Lay = Layout<KD, QMAX, VAR>;
+  const uint16_t* kg = p.key_gate + r * p.kg_stride + static_cast<long long>(h) * p.Q * 2 * KD;
+  const float* c = p.corr + r * p.corr_stride + static_cast<long long>(h) * p.Q * KD;
+  bulk_g2s(sl + Lay::kFoldKg, kg, static_cast<uint32_t>(m) * 2 * KD * 2, bar);
+  bulk_g2s(sl + Lay::kFoldC, c, static_cast<uint32_t>(m) * KD * 4, bar);
+}
+
+template <int KD, int QMAX, bool DF, int VAR>
 __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
-  using Lay = Layout<KD, QMAX, TC>;
-  Bars<KD, QMAX, TC> bars(smem);
+  using Lay = Layout<KD, QMAX, VAR>;
+  Bars<KD, QMAX, VAR> bars(smem);
   const int nloc = local_items(p.B * p.H);
   bool ok = true;
   for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
@@ -363,6 +408,9 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
     own.pad = 0.0f;
 #pragma unroll
     for (int t = 0; t < QMAX; ++t) own.beta[t] = beta[t];
+    own.fold_m = im.fold_m;
+    own.pad2 = 0;
+    own.fold_r = im.fold_r;
     const int count = min(32, nloc - i0);
     for (int j = 0; j < count && ok; ++j) {
       const int i = i0 + j;
@@ -371,6 +419,10 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
       const int jn = __shfl_sync(0xffffffffu, im.n, j);
       const long long js = shfl_ll(im.s, j);
       const int jh = __shfl_sync(0xffffffffu, im.h, j);
+      const int jfm = Lay::kFold ? __shfl_sync(0xffffffffu, im.fold_m, j) : 0;
+      const long long jfr = Lay::kFold ? shfl_ll(im.fold_r, j) : 0;
+      // fold variant: the item's pending key/gate and correction records
+      const uint32_t fold_bytes = (jflags & kLive) ? static_cast<uint32_t>(jfm) * (2 * KD * 2 + KD * 4) : 0u;
       const int slot = i % Lay::kNumSmall;
       ok = warp_wait(&bars.sm_empty[slot], ((i / Lay::kNumSmall) & 1) ^ 1, lane, abort_flag);
       if (!ok) break;
@@ -384,9 +436,10 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
           const int wb = p.conv_weight_fp32 ? 4 : 2;
           const int G = p.act_mode == 1 ? 4 : 3;
           const uint32_t total = KD * G * p.Q * 2 + (p.act_mode == 2 ? KD * p.Q * 2 : 0) + 3 * KD * Lc * 2 +
-                                 3 * KD * kConvWidth * wb + KD * 4;
+                                 3 * KD * kConvWidth * wb + KD * 4 + fold_bytes;
           uint64_t* bar = &bars.sm_full[slot];
           mbar_arrive_expect_tx(bar, total);
+          if (fold_bytes) fold_copies<KD, QMAX, VAR>(p, sl, jh, jfm, jfr, bar);
           tma_load_3d(sl + Lay::kAct, &p.tm_act, jh * KD, 0, jbos, bar);
           if (p.act_mode == 2) tma_load_2d(sl + Lay::kGate, &p.tm_gate, jh * KD, jbos, bar);
           if (DF)
@@ -405,19 +458,22 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
         uint32_t bytes[3] = {0, 0, 0};
         uint32_t mine = 0;
         if (DF && 4 * QMAX + 7 <= 32) {  // one copy per lane, computed without branches
-          if (!small_copy_lane<KD, QMAX, TC>(p, lane, jn, jbos, js, jh, sl, &src[0], &dst[0], &bytes[0]))
+          if (!small_copy_lane<KD, QMAX, VAR>(p, lane, jn, jbos, js, jh, sl, &src[0], &dst[0], &bytes[0]))
             bytes[0] = 0;
           mine = bytes[0];
         } else {
 #pragma unroll
           for (int c = 0; c < 3; ++c) {
-            if (!small_copy<KD, QMAX, DF, TC>(p, lane + 32 * c, jn, jbos, js, jh, sl, &src[c], &dst[c], &bytes[c]))
+            if (!small_copy<KD, QMAX, DF, VAR>(p, lane + 32 * c, jn, jbos, js, jh, sl, &src[c], &dst[c], &bytes[c]))
               bytes[c] = 0;
             mine += bytes[c];
           }
         }
-        mine = __reduce_add_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_arrive_expect_tx(&bars.sm_full[slot], mine);
+        mine = __reduce_add_sync(0xffffffffu, mine) + fold_bytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars.sm_full[slot], mine);
+          if (fold_bytes) fold_copies<KD, QMAX, VAR>(p, sl, jh, jfm, jfr, &bars.sm_full[slot]);
+        }
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 3; ++c)
@@ -436,10 +492,10 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
 
 // ---------------------------------------------------------------- state warp
 
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
-  using Lay = Layout<KD, QMAX, TC>;
-  Bars<KD, QMAX, TC> bars(smem);
+  using Lay = Layout<KD, QMAX, VAR>;
+  Bars<KD, QMAX, VAR> bars(smem);
   const int nloc = local_items(p.B * p.H);
   uint32_t ch_cnt = 0;
   bool ok = true;
@@ -499,10 +555,10 @@ struct ConvIn {
   uint16_t seq[kConvWidth - 1 + QMAX + 1];
 };
 
-template <int KD, int QMAX, bool DF, bool TC>
+template <int KD, int QMAX, bool DF, int VAR>
 __device__ __forceinline__ void conv_load(const VerifyParams& p, const unsigned char* sl, int g, int k, int n, int a,
                                           int Lc, uint32_t act_lo, ConvIn<QMAX>& in) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   const uint16_t* conv = reinterpret_cast<const uint16_t*>(sl + Lay::kConv);
   if (p.conv_weight_fp32) {
     const float4 wv = reinterpret_cast<const float4*>(sl + Lay::kW)[g * KD + k];
@@ -550,7 +606,7 @@ __device__ __forceinline__ void conv_pairs(const ConvIn<QMAX>& in, uint16_t (&y)
   }
 }
 
-template <int KD, int QMAX, bool DF, bool TC>
+template <int KD, int QMAX, bool DF, int VAR>
 __device__ __forceinline__ void conv_roll(const VerifyParams& p, const ConvIn<QMAX>& in, int g, int k, int n, int Lc,
                                           uint16_t* gconv, long long hk) {
   const long long HK = static_cast<long long>(p.H) * KD;
@@ -595,19 +651,18 @@ __device__ __forceinline__ void conv_two(const ConvIn<QMAX>& in0, const ConvIn<Q
   }
 }
 
-template <int KD, int QMAX, bool DF, bool TC>
+template <int KD, int QMAX, bool DF, int VAR>
 __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatile int* misc) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   constexpr int NREDP = Lay::kPart;  // |q_t|^2, |k_t|^2, raw M / N grid, padded to 32
   constexpr int PER = NREDP / 32;
-  Bars<KD, QMAX, TC> bars(smem);
+  Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   float* part = reinterpret_cast<float*>(smem + Lay::oPart);
   float* xs = reinterpret_cast<float*>(smem + Lay::oXs);  // [2][QMAX][KD] q | k
   const int warp = pt >> 5;
   const int lane = pt & 31;
   const int nloc = local_items(p.B * p.H);
-  const long long HK = static_cast<long long>(p.H) * KD;
   const int Lc = p.Q + kConvWidth - 2;
   const uint32_t qkv_lo = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.mixed_qkv));
   const uint32_t gate_lo = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.raw_gate));
@@ -634,7 +689,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
         p.out[static_cast<long long>(m.bos + t) * p.out_stride + static_cast<long long>(h) * KD + (e - t * KD)] = 0;
       }
     }
-    if (live) {
+    if (live && n > 0) {  // (a fold-only item of the fold variant has no window)
       const uint32_t act_lo = qkv_lo + static_cast<uint32_t>(m.bos) * static_cast<uint32_t>(p.qkv_stride) * 2u + hoff;
       uint16_t* gconv = p.conv_state + m.s * p.conv_slot_stride;
       const long long hk = static_cast<long long>(h) * KD;
@@ -644,9 +699,9 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       const int g0 = c0 / KD, k0 = c0 - g0 * KD;
       const int g1 = c1 / KD, k1 = c1 - g1 * KD;
       ConvIn<QMAX> in0, in1;
-      conv_load<KD, QMAX, DF, TC>(p, sl, g0, k0, n, m.a, Lc, act_lo, in0);
+      conv_load<KD, QMAX, DF, VAR>(p, sl, g0, k0, n, m.a, Lc, act_lo, in0);
       if (has1) {
-        conv_load<KD, QMAX, DF, TC>(p, sl, g1, k1, n, m.a, Lc, act_lo, in1);
+        conv_load<KD, QMAX, DF, VAR>(p, sl, g1, k1, n, m.a, Lc, act_lo, in1);
       } else {
 #pragma unroll
         for (int j = 0; j < kConvWidth; ++j) in1.w[j] = 0.0f;
@@ -655,8 +710,8 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       }
       uint16_t y0[QMAX], y1[QMAX];
       conv_two<QMAX>(in0, in1, n, y0, y1);
-      conv_roll<KD, QMAX, DF, TC>(p, in0, g0, k0, n, Lc, gconv, hk);
-      if (has1) conv_roll<KD, QMAX, DF, TC>(p, in1, g1, k1, n, Lc, gconv, hk);
+      conv_roll<KD, QMAX, DF, VAR>(p, in0, g0, k0, n, Lc, gconv, hk);
+      if (has1) conv_roll<KD, QMAX, DF, VAR>(p, in1, g1, k1, n, Lc, gconv, hk);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         if (cc == 1 && !has1) break;
@@ -728,6 +783,38 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
             vals[2 * QMAX + t * QMAX + u] = wu * kv[t];
           }
           vals[2 * QMAX + u * QMAX + t] = wu * qv[t];
+        }
+      }
+      if constexpr (Lay::kFold) {
+        // the pending records of the previous step: key k_u and decay e^{g_u}
+        // (this layer's gate), the unnormalised k_u prod_{w>u} e^{g_w}, the
+        // product of all the decays, |k_u|^2 into the reduction, and the
+        // corrections c_u of row v = k handed on to the gemv team
+        static_assert(Lay::kFoldIdx + QMAX <= NREDP, "room for the pending keys' norms");
+        const int mf = m.fold_m;
+        if (mf > 0) {
+          const uint16_t* fkg = reinterpret_cast<const uint16_t*>(sl + Lay::kFoldKg);
+          const float* fc = reinterpret_cast<const float*>(sl + Lay::kFoldC);
+          float* dall = reinterpret_cast<float*>(op + Lay::kOpDall);
+          float* kd = reinterpret_cast<float*>(op + Lay::kOpKd);
+          float* oc = reinterpret_cast<float*>(op + Lay::kOpFc);
+          float kf[QMAX], ef[QMAX];
+#pragma unroll
+          for (int u = 0; u < QMAX; ++u) {
+            kf[u] = u < mf ? bf16_to_f32(fkg[u * 2 * KD + k]) : 0.0f;
+            ef[u] = u < mf ? kda_decay_fast(bf16_to_f32(fkg[u * 2 * KD + KD + k]), dtb, m.A, p.lower_bound_gate,
+                                            p.lower_bound)
+                           : 1.0f;
+            vals[Lay::kFoldIdx + u] = kf[u] * kf[u];
+            if (u < mf) oc[u * KD + k] = fc[u * KD + k];
+          }
+          float suffix = 1.0f;
+#pragma unroll
+          for (int u = QMAX - 1; u >= 0; --u) {
+            if (u < mf) kd[u * KD + k] = kf[u] * suffix;
+            suffix *= ef[u];
+          }
+          dall[k] = suffix;
         }
       }
       reduce_scatter_stage<NREDP>(vals, 16, (lane & 16) != 0);
@@ -815,6 +902,19 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       om->r = m.r;
 #pragma unroll
       for (int t = 0; t < QMAX; ++t) om->beta[t] = m.beta[t];
+      om->fold_m = 0;
+      om->pad2 = 0;
+      om->s = m.s;
+      if constexpr (Lay::kFold) {
+        om->fold_m = live ? m.fold_m : 0;
+#pragma unroll
+        for (int u = 0; u < QMAX; ++u) {
+          float kk = 0.0f;
+#pragma unroll
+          for (int w = 0; w < KD / 32; ++w) kk += part[w * NREDP + Lay::kFoldIdx + u];
+          om->rkf[u] = rsqrtf(kk + 1e-6f);  // k^_u = k_u rsqrt(|k_u|^2 + eps)
+        }
+      }
     }
     if constexpr (Lay::kTC) fence_async_shared();  // the B operand is read by the tensor cores
     named_barrier(kBarPrep, kPrepConvThreads);
@@ -896,10 +996,10 @@ __device__ __forceinline__ void gemv_chunk(const float* __restrict__ st, const f
 // even and R_0..R_{N-1} if kq is odd.  The two lanes of a row swap their
 // halves and both run the recurrence; the even lane stores the corrections,
 // the odd lane the outputs.
-template <int KD, int QMAX, int N, bool TC>
+template <int KD, int QMAX, int N, int VAR>
 __device__ __forceinline__ void solve_regs(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op,
                                            int h, int gw, int lane, const float (&mine)[8]) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   static_assert(Lay::RW == 16, "two lanes per row: 16 rows per gemv warp");
   const int kq = lane & 3;
   const int row = gw * Lay::RW + (lane >> 2) + 8 * (kq >> 1);
@@ -933,11 +1033,64 @@ __device__ __forceinline__ void solve_regs(const VerifyParams& p, const OpMeta<Q
   }
 }
 
-template <int KD, int QMAX, bool TC>
-__device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, int lane, volatile int* misc) {
-  using Lay = Layout<KD, QMAX, TC>;
+// Fold variant: the gemv warp's chunk (rows gw RW .. gw RW + RW - 1 of the
+// item's state, [RW][K] fp32 in shared memory) folded in place with the
+// previous step's pending records,
+//   S[v, k] <- S[v, k] prod_u e^{g_u}[k] + sum_u (c_u[v] / |k_u|) k_u[k] prod_{w>u} e^{g_w}[k],
+// which is the commit's fold; then one lane stores the folded rows back to
+// the checkpoint with a bulk copy (its smem read is awaited before the chunk
+// slot is released).
+template <int KD, int QMAX, int VAR>
+__device__ __forceinline__ void fold_chunk(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op,
+                                           int h, int gw, int lane, float* st) {
+  using Lay = Layout<KD, QMAX, VAR>;
   constexpr int RW = Lay::RW;
-  Bars<KD, QMAX, TC> bars(smem);
+  constexpr int C4 = KD / 4;  // float4 per row
+  static_assert(32 % C4 == 0, "a lane keeps one float4 column of the chunk");
+  const int kc = lane % C4;
+  const float4 d4 = reinterpret_cast<const float4*>(op + Lay::kOpDall)[kc];
+  const float* kd = reinterpret_cast<const float*>(op + Lay::kOpKd);
+  const float* oc = reinterpret_cast<const float*>(op + Lay::kOpFc);
+  const int mf = m.fold_m;
+  float4 k4[QMAX];
+#pragma unroll
+  for (int u = 0; u < QMAX; ++u)
+    k4[u] = u < mf ? reinterpret_cast<const float4*>(kd + u * KD)[kc] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float4* s4 = reinterpret_cast<float4*>(st);
+#pragma unroll 4
+  for (int e = lane; e < RW * C4; e += 32) {
+    const int row = e / C4;  // row of the chunk
+    float4 v = s4[e];
+    v.x *= d4.x;
+    v.y *= d4.y;
+    v.z *= d4.z;
+    v.w *= d4.w;
+#pragma unroll
+    for (int u = 0; u < QMAX; ++u) {
+      if (u < mf) {
+        const float c = oc[u * KD + gw * RW + row] * m.rkf[u];
+        v.x = fmaf(c, k4[u].x, v.x);
+        v.y = fmaf(c, k4[u].y, v.y);
+        v.z = fmaf(c, k4[u].z, v.z);
+        v.w = fmaf(c, k4[u].w, v.w);
+      }
+    }
+    s4[e] = v;
+  }
+  fence_async_shared();  // the folded rows are read by the bulk store
+  __syncwarp();
+  if (lane == 0) {
+    float* g = const_cast<float*>(p.state) + m.s * p.state_slot_stride + (static_cast<long long>(h) * KD + gw * RW) * KD;
+    bulk_s2g(g, st, RW * KD * 4);
+    bulk_commit();
+  }
+}
+
+template <int KD, int QMAX, int VAR>
+__device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, int lane, volatile int* misc) {
+  using Lay = Layout<KD, QMAX, VAR>;
+  constexpr int RW = Lay::RW;
+  Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   float* red = reinterpret_cast<float*>(smem + Lay::oRed) + gw * Lay::kRedPerWarp;
   const int nloc = local_items(p.B * p.H);
@@ -957,35 +1110,54 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
       const int pos = pc % Lay::kNumChunk;
       ok = warp_wait(&bars.ch_full[pos], (pc / Lay::kNumChunk) & 1, lane, abort_flag);
       if (!ok) break;
-      const float* st = reinterpret_cast<const float*>(smem + Lay::oChunks + pos * Lay::kChunk);
+      float* st = reinterpret_cast<float*>(smem + Lay::oChunks + pos * Lay::kChunk);
       const float* vec = reinterpret_cast<const float*>(op + Lay::kOpVec);
+      bool stored = false;  // the folded chunk is on its way back to the checkpoint
+      if constexpr (Lay::kFold) {
+        if (m.fold_m > 0) {
+          fold_chunk<KD, QMAX, VAR>(p, m, op, h, gw, lane, st);
+          stored = true;
+        }
+      }
+      // the chunk slot goes back to the state warp once the products (and the
+      // bulk store of a folded chunk) have read it
+      auto release = [&] {
+        __syncwarp();
+        if (lane == 0) {
+          if (stored) bulk_wait_read();
+          mbar_arrive(&bars.ch_empty[pos]);
+        }
+      };
+      if (n == 0) {  // fold only: no window to verify
+        release();
+        ++live;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
+        continue;
+      }
       float mine[8];
       if (KD == 128 && n <= 4) {  // one vector group: P | R stay in registers
         if constexpr (KD == 128) {
           switch (n) {
             case 1:
               gemv_chunk<KD, 2, false>(st, vec, red, lane, mine);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 1, TC>(p, m, op, h, gw, lane, mine);
+              release();
+              solve_regs<KD, QMAX, 1, VAR>(p, m, op, h, gw, lane, mine);
               break;
             case 2:
               gemv_chunk<KD, 4, false>(st, vec, red, lane, mine);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 2, TC>(p, m, op, h, gw, lane, mine);
+              release();
+              solve_regs<KD, QMAX, 2, VAR>(p, m, op, h, gw, lane, mine);
               break;
             case 3:
               gemv_chunk<KD, 6, false>(st, vec, red, lane, mine);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 3, TC>(p, m, op, h, gw, lane, mine);
+              release();
+              solve_regs<KD, QMAX, 3, VAR>(p, m, op, h, gw, lane, mine);
               break;
             default:
               gemv_chunk<KD, 8, false>(st, vec, red, lane, mine);
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
-              solve_regs<KD, QMAX, 4, TC>(p, m, op, h, gw, lane, mine);
+              release();
+              solve_regs<KD, QMAX, 4, VAR>(p, m, op, h, gw, lane, mine);
               break;
           }
         }
@@ -1002,8 +1174,7 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
           default: gemv_chunk<KD, 8, true>(st, vec + cg * KD, red + cg * RW, lane, mine); break;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.ch_empty[pos]);
+      release();
       if (lane < RW) {
         const int row = gw * RW + lane;
         const float* mn = reinterpret_cast<const float*>(op + Lay::kOpMN);
@@ -1032,6 +1203,7 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
   }
+  if (Lay::kFold && lane == 0) bulk_wait_all();  // the folded chunks have reached the checkpoint
   if (!ok && lane == 0) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
@@ -1051,10 +1223,10 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
 
 // State producer: each live item's state as four K-slices (TMA tiles of 128
 // rows x 32 fp32 with the 128-byte swizzle) into the ring of slice slots.
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 __device__ void tc_produce_state(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
-  using Lay = Layout<KD, QMAX, TC>;
-  Bars<KD, QMAX, TC> bars(smem);
+  using Lay = Layout<KD, QMAX, VAR>;
+  Bars<KD, QMAX, VAR> bars(smem);
   const int nloc = local_items(p.B * p.H);
   uint32_t g = 0;  // slices issued
   bool ok = true;
@@ -1105,12 +1277,12 @@ struct LoPending {
   uint64_t bk;
 };
 
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 __device__ __forceinline__ bool tc_issue_lo(unsigned char* smem, uint32_t taddr, LoPending& lp,
                                             const volatile int* abort_flag) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   constexpr uint32_t kIdesc = umma_idesc_tf32(128, 16);
-  Bars<KD, QMAX, TC> bars(smem);
+  Bars<KD, QMAX, VAR> bars(smem);
   if (!lp.valid) return true;
   lp.valid = false;
   if (!mbar_wait_or_abort(&bars.lo_full[lp.pos], (lp.g / Lay::kNumChunk) & 1, abort_flag)) return false;
@@ -1127,11 +1299,11 @@ __device__ __forceinline__ bool tc_issue_lo(unsigned char* smem, uint32_t taddr,
   return true;
 }
 
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int* misc) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   constexpr uint32_t kIdesc = umma_idesc_tf32(128, 16);
-  Bars<KD, QMAX, TC> bars(smem);
+  Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   const int nloc = local_items(p.B * p.H);
   const uint32_t taddr = static_cast<uint32_t>(misc[kMiscTaddr]);
@@ -1146,7 +1318,7 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
     if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
       // finish the previous item first: its operand slot may be the next one
       // the prep team needs
-      ok = tc_issue_lo<KD, QMAX, TC>(smem, taddr, lp, abort_flag);
+      ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag);
       mbar_arrive(&bars.op_empty[oslot]);
       continue;
     }
@@ -1164,12 +1336,12 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) umma_tf32(d, a + 2 * ks, bk + 2 * ks, kIdesc, kb > 0 || ks > 0);
       umma_commit(&bars.hi_done[pos]);
-      ok = tc_issue_lo<KD, QMAX, TC>(smem, taddr, lp, abort_flag);
+      ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag);
       lp = LoPending{true, kb == 3, pos, oslot, g, db, bk};
     }
     ++live;
   }
-  if (ok) ok = tc_issue_lo<KD, QMAX, TC>(smem, taddr, lp, abort_flag);
+  if (ok) ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag);
   if (!ok) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
@@ -1179,10 +1351,10 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
 // Readout team (4 warps, warp q of the CTA's last warpgroup reads tensor-memory
 // lanes 32 q .. 32 q + 31): each lane owns one state row; it sums the hi and
 // lo columns into P_t | R_t and runs the row's solve.
-template <int KD, int QMAX, int N, bool TC>
+template <int KD, int QMAX, int N, int VAR>
 __device__ __forceinline__ void tc_solve(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op, int h,
                                          int row, const float (&d)[16]) {
-  using Lay = Layout<KD, QMAX, TC>;
+  using Lay = Layout<KD, QMAX, VAR>;
   const float* mn = reinterpret_cast<const float*>(op + Lay::kOpMN);
   const float* xv = reinterpret_cast<const float*>(op + Lay::kOpV);
   float* corr = p.corr + m.r * p.corr_stride + static_cast<long long>(h) * p.Q * KD + row;
@@ -1206,11 +1378,11 @@ __device__ __forceinline__ void tc_solve(const VerifyParams& p, const OpMeta<QMA
 // Readout of a live item's products, in the split warp that owns tensor-memory
 // lanes 32 wq .. 32 wq + 31 (one state row per lane): P_t | R_t = hi column +
 // lo column, then the row's solve.  Releases the D buffer and the operand slot.
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 __device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char* smem, int i, uint32_t live, int wq,
                                            int lane, uint32_t taddr, const volatile int* abort_flag) {
-  using Lay = Layout<KD, QMAX, TC>;
-  Bars<KD, QMAX, TC> bars(smem);
+  using Lay = Layout<KD, QMAX, VAR>;
+  Bars<KD, QMAX, VAR> bars(smem);
   const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
   const int h = it - (it / p.H) * p.H;
   const int oslot = i % Lay::kNumOp;
@@ -1226,10 +1398,10 @@ __device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char*
   const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta);
   const int row = wq * 32 + lane;
   switch (m.n) {
-    case 1: tc_solve<KD, QMAX, 1, TC>(p, m, op, h, row, d); break;
-    case 2: tc_solve<KD, QMAX, 2, TC>(p, m, op, h, row, d); break;
-    case 3: tc_solve<KD, QMAX, 3, TC>(p, m, op, h, row, d); break;
-    default: tc_solve<KD, QMAX, 4, TC>(p, m, op, h, row, d); break;
+    case 1: tc_solve<KD, QMAX, 1, VAR>(p, m, op, h, row, d); break;
+    case 2: tc_solve<KD, QMAX, 2, VAR>(p, m, op, h, row, d); break;
+    case 3: tc_solve<KD, QMAX, 3, VAR>(p, m, op, h, row, d); break;
+    default: tc_solve<KD, QMAX, 4, VAR>(p, m, op, h, row, d); break;
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
@@ -1242,10 +1414,10 @@ __device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char*
 // slice in place with its low part S - S_hi for the S_lo products.
 // Two slices into an item, the warp reads out the previous live item, whose
 // MMAs have completed by then.
-template <int KD, int QMAX, bool TC>
+template <int KD, int QMAX, int VAR>
 __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, volatile int* misc) {
-  using Lay = Layout<KD, QMAX, TC>;
-  Bars<KD, QMAX, TC> bars(smem);
+  using Lay = Layout<KD, QMAX, VAR>;
+  Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   const int lane = st & 31;
   const int wq = st >> 5;
@@ -1262,7 +1434,7 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
     if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
       // read the pending item out now: with no live item to follow soon, its
       // operand slot would be missing when the prep team comes round to it
-      if (pending >= 0) ok = tc_readout<KD, QMAX, TC>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
+      if (pending >= 0) ok = tc_readout<KD, QMAX, VAR>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
       pending = -1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
@@ -1287,7 +1459,7 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
       fence_async_shared();  // the low parts are read by the tensor cores
       mbar_arrive(&bars.lo_full[pos]);
       if (kb == 1 && pending >= 0) {  // the pending item's MMAs are done by now
-        ok = tc_readout<KD, QMAX, TC>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
+        ok = tc_readout<KD, QMAX, VAR>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
         pending = -1;
       }
     }
@@ -1295,22 +1467,22 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
     pending = i;
     ++live;
   }
-  if (ok && pending >= 0) ok = tc_readout<KD, QMAX, TC>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
+  if (ok && pending >= 0) ok = tc_readout<KD, QMAX, VAR>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
   if (!ok && lane == 0) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
   }
 }
 
-template <int KD, int QMAX, bool DF, bool TC>
-__global__ void __launch_bounds__(Layout<KD, QMAX, TC>::kThreads, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
-  using Lay = Layout<KD, QMAX, TC>;
+template <int KD, int QMAX, bool DF, int VAR>
+__global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
+  using Lay = Layout<KD, QMAX, VAR>;
   extern __shared__ __align__(1024) unsigned char smem[];
   volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::oMisc);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   if (tid == 0) {
-    Bars<KD, QMAX, TC> bars(smem);
+    Bars<KD, QMAX, VAR> bars(smem);
     for (int i = 0; i < Lay::kNumChunk; ++i) {
       mbar_init(&bars.ch_full[i], 1);
       mbar_init(&bars.ch_empty[i], 1);
@@ -1352,21 +1524,21 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, TC>::kThreads, 1) verify_kern
   __syncthreads();
   if constexpr (Lay::kTC) tmem_fence_after();
   if (warp == 0) {
-    produce_inputs<KD, QMAX, DF, TC>(p, smem, tid & 31, misc + kMiscAbort);
+    produce_inputs<KD, QMAX, DF, VAR>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp == 1) {
     if constexpr (Lay::kTC)
-      tc_produce_state<KD, QMAX, TC>(p, smem, tid & 31, misc + kMiscAbort);
+      tc_produce_state<KD, QMAX, VAR>(p, smem, tid & 31, misc + kMiscAbort);
     else
-      produce_state<KD, QMAX, TC>(p, smem, tid & 31, misc + kMiscAbort);
+      produce_state<KD, QMAX, VAR>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp < 2 + kPrepWarps) {
-    prep<KD, QMAX, DF, TC>(p, smem, tid - 64, misc);
+    prep<KD, QMAX, DF, VAR>(p, smem, tid - 64, misc);
   } else if constexpr (Lay::kTC) {
     if (warp < kMmaWarp)
-      tc_split<KD, QMAX, TC>(p, smem, tid - 32 * (2 + kPrepWarps), misc);
+      tc_split<KD, QMAX, VAR>(p, smem, tid - 32 * (2 + kPrepWarps), misc);
     else if ((tid & 31) == 0)
-      tc_mma<KD, QMAX, TC>(p, smem, misc);
+      tc_mma<KD, QMAX, VAR>(p, smem, misc);
   } else {
-    gemv_team<KD, QMAX, TC>(p, smem, warp - 2 - kPrepWarps, tid & 31, misc);
+    gemv_team<KD, QMAX, VAR>(p, smem, warp - 2 - kPrepWarps, tid & 31, misc);
   }
   if constexpr (Lay::kTC) {
     // every role is done and the MMA issuer has seen its last MMAs complete:
@@ -1512,14 +1684,14 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int KD, int QMAX, bool DF, bool TC>
+template <int KD, int QMAX, bool DF, int VAR>
 cudaError_t launch(const VerifyParams& p, cudaStream_t stream) {
-  constexpr int bytes = Layout<KD, QMAX, TC>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, DF, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  constexpr int bytes = Layout<KD, QMAX, VAR>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, DF, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const int items = p.B * p.H;
   const int grid = items < sm_count() ? items : sm_count();
-  verify_kernel<KD, QMAX, DF, TC><<<grid, Layout<KD, QMAX, TC>::kThreads, bytes, stream>>>(p);
+  verify_kernel<KD, QMAX, DF, VAR><<<grid, Layout<KD, QMAX, VAR>::kThreads, bytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1530,14 +1702,19 @@ cudaError_t launch_verify(const VerifyParams& params, int K, cudaStream_t stream
   build_tensor_maps(p, K);
   // the conv-state layout is a template parameter: straight-line tap addressing
   const bool q4 = p.Q <= 4;
-  if (K == 128 && q4 && tcgen05_requested() && build_state_map(p, K))
-    return p.conv_dim_first ? launch<128, 4, true, true>(p, stream) : launch<128, 4, false, true>(p, stream);
-  if (p.conv_dim_first) {
-    if (K == 128) return q4 ? launch<128, 4, true, false>(p, stream) : launch<128, 8, true, false>(p, stream);
-    return q4 ? launch<64, 4, true, false>(p, stream) : launch<64, 8, true, false>(p, stream);
+  if (p.fold_qsl != nullptr) {  // the host accepts the fold for windows up to 4 only
+    if (!q4) return cudaErrorInvalidValue;
+    if (K == 128) return p.conv_dim_first ? launch<128, 4, true, kVarFold>(p, stream) : launch<128, 4, false, kVarFold>(p, stream);
+    return p.conv_dim_first ? launch<64, 4, true, kVarFold>(p, stream) : launch<64, 4, false, kVarFold>(p, stream);
   }
-  if (K == 128) return q4 ? launch<128, 4, false, false>(p, stream) : launch<128, 8, false, false>(p, stream);
-  return q4 ? launch<64, 4, false, false>(p, stream) : launch<64, 8, false, false>(p, stream);
+  if (K == 128 && q4 && tcgen05_requested() && build_state_map(p, K))
+    return p.conv_dim_first ? launch<128, 4, true, kVarTcgen05>(p, stream) : launch<128, 4, false, kVarTcgen05>(p, stream);
+  if (p.conv_dim_first) {
+    if (K == 128) return q4 ? launch<128, 4, true, kVarPlain>(p, stream) : launch<128, 8, true, kVarPlain>(p, stream);
+    return q4 ? launch<64, 4, true, kVarPlain>(p, stream) : launch<64, 8, true, kVarPlain>(p, stream);
+  }
+  if (K == 128) return q4 ? launch<128, 4, false, kVarPlain>(p, stream) : launch<128, 8, false, kVarPlain>(p, stream);
+  return q4 ? launch<64, 4, false, kVarPlain>(p, stream) : launch<64, 8, false, kVarPlain>(p, stream);
 }
 
 }  // namespace kda

@@ -37,7 +37,10 @@ def conv_state_view(prob: Problem, l: int) -> torch.Tensor:
 
 
 def verify_layer(prob: Problem, l: int, dm: DeviceMeta, *, out=None, workspace=None, stream=None,
-                 fused=None) -> None:
+                 fused=None, fold: DeviceMeta | None = None) -> None:
+    """One layer's verify.  With ``fold`` (the previous step's metadata) the
+    previous step's accepted records are folded into the checkpoints first,
+    in the same launch (``kda_verify_fold``)."""
     cfg = prob.cfg
     H, K = cfg.H, cfg.K
     f = prob.fused[l] if fused is None else fused
@@ -50,7 +53,10 @@ def verify_layer(prob: Problem, l: int, dm: DeviceMeta, *, out=None, workspace=N
         num_accepted_tokens=dm.num_accepted_prev, record_indices=dm.record_indices,
         conv_state=prob.conv_state[l], conv_weight=prob.conv_weight[l],
         out=prob.out[l] if out is None else out, window=cfg.Q, conv_dim_first=cfg.conv_dim_first,
-        workspace=workspace, stream=stream)
+        workspace=workspace, stream=stream,
+        fold_query_start_loc=None if fold is None else fold.query_start_loc,
+        fold_num_accepted=None if fold is None else fold.num_accepted,
+        fold_record_indices=None if fold is None else fold.record_indices)
 
 
 def commit_context(prob: Problem) -> kda.CommitContext:

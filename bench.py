@@ -56,9 +56,13 @@ def step_accounting(cfg, meta) -> dict:
                     + lens[~live].sum() * H * V * 2 + params)
     m = acc[live & (acc > 0)]
     commit = L * H * (m.size * 2 * 4 * V * K + (4 * V + 4 * K) * m.sum())
+    # the deferred schedule folds inside the verify, which reads the state once
+    # for both: one state read fewer per folded (layer, request, head)
+    deferred = L * verify_layer + commit - L * H * m.size * 4 * V * K
     return dict(tokens=int(lens[live].sum()), verify_layer_bytes=int(verify_layer),
                 verify_bytes=int(L * verify_layer), commit_bytes=int(commit),
-                step_bytes=int(L * verify_layer + commit), commit_items=int(L * H * m.size))
+                step_bytes=int(L * verify_layer + commit), commit_items=int(L * H * m.size),
+                deferred_step_bytes=int(deferred))
 
 
 def measured_peak_gbs():
@@ -291,6 +295,34 @@ def run_e2e(args, prob, ctx, stream, dev, world):
     return e2e_ms, e2e_steps, h2d, d2h
 
 
+def run_deferred(args, prob, dm, stream, dev, world):
+    """The deferred schedule of the same workload (``kda_verify_fold``): each
+    layer's verify first folds the previous step's accepted records into the
+    checkpoint, so a step is L launches and no commit launch.  Every step uses
+    the same request metadata, so each folds what the step before accepted."""
+    from workloads.drive import verify_layer
+
+    L = prob.cfg.L
+
+    def step():
+        for l in range(L):
+            verify_layer(prob, l, dm, stream=stream, fold=dm)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    d_start = torch.cuda.Event(enable_timing=True)
+    d_end = torch.cuda.Event(enable_timing=True)
+    steps = max(3, args.steps // 2)
+    barrier(world)
+    d_start.record(stream)
+    for _ in range(steps):
+        step()
+    d_end.record(stream)
+    torch.cuda.synchronize(dev)
+    return d_start.elapsed_time(d_end), steps
+
+
 def run_gpu(args, rank, local, world):
     import linear_attention_ssm_kda_gb300 as kda
     from linear_attention_ssm_kda_gb300 import _build
@@ -359,6 +391,9 @@ def run_gpu(args, rank, local, world):
     e2e_ms, e2e_steps, h2d, d2h = None, 0, 0, 0
     if not args.no_e2e:
         e2e_ms, e2e_steps, h2d, d2h = run_e2e(args, prob, ctx, stream, dev, world)
+    d_ms, d_steps = None, 0
+    if not args.no_deferred and cfg.Q <= 4:
+        d_ms, d_steps = run_deferred(args, prob, dm, stream, dev, world)
 
     # aggregate over ranks: units of all ranks / the slowest rank's time
     t_max = max_over_ranks(elapsed_ms, world)
@@ -366,6 +401,9 @@ def run_gpu(args, rank, local, world):
     tokens_all = sum_over_ranks(acct["tokens"] * args.steps, world)
     tokens_e2e = sum_over_ranks(acct["tokens"] * e2e_steps, world)
     bytes_all = sum_over_ranks(acct["step_bytes"] * args.steps, world)
+    d_max = max_over_ranks(d_ms, world) if d_ms is not None else None
+    tokens_d = sum_over_ranks(acct["tokens"] * d_steps, world)
+    bytes_d = sum_over_ranks(acct["deferred_step_bytes"] * d_steps, world)
     if rank != 0:
         return None
     ms_per_step = t_max / args.steps
@@ -418,6 +456,12 @@ def run_gpu(args, rank, local, world):
             "value": tokens_e2e / (e_max / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
             "copies": "per layer on two copy streams, overlapping the other layers' kernels"},
+        "deferred": None if d_max is None else {
+            "value": tokens_d / (d_max / 1e3), "unit": "tokens/s", "ms_per_step": d_max / d_steps,
+            "achieved_hbm_gbs": bytes_d / (d_max / 1e3) / 1e9,
+            "algorithmic_bytes_per_step": acct["deferred_step_bytes"], "steps": d_steps,
+            "schedule": "each layer's verify first folds the previous step's accepted records into the "
+                        "checkpoint (kda_verify_fold), no commit launch"},
         "gpu_launches": args.steps * (L + 1),
         "clocks": clk,
         "cpu_baseline": cpu,
@@ -466,6 +510,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (small cases for profiling; not a bench line)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-deferred", action="store_true", help="skip the deferred-schedule timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -87,6 +87,8 @@ class _CommitArgs(ctypes.Structure):
         ("query_start_loc", _p), ("state_indices", _p), ("record_indices", _p),
         ("num_accepted", _p), ("item_mask", _p),
         ("num_threads", _i32),
+        ("final_state_indices", _p), ("boundary_state_indices", _p), ("boundary_recovery_lens", _p),
+        ("boundary_exact", _p),
     ]
 
 
@@ -235,10 +237,17 @@ def verify(*, H, K, Q, W, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_b
 
 def commit(*, H, K, Q, state, corr, key_gate, A_log, dt_bias, lower_bound,
            query_start_loc, state_indices, num_accepted, record_indices=None,
-           null_block_id=0, item_mask=None, want_exact=False, num_threads=0):
+           null_block_id=0, item_mask=None, want_exact=False, num_threads=0,
+           final_state_indices=None, boundary_state_indices=None, boundary_recovery_lens=None,
+           boundary_exact=None):
     """One layer's commit: folds each request's first
     min(max(num_accepted, 0), query_len) records into ``state`` (fp32, in
-    place).  Returns the unrounded double states [B, H, V, K] when asked."""
+    place).  Returns the unrounded double states [B, H, V, K] when asked.
+
+    Align mode: the committed state goes to ``final_state_indices[b]`` (None:
+    the source slot), and a live ``boundary_state_indices[b]`` receives the
+    state after the first ``boundary_recovery_lens[b]`` tokens (its unrounded
+    value into ``boundary_exact`` [B, H, V, K] float64 when given)."""
     lib = _load()
     B = int(state_indices.shape[0])
     V = K
@@ -265,6 +274,13 @@ def commit(*, H, K, Q, state, corr, key_gate, A_log, dt_bias, lower_bound,
     a.num_accepted = _ptr(num_accepted, np.int32)
     a.item_mask = _ptr(item_mask, np.uint8)
     a.num_threads = num_threads
+    a.final_state_indices = _ptr(final_state_indices, np.int32)
+    a.boundary_state_indices = _ptr(boundary_state_indices, np.int32)
+    a.boundary_recovery_lens = _ptr(boundary_recovery_lens, np.int32)
+    if boundary_exact is not None:
+        if boundary_exact.dtype != np.float64 or boundary_exact.shape != (B, H, V, K):
+            raise ValueError("boundary_exact must be float64 [B, H, V, K]")
+    a.boundary_exact = _ptr(boundary_exact)
     st = lib.kda_oracle_commit(ctypes.byref(a))
     if st != 0:
         raise RuntimeError(f"oracle commit: status {st}")

@@ -404,12 +404,21 @@ typedef struct {
     const int32_t *query_start_loc, *state_indices, *record_indices, *num_accepted;
     const uint8_t *item_mask;   /* [B*H] or NULL */
     int32_t num_threads;
+    /* align mode (prefix caching), all [B] or NULL: the slot the committed
+     * state goes to (NULL: the source slot), and a boundary slot that receives
+     * the state after the first boundary_recovery_lens[b] of the m tokens */
+    const int32_t *final_state_indices, *boundary_state_indices, *boundary_recovery_lens;
+    double *boundary_exact;     /* [B,H,V,K] or NULL: unrounded boundary states */
 } kda_oracle_commit_args;
 
 /* [ops] _commit_kda_state_kernel: the accepted state is the verify's running
  * state after m tokens.  Each recorded step is replayed in order from the
  * stored records: k^ and the gate are recomputed from the key/gate record,
- * c is the stored correction, and S <- S diag(e^g) + c k^T. */
+ * c is the stored correction, and S <- S diag(e^g) + c k^T.
+ * Align mode (the kernel's ALIGN_MODE): the state after the tokens before the
+ * boundary recovery length R also goes to the boundary slot when that slot is
+ * live, and the committed state goes to the final slot; a final slot at or
+ * below the null block writes nothing. */
 static int commit_item(const kda_oracle_commit_args *a, int b, int h) {
     const int K = a->K, V = a->V, Q = a->Q;
     int64_t s = a->state_indices[b];
@@ -421,12 +430,18 @@ static int commit_item(const kda_oracle_commit_args *a, int b, int h) {
     if (m == 0) return ORACLE_OK;
     int64_t r = a->record_indices ? a->record_indices[b] : s;
     if (s >= a->num_slots || r < 0 || r >= a->num_record_rows) return ORACLE_BAD_DATA;
+    const int64_t fs = a->final_state_indices ? a->final_state_indices[b] : s;
+    if (fs <= a->null_block_id) return ORACLE_OK;
+    const int64_t bs = a->boundary_state_indices ? a->boundary_state_indices[b] : a->null_block_id;
+    if (fs >= a->num_slots || bs >= a->num_slots) return ORACLE_BAD_DATA;
+    const int R = a->boundary_recovery_lens ? a->boundary_recovery_lens[b] : 0;
 
     float *S0 = a->state + s * a->state_slot_stride + (int64_t)h * V * K;
     double *S = (double *)malloc(sizeof(double) * (size_t)V * K);
+    double *Sb = (double *)malloc(sizeof(double) * (size_t)V * K);
     double *kn = (double *)malloc(sizeof(double) * K);
     double *eg = (double *)malloc(sizeof(double) * K);
-    for (int64_t e = 0; e < (int64_t)V * K; ++e) S[e] = (double)S0[e];
+    for (int64_t e = 0; e < (int64_t)V * K; ++e) S[e] = Sb[e] = (double)S0[e];
     double A = exp((double)a->A_log[h]);
     for (int t = 0; t < m; ++t) {
         const uint16_t *kg = a->key_gate + r * a->kg_row_stride + ((int64_t)h * Q + t) * 2 * K;
@@ -442,12 +457,25 @@ static int commit_item(const kda_oracle_commit_args *a, int b, int h) {
         for (int v = 0; v < V; ++v)
             for (int k = 0; k < K; ++k)
                 S[(size_t)v * K + k] = S[(size_t)v * K + k] * eg[k] + (double)c[v] * kn[k];
+        if (t + 1 == R)  /* the state after the tokens before the boundary */
+            for (int64_t e = 0; e < (int64_t)V * K; ++e) Sb[e] = S[e];
     }
+    if (R > m)  /* the boundary lies past the committed tokens: it holds them all */
+        for (int64_t e = 0; e < (int64_t)V * K; ++e) Sb[e] = S[e];
+    const int64_t off = (int64_t)h * V * K;
+    if (bs > a->null_block_id) {  /* written first: a final slot equal to it wins */
+        float *Bst = a->state + bs * a->state_slot_stride + off;
+        for (int64_t e = 0; e < (int64_t)V * K; ++e) {
+            Bst[e] = (float)Sb[e];
+            if (a->boundary_exact) a->boundary_exact[((int64_t)b * a->H + h) * (int64_t)V * K + e] = Sb[e];
+        }
+    }
+    float *F = a->state + fs * a->state_slot_stride + off;
     for (int64_t e = 0; e < (int64_t)V * K; ++e) {
-        S0[e] = (float)S[e];
+        F[e] = (float)S[e];
         if (a->state_exact) a->state_exact[((int64_t)b * a->H + h) * (int64_t)V * K + e] = S[e];
     }
-    free(S); free(kn); free(eg);
+    free(S); free(Sb); free(kn); free(eg);
     return ORACLE_OK;
 }
 

@@ -291,6 +291,80 @@ def test_commit_prefix_property(lb):
                                                atol=2e-6 * np.abs(ref).max())
 
 
+@pytest.mark.parametrize("lb", [None, -5.0])
+def test_align_commit_boundary_is_the_state_after_r_tokens(lb):
+    """Align mode ([ops] _commit_kda_state_kernel, ALIGN_MODE): the boundary
+    slot receives the state after the first min(R, m) tokens, which is the
+    verify's running state (S0 itself for R = 0) and the plain commit of that
+    many tokens bit for bit; the final slot receives the committed state; the
+    source slot keeps S0."""
+    cfg = _tiny(B=4, slots=16, K=8, lower_bound=lb)
+    prob = make_problem(cfg)
+    meta = prob.meta
+    B, H = cfg.B, cfg.H
+    hl = host_layer(prob, 0)
+    res = run_verify(prob, hl, want_running=True)
+    lens = np.minimum(np.diff(meta.query_start_loc), cfg.Q)
+    acc = np.minimum(np.maximum(meta.num_accepted, 0), lens)
+    used = {int(x) for x in meta.state_indices if x > 0}
+    free = [x for x in range(1, cfg.slots) if x not in used]
+    final = np.array(free[:B], np.int32)
+    bnd = np.array(free[B:2 * B], np.int32)
+    R = np.array([0, 1, 2, 9], np.int32)  # none, inside the window, past it
+    S0 = hl.state.copy()
+    bexact = np.full((B, H, cfg.K, cfg.K), np.nan)
+    exact = run_commit(prob, hl, want_exact=True, final_state_indices=final, boundary_state_indices=bnd,
+                       boundary_recovery_lens=R, boundary_exact=bexact)
+    # the plain commit of min(R, m) and of m tokens, on copies
+    plain = {}
+    for name, counts in (("boundary", np.minimum(R, acc)), ("final", acc)):
+        hl2 = host_layer(prob, 0)
+        hl2.corr[...] = hl.corr
+        hl2.key_gate[...] = hl.key_gate
+        hl2.state[...] = S0
+        saved = meta.num_accepted
+        meta.num_accepted = counts.astype(np.int32)
+        run_commit(prob, hl2)
+        meta.num_accepted = saved
+        plain[name] = hl2.state
+    checked = 0
+    for b in range(B):
+        s = int(meta.state_indices[b])
+        if s <= 0 or acc[b] == 0:
+            np.testing.assert_array_equal(hl.state[final[b]], S0[final[b]])
+            np.testing.assert_array_equal(hl.state[bnd[b]], S0[bnd[b]])
+            continue
+        np.testing.assert_array_equal(hl.state[s], S0[s])  # the source keeps S0
+        rb = min(int(R[b]), int(acc[b]))
+        for h in range(H):
+            np.testing.assert_array_equal(hl.state[bnd[b], h], plain["boundary"][s, h])
+            np.testing.assert_array_equal(hl.state[final[b], h], plain["final"][s, h])
+            np.testing.assert_array_equal(hl.state[final[b], h], exact[b, h].astype(np.float32))
+            np.testing.assert_array_equal(hl.state[bnd[b], h], bexact[b, h].astype(np.float32))
+            if rb == 0:
+                np.testing.assert_array_equal(hl.state[bnd[b], h], S0[s, h])
+            else:
+                ref = res["running_state"][b, h, rb - 1]
+                np.testing.assert_allclose(hl.state[bnd[b], h], ref, rtol=0, atol=2e-6 * np.abs(ref).max())
+            checked += 1
+    assert checked >= 4
+
+
+def test_align_commit_null_final_slot_writes_nothing():
+    prob = make_problem(_tiny(B=4, slots=16))
+    meta = prob.meta
+    meta.num_accepted[:] = np.minimum(np.diff(meta.query_start_loc), 4)
+    hl = host_layer(prob, 0)
+    run_verify(prob, hl)
+    before = hl.state.copy()
+    B = prob.cfg.B
+    final = np.zeros(B, np.int32)  # every final slot null
+    bnd = np.arange(10, 10 + B, dtype=np.int32)
+    run_commit(prob, hl, final_state_indices=final, boundary_state_indices=bnd,
+               boundary_recovery_lens=np.ones(B, np.int32))
+    np.testing.assert_array_equal(hl.state, before)
+
+
 def test_commit_zero_accepted_and_null_are_bit_identical():
     prob = make_problem(_tiny(B=4, slots=8))
     meta = prob.meta

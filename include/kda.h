@@ -223,6 +223,32 @@ typedef struct kda_fold_args {
 
 kda_status kda_verify_fold(const kda_verify_args *args, const kda_fold_args *fold, kda_stream_t stream);
 
+/*
+ * kda_commit_align -- kda_commit in the align mode of prefix caching
+ * ("vLLM/vllm/models/kimi_k3/nvidia/ops/recoverssm.py",
+ * _commit_kda_state_kernel with ALIGN_MODE; the mode is chosen per step in
+ * "vllm.models.kimi_k3.nvidia.specialized_decode.recoverssm.state",
+ * _build_deferred).  Per (layer, request, head) with a live source slot s and
+ * m > 0 as in kda_commit (records read at row r from S = state[s]):
+ *   - fs = final_state_indices ? final_state_indices[b] : s; fs at or below
+ *     null_block_id writes nothing; otherwise state[fs] = the committed state;
+ *   - bs = boundary_state_indices ? boundary_state_indices[b] : null; when
+ *     bs is live, state[bs] = the state after the first
+ *     R = min(max(boundary_recovery_lens[b], 0), m) tokens (S itself for
+ *     R = 0), written before the final state (so fs == bs keeps the final).
+ * Slots written must not be read as a source by another request of the same
+ * launch.  All three arrays are device [B]; align == NULL or all three NULL
+ * is kda_commit.  A final or boundary slot >= num_slots is a device error
+ * (KDA_DEVERR_SLOT_RANGE) that skips the item.
+ */
+typedef struct kda_align_args {
+    const int32_t *final_state_indices;     /* [B] or NULL (the source slot)           */
+    const int32_t *boundary_state_indices;  /* [B] or NULL (no boundary state)          */
+    const int32_t *boundary_recovery_lens;  /* [B], required with boundary slots        */
+} kda_align_args;
+
+kda_status kda_commit_align(const kda_commit_args *args, const kda_align_args *align, kda_stream_t stream);
+
 /* Enqueue the verify of one layer.  Returns before the kernel runs.
  * With the environment variable KDA_VERIFY_TCGEN05=1 at the call, K == 128
  * and Q <= 4, the products S0 [X | Y] run on tcgen05 tensor cores (tf32 with

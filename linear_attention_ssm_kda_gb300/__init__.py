@@ -71,6 +71,11 @@ class VerifyArgs(ctypes.Structure):
     ]
 
 
+class AlignArgs(ctypes.Structure):
+    """Mirror of ``kda_align_args``."""
+    _fields_ = [("final_state_indices", _p), ("boundary_state_indices", _p), ("boundary_recovery_lens", _p)]
+
+
 class FoldArgs(ctypes.Structure):
     """Mirror of ``kda_fold_args``."""
     _fields_ = [("query_start_loc", _p), ("num_accepted", _p), ("record_indices", _p)]
@@ -113,6 +118,8 @@ def load_library():
             lib.kda_verify_fold.restype = ctypes.c_int
             lib.kda_commit.argtypes = [ctypes.POINTER(CommitArgs), _p]
             lib.kda_commit.restype = ctypes.c_int
+            lib.kda_commit_align.argtypes = [ctypes.POINTER(CommitArgs), ctypes.POINTER(AlignArgs), _p]
+            lib.kda_commit_align.restype = ctypes.c_int
             lib.kda_commit_noalloc.argtypes = [ctypes.POINTER(CommitArgs), _p]
             lib.kda_commit_noalloc.restype = ctypes.c_int
             lib.kda_workspace_bytes.argtypes = []
@@ -359,9 +366,17 @@ class CommitContext:
 
     def commit(self, num_accepted_tokens: torch.Tensor, state_indices: torch.Tensor,
                query_start_loc: torch.Tensor, record_indices: torch.Tensor | None = None,
-               null_block_id: int = 0, workspace: torch.Tensor | None = None, stream=None) -> None:
+               null_block_id: int = 0, workspace: torch.Tensor | None = None, stream=None,
+               final_state_indices: torch.Tensor | None = None,
+               boundary_state_indices: torch.Tensor | None = None,
+               boundary_recovery_lens: torch.Tensor | None = None) -> None:
         """Fold each request's first min(max(accepted, 0), query_len) records
-        into every layer's state (one kernel launch, asynchronous)."""
+        into every layer's state (one kernel launch, asynchronous).
+
+        Align mode (``kda_commit_align``): the committed state goes to
+        ``final_state_indices[b]`` (default the source slot; a null one writes
+        nothing) and a live ``boundary_state_indices[b]`` receives the state
+        after the first ``boundary_recovery_lens[b]`` tokens."""
         dev = self.device
         B = state_indices.shape[0]
         _need(num_accepted_tokens, "num_accepted_tokens", torch.int32, dev, 1)
@@ -378,6 +393,21 @@ class CommitContext:
                 raise ValueError("record_indices is too short")
         if workspace is not None:
             _need(workspace, "workspace", torch.int32, dev)
+        align = None
+        if final_state_indices is not None or boundary_state_indices is not None:
+            if boundary_state_indices is not None and boundary_recovery_lens is None:
+                raise ValueError("boundary_recovery_lens is required with boundary_state_indices")
+            for name, t in (("final_state_indices", final_state_indices),
+                            ("boundary_state_indices", boundary_state_indices),
+                            ("boundary_recovery_lens", boundary_recovery_lens)):
+                if t is not None:
+                    _need(t, name, torch.int32, dev, 1)
+                    if t.shape[0] < B or not t.is_contiguous():
+                        raise ValueError(f"{name} must be contiguous with at least B entries")
+            align = AlignArgs()
+            align.final_state_indices = _ptr(final_state_indices)
+            align.boundary_state_indices = _ptr(boundary_state_indices)
+            align.boundary_recovery_lens = _ptr(boundary_recovery_lens)
         a = CommitArgs()
         a.L, a.B, a.H, a.K, a.V, a.Q = self.L, B, self.H, self.K, self.V, self.window
         a.null_block_id = null_block_id
@@ -392,7 +422,11 @@ class CommitContext:
         a.record_indices = _ptr(record_indices)
         a.num_accepted = num_accepted_tokens.data_ptr()
         a.workspace = _ptr(workspace)
-        _check(load_library().kda_commit(ctypes.byref(a), ctypes.c_void_p(_stream_handle(dev, stream))))
+        handle = ctypes.c_void_p(_stream_handle(dev, stream))
+        if align is None:
+            _check(load_library().kda_commit(ctypes.byref(a), handle))
+        else:
+            _check(load_library().kda_commit_align(ctypes.byref(a), ctypes.byref(align), handle))
 
 
 NOALLOC_MAX_LAYERS = 64  # KDA_NOALLOC_MAX_LAYERS

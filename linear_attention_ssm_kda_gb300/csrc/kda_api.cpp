@@ -169,8 +169,12 @@ kda_status kda_verify_fold(const kda_verify_args* a, const kda_fold_args* f, kda
   return KDA_OK;
 }
 
-kda_status kda_commit(const kda_commit_args* a, kda_stream_t stream) {
+kda_status kda_commit(const kda_commit_args* a, kda_stream_t stream) { return kda_commit_align(a, nullptr, stream); }
+
+kda_status kda_commit_align(const kda_commit_args* a, const kda_align_args* al, kda_stream_t stream) {
   if (a == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_commit: args is NULL");
+  if (al != nullptr && al->boundary_state_indices != nullptr && al->boundary_recovery_lens == nullptr)
+    return fail(KDA_ERR_INVALID_ARG, "kda_commit_align: boundary_recovery_lens is NULL with boundary slots");
   if (a->L <= 0) return fail(KDA_ERR_INVALID_ARG, "kda_commit: needs at least one layer (L=%d)", a->L);
   if (a->B < 0) return fail(KDA_ERR_INVALID_ARG, "kda_commit: negative B (%d)", a->B);
   kda_status st = check_dims(a->H, a->K, a->V, a->Q);
@@ -205,6 +209,11 @@ kda_status kda_commit(const kda_commit_args* a, kda_stream_t stream) {
   p.qsl = a->query_start_loc; p.state_indices = a->state_indices;
   p.record_indices = a->record_indices; p.num_accepted = a->num_accepted;
   p.workspace = a->workspace;
+  if (al != nullptr) {
+    p.final_state_indices = al->final_state_indices;
+    p.boundary_state_indices = al->boundary_state_indices;
+    p.boundary_recovery_lens = al->boundary_recovery_lens;
+  }
   cudaError_t e = kda::launch_commit(p, a->K, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_commit: launch failed: %s", cudaGetErrorString(e));
   return KDA_OK;

@@ -10,6 +10,12 @@
 // correction.  One CTA per (layer, request, head); the 64 KB state block
 // arrives by one bulk copy (TMA) issued first, the records and gates are
 // prepared while it is in flight, and the result leaves by 16-byte stores.
+//
+// Align mode (prefix caching, the kernel's ALIGN_MODE on the same page): the
+// committed state goes to final_state_indices[b] (nothing is written when
+// that slot is null), and a live boundary_state_indices[b] receives the state
+// after the first R = boundary_recovery_lens[b] of the m tokens, from the
+// same pass over the state.
 #include <cuda_runtime.h>
 
 #include "kda_device.cuh"
@@ -20,12 +26,15 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool ALIGN>
 struct CommitLayout {
   static constexpr int kState = 0;                       // float [KD][KD]
   static constexpr int kKd = kState + KD * KD * 4;       // float [QMAX][KD]  k^_t * prod_{u>t} e^g
   static constexpr int kDall = kKd + QMAX * KD * 4;      // float [KD]        prod_t e^g
-  static constexpr int kC = kDall + KD * 4;              // float [QMAX][KD]  c_t
+  // align mode: the same over the tokens before the boundary
+  static constexpr int kKdb = kDall + KD * 4;            // float [QMAX][KD]  k^_t * prod_{t<u<R} e^g
+  static constexpr int kDallb = kKdb + (ALIGN ? QMAX * KD * 4 : 0);  // float [KD] prod_{t<R} e^g
+  static constexpr int kC = kDallb + (ALIGN ? KD * 4 : 0);           // float [QMAX][KD]  c_t
   static constexpr int kNorm = kC + QMAX * KD * 4;       // float [QMAX][KD/32] per-warp parts of |k_t|^2
   static constexpr int kBar = (kNorm + QMAX * (KD / 32) * 4 + 7) / 8 * 8;
   static constexpr int kBytes = kBar + 8;
@@ -33,9 +42,9 @@ struct CommitLayout {
 
 __device__ __forceinline__ bool aligned16(long long addr) { return (addr & 15) == 0; }
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool ALIGN>
 __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams p) {
-  using Lay = CommitLayout<KD, QMAX>;
+  using Lay = CommitLayout<KD, QMAX, ALIGN>;
   extern __shared__ __align__(128) unsigned char smem[];
   float* s_state = reinterpret_cast<float*>(smem + Lay::kState);
   float* s_kd = reinterpret_cast<float*>(smem + Lay::kKd);
@@ -68,6 +77,18 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
     if (tid == 0) report(p.workspace, KDA_DEVERR_ROW_RANGE, item);
     return;
   }
+  long long fs = s, bs = p.null_block_id;  // final and boundary slots
+  int rb = 0;                              // tokens before the boundary
+  if constexpr (ALIGN) {
+    fs = p.final_state_indices ? (long long)p.final_state_indices[b] : s;
+    if (fs <= p.null_block_id) return;
+    bs = p.boundary_state_indices ? (long long)p.boundary_state_indices[b] : p.null_block_id;
+    if (fs >= p.num_slots || bs >= p.num_slots) {
+      if (tid == 0) report(p.workspace, KDA_DEVERR_SLOT_RANGE, item);
+      return;
+    }
+    rb = p.boundary_recovery_lens ? min(max(p.boundary_recovery_lens[b], 0), m) : 0;
+  }
   const long long state_base = p.state_base[l], state_stride = p.state_stride[l];
   const long long corr_base = p.corr_base[l], corr_stride = p.corr_stride[l];
   const long long kg_base = p.kg_base[l], kg_stride = p.kg_stride[l];
@@ -77,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
     return;
   }
   float* gS = reinterpret_cast<float*>(state_base) + s * state_stride + (long long)h * KD * KD;
+  float* gF = reinterpret_cast<float*>(state_base) + fs * state_stride + (long long)h * KD * KD;
+  float* gB = reinterpret_cast<float*>(state_base) + bs * state_stride + (long long)h * KD * KD;
   const float* gc = reinterpret_cast<const float*>(corr_base) + r * corr_stride + (long long)h * p.Q * KD;
   const uint16_t* gkg = reinterpret_cast<const uint16_t*>(kg_base) + r * kg_stride + (long long)h * p.Q * 2 * KD;
 
@@ -108,18 +131,27 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
   }
   __syncthreads();
   if (tid < KD) {
-    float suffix = 1.0f;  // prod_{u>t} e^{g_u}
+    float suffix = 1.0f;   // prod_{u>t} e^{g_u}
+    float suffixb = 1.0f;  // align mode: prod_{t<u<R} e^{g_u}
 #pragma unroll
     for (int t = QMAX - 1; t >= 0; --t) {
       if (t < m) {
         float kk = 0.0f;
 #pragma unroll
         for (int w = 0; w < KD / 32; ++w) kk += s_norm[t * (KD / 32) + w];
-        s_kd[t * KD + tid] = kv[t] * rsqrtf(kk + 1e-6f) * suffix;
+        const float kn = kv[t] * rsqrtf(kk + 1e-6f);
+        s_kd[t * KD + tid] = kn * suffix;
         suffix *= eg[t];
+        if constexpr (ALIGN) {
+          if (t < rb) {
+            reinterpret_cast<float*>(smem + Lay::kKdb)[t * KD + tid] = kn * suffixb;
+            suffixb *= eg[t];
+          }
+        }
       }
     }
     s_dall[tid] = suffix;
+    if constexpr (ALIGN) reinterpret_cast<float*>(smem + Lay::kDallb)[tid] = suffixb;
   }
   __syncthreads();
 
@@ -136,8 +168,36 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
   const float4* st4 = reinterpret_cast<const float4*>(s_state);
   const float4* dall4 = reinterpret_cast<const float4*>(s_dall);
   const float4* kd4 = reinterpret_cast<const float4*>(s_kd);
-  float4* out4 = reinterpret_cast<float4*>(gS);
+  float4* out4 = reinterpret_cast<float4*>(gF);
   constexpr int kChunksPerRow = KD / 4;
+  if constexpr (ALIGN) {
+    if (bs > p.null_block_id) {  // written first: a final slot equal to it wins
+      const float4* dallb4 = reinterpret_cast<const float4*>(smem + Lay::kDallb);
+      const float4* kdb4 = reinterpret_cast<const float4*>(smem + Lay::kKdb);
+      float4* bnd4 = reinterpret_cast<float4*>(gB);
+#pragma unroll 4
+      for (int idx = tid; idx < KD * KD / 4; idx += kThreads) {
+        const int row = idx / kChunksPerRow;
+        const int kc = idx - row * kChunksPerRow;
+        const float4 sv = st4[idx];
+        const float4 d = dallb4[kc];
+        float4 o = make_float4(sv.x * d.x, sv.y * d.y, sv.z * d.z, sv.w * d.w);
+#pragma unroll
+        for (int t = 0; t < QMAX; ++t) {
+          if (t < rb) {
+            const float c = s_c[t * KD + row];
+            const float4 k = kdb4[t * kChunksPerRow + kc];
+            o.x = fmaf(c, k.x, o.x);
+            o.y = fmaf(c, k.y, o.y);
+            o.z = fmaf(c, k.z, o.z);
+            o.w = fmaf(c, k.w, o.w);
+          }
+        }
+        bnd4[idx] = o;
+      }
+      if (bs == fs) __syncthreads();  // the final state overwrites it in order
+    }
+  }
 #pragma unroll 4
   for (int idx = tid; idx < KD * KD / 4; idx += kThreads) {
     const int row = idx / kChunksPerRow;
@@ -160,20 +220,27 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
   }
 }
 
-template <int KD, int QMAX>
+template <int KD, int QMAX, bool ALIGN>
 cudaError_t launch(const CommitParams& p, cudaStream_t stream) {
-  constexpr int bytes = CommitLayout<KD, QMAX>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(commit_kernel<KD, QMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  constexpr int bytes = CommitLayout<KD, QMAX, ALIGN>::kBytes;
+  cudaError_t e =
+      cudaFuncSetAttribute(commit_kernel<KD, QMAX, ALIGN>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  commit_kernel<KD, QMAX><<<p.L * p.B * p.H, kThreads, bytes, stream>>>(p);
+  commit_kernel<KD, QMAX, ALIGN><<<p.L * p.B * p.H, kThreads, bytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <bool ALIGN>
+cudaError_t launch_k(const CommitParams& p, int K, cudaStream_t stream) {
+  if (K == 128) return p.Q <= 4 ? launch<128, 4, ALIGN>(p, stream) : launch<128, 8, ALIGN>(p, stream);
+  return p.Q <= 4 ? launch<64, 4, ALIGN>(p, stream) : launch<64, 8, ALIGN>(p, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_commit(const CommitParams& p, int K, cudaStream_t stream) {
-  if (K == 128) return p.Q <= 4 ? launch<128, 4>(p, stream) : launch<128, 8>(p, stream);
-  return p.Q <= 4 ? launch<64, 4>(p, stream) : launch<64, 8>(p, stream);
+  const bool align = p.final_state_indices != nullptr || p.boundary_state_indices != nullptr;
+  return align ? launch_k<true>(p, K, stream) : launch_k<false>(p, K, stream);
 }
 
 }  // namespace kda

@@ -51,6 +51,9 @@ struct CommitParams {
   int lower_bound_gate; float lower_bound;
   const int* qsl; const int* state_indices; const int* record_indices; const int* num_accepted;
   int* workspace;
+  // align mode (kda_commit_align), each [B] or nullptr: the final slot (the
+  // source slot when null), the boundary slot and its recovery length
+  const int* final_state_indices; const int* boundary_state_indices; const int* boundary_recovery_lens;
 };
 
 }  // namespace kda

@@ -250,10 +250,11 @@ typedef struct kda_align_args {
 kda_status kda_commit_align(const kda_commit_args *args, const kda_align_args *align, kda_stream_t stream);
 
 /* Enqueue the verify of one layer.  Returns before the kernel runs.
- * With the environment variable KDA_VERIFY_TCGEN05=1 at the call, K == 128
- * and Q <= 4, the products S0 [X | Y] run on tcgen05 tensor cores (tf32 with
- * a hi/lo split of the state, same tolerances); the default is the CUDA-core
- * kernel, which is faster on GB300. */
+ * At K == 128 the products S0 [X | Y] run on tcgen05 tensor cores (tf32 with
+ * a hi/lo split of the state, same tolerances) for windows Q > 4 and on the
+ * CUDA cores for Q <= 4, the faster of the two on GB300 for each; the
+ * environment variable KDA_VERIFY_TCGEN05=1 (or =0) at the call forces the
+ * tensor cores (or the CUDA cores). */
 kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
 
 /* Enqueue the commit of all layers (one kernel launch). */

@@ -100,7 +100,7 @@ struct Layout {
   // Tensor-core instantiation (K = 128, windows up to 4 tokens): the state
   // streams as K-slices of 32 (128 rows x 128 bytes, 128-byte swizzle) and the
   // products S0 [X | Y] come from tcgen05 MMAs; otherwise CUDA-core gemv warps.
-  static_assert(VAR != kVarTcgen05 || (KD == 128 && QMAX == 4), "the tensor-core path covers K = 128, windows up to 4");
+  static_assert(VAR != kVarTcgen05 || (KD == 128 && (QMAX == 4 || QMAX == 8)), "the tensor-core path covers K = 128");
   static_assert(VAR != kVarFold || QMAX <= 4, "the fold variant covers windows up to 4");
   static constexpr bool kTC = VAR == kVarTcgen05;
   static constexpr bool kFold = VAR == kVarFold;
@@ -124,7 +124,11 @@ struct Layout {
   // operand slot (prep -> gemv).  Tensor-core path: first the MMA's B operand,
   // [X | Y]_hi rows 0..7 and [X | Y]_lo rows 8..15, as four K-slices of
   // [16][32] fp32 with the 128-byte swizzle (8 KB), then the rest.
-  static constexpr int kOpMeta = kTC ? 4 * 2048 : 0;
+  static constexpr int kMmaN = 4 * QMAX;          // MMA N: the 2 QMAX vectors' hi rows, then their lo rows
+  static constexpr int kBSlice = kMmaN * 128;     // bytes of the B operand per K-slice of 32
+  static constexpr int kDCols = kMmaN;            // tensor-memory columns per D buffer (two buffers)
+  static constexpr int kTmemCols = 2 * kDCols < 32 ? 32 : 2 * kDCols;
+  static constexpr int kOpMeta = kTC ? 4 * kBSlice : 0;
   static constexpr int kOpVec = ru(kOpMeta + int(sizeof(OpMeta<QMAX>)), 16);  // [2 QMAX][KD] X_t | Y_t
   static constexpr int kOpV = kTC ? kOpVec : kOpVec + 2 * QMAX * KD * 4;        // [QMAX][KD] v_t
   static constexpr int kOpMN = kOpV + QMAX * KD * 4;                            // [QMAX][QMAX] M | N
@@ -136,7 +140,7 @@ struct Layout {
   static constexpr int kOp = ru(kOpFc + (kFold ? QMAX * KD * 4 : 0), kTC ? 1024 : 128);
   // prep runs up to two items ahead of the gemv team; on the tensor-core path
   // an item's slot is also held until its readout, one item later
-  static constexpr int kNumOp = kTC ? 4 : QMAX <= 4 ? 3 : 2;
+  static constexpr int kNumOp = kTC ? (QMAX <= 4 ? 4 : 3) : QMAX <= 4 ? 3 : 2;
   // per-item scratch of the prep team
   static constexpr int kXs = 2 * QMAX * KD * 4;                        // [2][QMAX][KD] q | k conv outputs
   // per-warp scratch
@@ -847,13 +851,13 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       if constexpr (Lay::kTC) {
         // the MMA's B operand: vector c (X_0..X_{n-1}, Y_0..Y_{n-1}, then
         // zeros) split as hi = the value with its low 13 mantissa bits cleared
-        // (exact in tf32) in row c and lo = value - hi in row 8 + c
-        unsigned char* bt = op + (pt >> 5) * 2048;
+        // (exact in tf32) in row c and lo = value - hi in row 2 QMAX + c
+        unsigned char* bt = op + (pt >> 5) * Lay::kBSlice;
         const int kk = pt & 31;
         auto put = [&](int c, float v) {
           const float hi = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
           *reinterpret_cast<float*>(bt + sw128_offset(c, kk)) = hi;
-          *reinterpret_cast<float*>(bt + sw128_offset(8 + c, kk)) = v - hi;
+          *reinterpret_cast<float*>(bt + sw128_offset(2 * QMAX + c, kk)) = v - hi;
         };
         float D = 1.0f;
 #pragma unroll
@@ -1210,16 +1214,16 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
   }
 }
 
-// ---------------------------------------------------------------- tensor-core path (K = 128, Q <= 4)
+// ---------------------------------------------------------------- tensor-core path (K = 128, Q = 4 or 8)
 //
 // The products P | R = S0 [X_0..X_{n-1} | Y_0..Y_{n-1}] of an item come from
-// tcgen05 MMAs: D[128 x 16] in tensor memory = S0 [128 x 128] times B^T, B =
-// [hi rows 0..7 | lo rows 8..15] of the 2n <= 8 operand vectors.  fp32
+// tcgen05 MMAs: D[128 x 4Q] in tensor memory = S0 [128 x 128] times B^T, B =
+// [hi rows 0..2Q-1 | lo rows 2Q..4Q-1] of the 2n <= 2Q operand vectors.  fp32
 // accuracy from tf32 inputs: S0 = S_hi + S_lo with S_hi the value with its
 // low 13 mantissa bits cleared (exact in tf32) and S_lo = S0 - S_hi (exact in
 // fp32, at most 11 significant bits, rounded to tf32 within 2^-21 of S0);
 // likewise for B.  Two MMAs per K step, S_hi B^T + S_lo B^T, accumulate
-// column c < 8 = S0 v_c,hi and column 8 + c = S0 v_c,lo, whose sum is S0 v_c.
+// column c < 2Q = S0 v_c,hi and column 2Q + c = S0 v_c,lo, whose sum is S0 v_c.
 
 // State producer: each live item's state as four K-slices (TMA tiles of 128
 // rows x 32 fp32 with the 128-byte swizzle) into the ring of slice slots.
@@ -1281,14 +1285,14 @@ template <int KD, int QMAX, int VAR>
 __device__ __forceinline__ bool tc_issue_lo(unsigned char* smem, uint32_t taddr, LoPending& lp,
                                             const volatile int* abort_flag) {
   using Lay = Layout<KD, QMAX, VAR>;
-  constexpr uint32_t kIdesc = umma_idesc_tf32(128, 16);
+  constexpr uint32_t kIdesc = umma_idesc_tf32(128, Layout<KD, QMAX, VAR>::kMmaN);
   Bars<KD, QMAX, VAR> bars(smem);
   if (!lp.valid) return true;
   lp.valid = false;
   if (!mbar_wait_or_abort(&bars.lo_full[lp.pos], (lp.g / Lay::kNumChunk) & 1, abort_flag)) return false;
   tmem_fence_after();
   const uint64_t a = umma_desc_sw128(smem + Lay::oChunks + lp.pos * Lay::kChunk);
-  const uint32_t d = taddr + lp.db * 16;
+  const uint32_t d = taddr + lp.db * Lay::kDCols;
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks) umma_tf32(d, a + 2 * ks, lp.bk + 2 * ks, kIdesc, true);
   umma_commit(&bars.ch_empty[lp.pos]);
@@ -1302,7 +1306,7 @@ __device__ __forceinline__ bool tc_issue_lo(unsigned char* smem, uint32_t taddr,
 template <int KD, int QMAX, int VAR>
 __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int* misc) {
   using Lay = Layout<KD, QMAX, VAR>;
-  constexpr uint32_t kIdesc = umma_idesc_tf32(128, 16);
+  constexpr uint32_t kIdesc = umma_idesc_tf32(128, Layout<KD, QMAX, VAR>::kMmaN);
   Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   const int nloc = local_items(p.B * p.H);
@@ -1325,14 +1329,14 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
     const uint32_t db = live & 1;
     ok = mbar_wait_or_abort(&bars.d_empty[db], ((live >> 1) & 1) ^ 1, abort_flag);
     const uint64_t b = umma_desc_sw128(op);
-    const uint32_t d = taddr + db * 16;
+    const uint32_t d = taddr + db * Lay::kDCols;
     for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
       const int pos = static_cast<int>(g % Lay::kNumChunk);
       ok = mbar_wait_or_abort(&bars.ch_full[pos], (g / Lay::kNumChunk) & 1, abort_flag);
       if (!ok) break;
       tmem_fence_after();
       const uint64_t a = umma_desc_sw128(smem + Lay::oChunks + pos * Lay::kChunk);
-      const uint64_t bk = b + static_cast<uint64_t>(kb) * (2048 >> 4);  // B slice kb: 2 KB further
+      const uint64_t bk = b + static_cast<uint64_t>(kb) * (Lay::kBSlice >> 4);  // B slice kb
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) umma_tf32(d, a + 2 * ks, bk + 2 * ks, kIdesc, kb > 0 || ks > 0);
       umma_commit(&bars.hi_done[pos]);
@@ -1353,7 +1357,7 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
 // lo columns into P_t | R_t and runs the row's solve.
 template <int KD, int QMAX, int N, int VAR>
 __device__ __forceinline__ void tc_solve(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op, int h,
-                                         int row, const float (&d)[16]) {
+                                         int row, const float* d) {
   using Lay = Layout<KD, QMAX, VAR>;
   const float* mn = reinterpret_cast<const float*>(op + Lay::kOpMN);
   const float* xv = reinterpret_cast<const float*>(op + Lay::kOpV);
@@ -1362,12 +1366,12 @@ __device__ __forceinline__ void tc_solve(const VerifyParams& p, const OpMeta<QMA
   float cv[N];
 #pragma unroll
   for (int t = 0; t < N; ++t) {
-    float x = xv[t * KD + row] - (d[t] + d[8 + t]);
+    float x = xv[t * KD + row] - (d[t] + d[2 * QMAX + t]);
 #pragma unroll
     for (int u = 0; u < t; ++u) x = fmaf(-mn[t * QMAX + u], cv[u], x);
     const float c = x * m.beta[t];
     cv[t] = c;
-    float o = d[N + t] + d[8 + N + t];
+    float o = d[N + t] + d[2 * QMAX + N + t];
 #pragma unroll
     for (int u = 0; u <= t; ++u) o = fmaf(mn[u * QMAX + t], cv[u], o);
     corr[t * KD] = c;
@@ -1390,18 +1394,33 @@ __device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char*
   const uint32_t db = live & 1;
   if (!warp_wait(&bars.d_full[db], (live >> 1) & 1, lane, abort_flag)) return false;
   tmem_fence_after();
-  float d[16];
-  tmem_ld16(taddr + db * 16 + (static_cast<uint32_t>(wq * 32) << 16), d);
+  float d[Lay::kDCols];
+  const uint32_t ta = taddr + db * Lay::kDCols + (static_cast<uint32_t>(wq * 32) << 16);
+#pragma unroll
+  for (int c = 0; c < Lay::kDCols; c += 16) tmem_ld16(ta + c, *reinterpret_cast<float(*)[16]>(d + c));
   tmem_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&bars.d_empty[db]);
   const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta);
   const int row = wq * 32 + lane;
-  switch (m.n) {
-    case 1: tc_solve<KD, QMAX, 1, VAR>(p, m, op, h, row, d); break;
-    case 2: tc_solve<KD, QMAX, 2, VAR>(p, m, op, h, row, d); break;
-    case 3: tc_solve<KD, QMAX, 3, VAR>(p, m, op, h, row, d); break;
-    default: tc_solve<KD, QMAX, 4, VAR>(p, m, op, h, row, d); break;
+  if constexpr (QMAX <= 4) {
+    switch (m.n) {
+      case 1: tc_solve<KD, QMAX, 1, VAR>(p, m, op, h, row, d); break;
+      case 2: tc_solve<KD, QMAX, 2, VAR>(p, m, op, h, row, d); break;
+      case 3: tc_solve<KD, QMAX, 3, VAR>(p, m, op, h, row, d); break;
+      default: tc_solve<KD, QMAX, 4, VAR>(p, m, op, h, row, d); break;
+    }
+  } else {
+    switch (m.n) {
+      case 1: tc_solve<KD, QMAX, 1, VAR>(p, m, op, h, row, d); break;
+      case 2: tc_solve<KD, QMAX, 2, VAR>(p, m, op, h, row, d); break;
+      case 3: tc_solve<KD, QMAX, 3, VAR>(p, m, op, h, row, d); break;
+      case 4: tc_solve<KD, QMAX, 4, VAR>(p, m, op, h, row, d); break;
+      case 5: tc_solve<KD, QMAX, 5, VAR>(p, m, op, h, row, d); break;
+      case 6: tc_solve<KD, QMAX, 6, VAR>(p, m, op, h, row, d); break;
+      case 7: tc_solve<KD, QMAX, 7, VAR>(p, m, op, h, row, d); break;
+      default: tc_solve<KD, QMAX, 8, VAR>(p, m, op, h, row, d); break;
+    }
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(&bars.op_empty[oslot]);
@@ -1516,9 +1535,9 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
       if (tid == 0) report(p.workspace, KDA_DEVERR_MISALIGNED, blockIdx.x);
       return;
     }
-    // tensor memory for two D buffers of 16 fp32 columns, owned by the MMA warp
+    // tensor memory for two D buffers of 4 QMAX fp32 columns, owned by the MMA warp
     if (warp == kMmaWarp)
-      tmem_alloc(reinterpret_cast<uint32_t*>(const_cast<int*>(misc) + kMiscTaddr), 32);
+      tmem_alloc(reinterpret_cast<uint32_t*>(const_cast<int*>(misc) + kMiscTaddr), Lay::kTmemCols);
     tmem_fence_before();
   }
   __syncthreads();
@@ -1547,7 +1566,7 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
     __syncthreads();
     if (warp == kMmaWarp) {
       tmem_fence_after();
-      tmem_dealloc(static_cast<uint32_t>(misc[kMiscTaddr]), 32);
+      tmem_dealloc(static_cast<uint32_t>(misc[kMiscTaddr]), Lay::kTmemCols);
     }
   }
 }
@@ -1662,14 +1681,17 @@ void build_tensor_maps(VerifyParams& p, int KD) {
   p.act_mode = mode;
 }
 
-// The tensor-core verify (K = 128, windows up to 4) is opt-in: set
-// KDA_VERIFY_TCGEN05=1.  It matches the CUDA-core gemv within the same
-// tolerances but runs slower on GB300: an M = 128 tf32 MMA costs about the
-// same whatever N is, so the 2n <= 8 operand vectors use a few percent of the
-// tensor core, and fp32 accuracy takes a second (low-part) pass.
-bool tcgen05_requested() {
+// Which verify runs the products at K = 128.  An M = 128 tf32 MMA costs about
+// the same whatever N is, and fp32 accuracy takes a second (low-part) pass,
+// so the tensor cores win only when the window brings many operand vectors:
+// measured on GB300, the tcgen05 verify is faster for windows of 8 (C3) and
+// slower for windows of 4 (C2), so that is the default split.
+// KDA_VERIFY_TCGEN05=1 forces the tensor cores, =0 the CUDA-core gemv.
+bool use_tcgen05(bool window_up_to_4) {
   const char* v = std::getenv("KDA_VERIFY_TCGEN05");
-  return v != nullptr && v[0] == '1' && v[1] == '\0';
+  if (v != nullptr && v[0] == '1' && v[1] == '\0') return true;
+  if (v != nullptr && v[0] == '0' && v[1] == '\0') return false;
+  return !window_up_to_4;
 }
 
 int sm_count() {
@@ -1707,8 +1729,10 @@ cudaError_t launch_verify(const VerifyParams& params, int K, cudaStream_t stream
     if (K == 128) return p.conv_dim_first ? launch<128, 4, true, kVarFold>(p, stream) : launch<128, 4, false, kVarFold>(p, stream);
     return p.conv_dim_first ? launch<64, 4, true, kVarFold>(p, stream) : launch<64, 4, false, kVarFold>(p, stream);
   }
-  if (K == 128 && q4 && tcgen05_requested() && build_state_map(p, K))
-    return p.conv_dim_first ? launch<128, 4, true, kVarTcgen05>(p, stream) : launch<128, 4, false, kVarTcgen05>(p, stream);
+  if (K == 128 && use_tcgen05(q4) && build_state_map(p, K)) {
+    if (q4) return p.conv_dim_first ? launch<128, 4, true, kVarTcgen05>(p, stream) : launch<128, 4, false, kVarTcgen05>(p, stream);
+    return p.conv_dim_first ? launch<128, 8, true, kVarTcgen05>(p, stream) : launch<128, 8, false, kVarTcgen05>(p, stream);
+  }
   if (p.conv_dim_first) {
     if (K == 128) return q4 ? launch<128, 4, true, kVarPlain>(p, stream) : launch<128, 8, true, kVarPlain>(p, stream);
     return q4 ? launch<64, 4, true, kVarPlain>(p, stream) : launch<64, 8, true, kVarPlain>(p, stream);

@@ -1,6 +1,7 @@
-"""The opt-in tensor-core verify (KDA_VERIFY_TCGEN05=1: K = 128, windows up to
-4 tokens, P | R from tcgen05 tf32 MMAs with a hi/lo split of the state) against
-the oracle, under the same comparison rules as the CUDA-core path."""
+"""The tensor-core verify (K = 128; the default for windows of 8, forced here
+for every window with KDA_VERIFY_TCGEN05=1: P | R from tcgen05 tf32 MMAs with
+a hi/lo split of the state) against the oracle, under the same comparison
+rules as the CUDA-core path."""
 from __future__ import annotations
 
 import numpy as np
@@ -32,6 +33,19 @@ def test_c1_full_size_with_null_slots():
 
 def test_c2_verify_then_commit_reduced():
     prob = make_problem(CONFIGS["C2"], DEV, B=40, L=3, slots=64)
+    run_and_check(prob)
+
+
+def test_c3_window_of_eight_reduced():
+    """Q = 8: the MMA's N is 32 (16 vectors' hi and lo rows)."""
+    prob = make_problem(CONFIGS["C3"], DEV, B=48, slots=128)
+    run_and_check(prob)
+
+
+def test_c3_cuda_core_path_when_forced_off(monkeypatch):
+    """KDA_VERIFY_TCGEN05=0 keeps the CUDA-core gemv for windows of 8."""
+    monkeypatch.setenv("KDA_VERIFY_TCGEN05", "0")
+    prob = make_problem(CONFIGS["C3"], DEV, B=48, slots=128)
     run_and_check(prob)
 
 

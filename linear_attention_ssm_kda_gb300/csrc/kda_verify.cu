@@ -65,7 +65,8 @@ constexpr int kMmaWarp = 2 + kPrepWarps + kSplitWarps;  // warp 12 issues the MM
 
 constexpr int ru(int x, int a) { return (x + a - 1) / a * a; }
 
-// Kernel variants: the CUDA-core verify, the tcgen05 verify (opt-in), and the
+// Kernel variants: the CUDA-core verify, the tcgen05 verify (K = 128: the
+// default for windows of 8, forced by KDA_VERIFY_TCGEN05), and the
 // CUDA-core verify that first folds each request's pending records of the
 // previous step into its checkpoint.
 enum : int { kVarPlain = 0, kVarTcgen05 = 1, kVarFold = 2 };
@@ -97,7 +98,7 @@ struct OpMeta {
 template <int KD, int QMAX, int VAR>
 struct Layout {
   static_assert(7 * QMAX + 10 <= 96, "small-input copies per item exceed three per lane");
-  // Tensor-core instantiation (K = 128, windows up to 4 tokens): the state
+  // Tensor-core instantiation (K = 128, windows of 4 or 8 tokens): the state
   // streams as K-slices of 32 (128 rows x 128 bytes, 128-byte swizzle) and the
   // products S0 [X | Y] come from tcgen05 MMAs; otherwise CUDA-core gemv warps.
   static_assert(VAR != kVarTcgen05 || (KD == 128 && (QMAX == 4 || QMAX == 8)), "the tensor-core path covers K = 128");

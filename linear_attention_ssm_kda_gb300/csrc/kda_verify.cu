@@ -956,7 +956,9 @@ __device__ __forceinline__ void gemv_chunk(const float* __restrict__ st, const f
   float2 acc2[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) acc2[i] = make_float2(0.0f, 0.0f);
-#pragma unroll
+  // not unrolled: one step already holds NV independent FMA chains, and the
+  // kernel's hot code competes for the instruction cache with four roles
+#pragma unroll 1
   for (int j = 0; j < J; ++j) {
     const int kk = 4 * (4 * (j ^ flip) + kq);
     float4 vv[NCG];

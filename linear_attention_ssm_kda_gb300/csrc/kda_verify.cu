@@ -13,29 +13,35 @@
 //   c_t = beta_t (v_t - P_t - sum_{u<t} M_tu c_u),   o_t = R_t + sum_{u<=t} N_tu c_u,
 // which is the recurrence S <- S diag(e^g), c = beta (v - S k^), S <- S + c k^T,
 // o = S q^ expanded: the checkpoint S0 is read once (2n FMAs per element) and
-// never written.
+// never written (except by the fold variant, which writes the folded state).
 //
 // Schedule.  One persistent CTA per SM walks the (request, head) items
 // blockIdx.x + i * gridDim.x (local index i) with four roles that meet only
-// at mbarrier rings in shared memory, so the three stages of consecutive
-// items overlap:
+// at mbarrier rings in shared memory, so the stages of consecutive items
+// overlap:
 //   inputs (1 warp)  reads request metadata 32 items per round trip and
-//                    bulk-copies (TMA) each item's small inputs into a ring:
-//                    the 16-byte hulls of its activation and gate row
-//                    segments (rows may start anywhere), its conv taps, conv
-//                    weights and dt_bias;
+//                    copies each item's small inputs into a ring: TMA tiles
+//                    of its q | k | v (| gate) rows, conv taps and conv
+//                    weights when they are 16-byte aligned, otherwise bulk
+//                    copies of the 16-byte hulls of each row segment (rows
+//                    may start anywhere); dt_bias by a bulk copy;
 //   state (1 warp)   streams each live item's 64 KB fp32 state as eight row
 //                    chunks into a ring of chunk slots, running ahead of the
 //                    arithmetic by two to three items;
-//   prep (4 warps)   one key channel per thread: conv + SiLU of its q, k and
-//                    v channels over the window (the bf16 codes, the key
-//                    record, the rolled conv taps, which leave by bulk
-//                    stores), the gates and gate record, the norms and the
+//   prep (6 warps)   conv + SiLU of two channels per thread over the window
+//                    (the bf16 codes, the key record, the rolled conv taps
+//                    stored straight to the slot), then one key channel per
+//                    thread: the gates and gate record, the norms and the
 //                    closed-form operands X_t, Y_t, M, N, handed on through a
 //                    ring of operand slots;
 //   gemv (8 warps)   each on its own row chunk of the state: P | R with
 //                    packed fp32x2 FMAs, then the corrections and outputs of
 //                    its rows.
+// Two more variants share the roles: the tcgen05 variant (K = 128) replaces
+// the gemv warps by four split warps and one MMA thread (products on the
+// tensor cores, tensor-core path below), and the fold variant first folds
+// each item's pending records of the previous step into its state chunk and
+// stores the folded checkpoint back (fold_chunk).
 // Every wait is bounded; a timeout sets KDA_DEVERR_TIMEOUT and an abort flag
 // that stops the other roles.
 #include <cuda.h>

@@ -83,8 +83,9 @@ def pinned_meta(meta: Metadata) -> dict:
 class HostPipeline:
     """Decode steps (verify of every layer, then the commit) fed from pinned
     host memory, with the copies of one layer overlapping the kernels of its
-    neighbours.  Layer l's activations go up on one copy stream while earlier
-    layers run; its outputs come back on another while later layers run.
+    neighbours.  Layer l's activations go up on one copy stream while the
+    previous step's later layers run; its outputs come back on another while
+    later layers run.
     Events order every reuse of a device buffer: a layer's activations are
     overwritten only after the previous step's verify of that layer, its
     outputs only after they were read back, and the request metadata
@@ -122,10 +123,13 @@ class HostPipeline:
                 up.wait_event(self.verified[l])  # the previous step's verify has read these activations
                 prob.fused[l].copy_(host_fused[l], non_blocking=True)
                 self.in_ready[l].record(up)
+        # events of one stream complete in order: the last layer's upload of this
+        # step and the last layer's read-back of the previous step cover every
+        # layer, and both are done by the time the previous step's commit ends
         stream.wait_event(self.meta_ready)
+        stream.wait_event(self.in_ready[L - 1])
+        stream.wait_event(self.read_back[L - 1])
         for l in range(L):
-            stream.wait_event(self.in_ready[l])
-            stream.wait_event(self.read_back[l])  # the previous step's outputs of this layer are home
             verify_layer(prob, l, d, stream=stream)
             self.verified[l].record(stream)
         commit_all(self.ctx, d, stream=stream)

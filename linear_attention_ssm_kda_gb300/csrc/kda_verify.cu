@@ -135,6 +135,7 @@ struct Layout {
   static constexpr int kBSlice = kMmaN * 128;     // bytes of the B operand per K-slice of 32
   static constexpr int kDCols = kMmaN;            // tensor-memory columns per D buffer (two buffers)
   static constexpr int kTmemCols = 2 * kDCols < 32 ? 32 : 2 * kDCols;
+  static_assert(kTmemCols >= 2 * kDCols && kTmemCols <= 512, "two D buffers fit the tensor-memory allocation");
   static constexpr int kOpMeta = kTC ? 4 * kBSlice : 0;
   static constexpr int kOpVec = ru(kOpMeta + int(sizeof(OpMeta<QMAX>)), 16);  // [2 QMAX][KD] X_t | Y_t
   static constexpr int kOpV = kTC ? kOpVec : kOpVec + 2 * QMAX * KD * 4;        // [QMAX][KD] v_t

@@ -210,7 +210,9 @@ typedef struct kda_commit_args {
  * row.  A request with n = 0 and m > 0 is folded only.  The result equals
  * kda_commit with the fold arguments followed by kda_verify, up to fp32
  * rounding.  The fold pointers are device arrays ([B+1], [B], [B] or NULL);
- * fold == NULL or fold->query_start_loc == NULL runs the plain verify.
+ * fold == NULL or fold->query_start_loc == NULL runs the plain verify.  With
+ * T == 0 (every window empty) only the folds run, and the activation
+ * pointers may be NULL.
  * Supported: Q <= 4 (KDA_ERR_UNSUPPORTED otherwise); the other arguments and
  * errors are those of kda_verify; a pending record row out of range is a
  * device error (KDA_DEVERR_ROW_RANGE) that skips the item.

@@ -77,11 +77,15 @@ kda_status verify_params(const kda_verify_args* a, bool fold, kda::VerifyParams&
     *noop = true;
     return KDA_OK;
   }
-  const void* required[] = {a->mixed_qkv, a->raw_gate,  a->raw_beta, a->out,   a->A_log,
-                            a->dt_bias,   a->conv_weight, a->conv_state, a->state, a->corr,
-                            a->key_gate,  a->query_start_loc, a->state_indices};
+  const void* required[] = {a->A_log,    a->dt_bias, a->conv_weight,     a->conv_state,   a->state,
+                            a->corr,     a->key_gate, a->query_start_loc, a->state_indices};
   for (const void* ptr : required)
     if (ptr == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify: a required pointer is NULL");
+  // the activations are read only for token rows: a fold-only step (T == 0)
+  // may pass NULL for them
+  const void* activations[] = {a->mixed_qkv, a->raw_gate, a->raw_beta, a->out};
+  for (const void* ptr : activations)
+    if (ptr == nullptr && a->T > 0) return fail(KDA_ERR_INVALID_ARG, "kda_verify: an activation pointer is NULL");
   if (a->gate_mode != KDA_GATE_SOFTPLUS && a->gate_mode != KDA_GATE_LOWER_BOUND)
     return fail(KDA_ERR_INVALID_ARG, "kda_verify: gate_mode %d", a->gate_mode);
   if (a->gate_mode == KDA_GATE_LOWER_BOUND && !std::isfinite(a->lower_bound))

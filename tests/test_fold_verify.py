@@ -105,6 +105,32 @@ def test_fold_chain_matches_commit_then_verify(name):
     assert folded_only > 0
 
 
+def test_fold_only_step_with_no_token_rows():
+    """Every window of the step empty (T = 0): the pending records are folded
+    and nothing else is written."""
+    prob = make_problem(CONFIGS["C0"], DEV)
+    cfg = prob.cfg
+    meta0 = prob.meta
+    meta0.num_accepted = np.minimum(np.diff(meta0.query_start_loc), cfg.Q).astype(np.int32)  # all accepted
+    dm0 = device_meta(meta0, DEV)
+    verify_layer(prob, 0, dm0)
+    hl = host_layer(prob, 0)
+    gpu_before = prob.state.cpu().numpy()
+    conv_before = prob.conv_state.clone()
+    B = cfg.B
+    empty = Metadata(np.zeros(B + 1, np.int32), meta0.state_indices.copy(), meta0.record_indices,
+                     meta0.num_accepted.copy(), np.zeros(B, np.int32))
+    prob.meta = empty
+    prob.fused = torch.empty((cfg.L, 0, prob.fused.shape[2]), dtype=torch.bfloat16, device=DEV)
+    prob.out = torch.empty((cfg.L, 0, cfg.H * cfg.K), dtype=torch.bfloat16, device=DEV)
+    ws = kda.new_workspace(DEV)
+    verify_layer(prob, 0, device_meta(empty, DEV), workspace=ws, fold=dm0)
+    assert kda.read_device_error(ws) == 0
+    exact = run_commit(prob, hl, meta=meta0, want_exact=True)
+    assert check_commit_layer(prob, 0, hl, exact, meta0, before=gpu_before[0]) is not None
+    assert torch.equal(prob.conv_state.view(torch.int16), conv_before.view(torch.int16))
+
+
 def test_fold_rejects_long_windows():
     prob = make_problem(CONFIGS["C3"], DEV, B=8, slots=32)
     dm = device_meta(prob.meta, DEV)

@@ -105,11 +105,8 @@ def _load():
             lib.kda_oracle_bf16_round.restype = ctypes.c_uint16
             lib.kda_oracle_gate.argtypes = [ctypes.c_double] * 3 + [ctypes.c_int, ctypes.c_double]
             lib.kda_oracle_gate.restype = ctypes.c_double
-            for fn in (lib.kda_oracle_exp_neg_f32, lib.kda_oracle_silu_f32):
-                fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
-                fn.restype = None
-            lib.kda_oracle_conv_silu_bf16_f32.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_int]
-            lib.kda_oracle_conv_silu_bf16_f32.restype = None
+            lib.kda_oracle_conv_silu_bf16.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_int]
+            lib.kda_oracle_conv_silu_bf16.restype = None
             _lib = lib
     return _lib
 
@@ -139,30 +136,15 @@ def gate(raw_g: float, dt_bias: float, A: float, lower_bound: float | None = Non
     return float(_load().kda_oracle_gate(raw_g, dt_bias, A, int(use_lb), float(lower_bound or 0.0)))
 
 
-def exp_neg_f32(x) -> np.ndarray:
-    """The specified fp32 e^x (x <= 0) of the convolution's SiLU, elementwise."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    y = np.empty_like(x)
-    _load().kda_oracle_exp_neg_f32(x.ctypes.data, y.ctypes.data, x.size)
-    return y
-
-
-def silu_f32(x) -> np.ndarray:
-    """The specified fp32 SiLU y sigma(y), elementwise."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    y = np.empty_like(x)
-    _load().kda_oracle_silu_f32(x.ctypes.data, y.ctypes.data, x.size)
-    return y
-
-
-def conv_silu_bf16_f32(w, x) -> np.ndarray:
-    """bf16 codes of the specified fp32 conv + SiLU; w, x: [n, W] taps oldest first."""
-    w = np.ascontiguousarray(w, dtype=np.float32)
-    x = np.ascontiguousarray(x, dtype=np.float32)
+def conv_silu_bf16(w, x) -> np.ndarray:
+    """bf16 codes of SiLU(sum_j w_j x_j) by the plain definition in double,
+    rounded once; w, x: [n, W] taps oldest first (values, any float dtype)."""
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    x = np.ascontiguousarray(x, dtype=np.float64)
     if w.shape != x.shape or w.ndim != 2:
         raise ValueError("oracle: w and x must both be [n, W]")
     out = np.empty(w.shape[0], np.uint16)
-    _load().kda_oracle_conv_silu_bf16_f32(w.ctypes.data, x.ctypes.data, out.ctypes.data, w.shape[0], w.shape[1])
+    _load().kda_oracle_conv_silu_bf16(w.ctypes.data, x.ctypes.data, out.ctypes.data, w.shape[0], w.shape[1])
     return out
 
 

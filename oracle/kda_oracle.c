@@ -26,20 +26,13 @@
  * to bf16 (round to nearest even), corrections and committed states to fp32.
  *
  * The convolution output is the one place where floating point decides a
- * stored code: the bf16 value that every later step consumes.  The pages fuse
- * the convolution as causal_conv1d_update does, which accumulates and applies
- * SiLU in fp32 and then casts to bf16, without fixing the order of the sums or
- * the exp routine.  So the oracle takes that decision in fp32 with a fully
- * specified procedure (conv_silu_bf16_f32 below): the taps are summed oldest
- * first, y = w0 x0, then y = fma(wj, xj, y); SiLU is y sigma(y) with
- * sigma(y) = 1/(1+z) or z/(1+z) by the sign of y and z = e^-|y| (Cody-Waite
- * reduction by ln 2, split in a 15-bit head and a tail, and a degree-7 Taylor
- * polynomial), the reciprocal of 1+z in [1, 2] by three Newton steps from a
- * linear start; the result is rounded to bf16, nearest even.  Every step is
- * an IEEE-754 fp32 add, multiply or fma, or integer arithmetic on the bits,
- * so any conforming implementation gets the same bits.  The pins check it against the exact
- * double-precision value (within a few fp32 ulp), so it is an accurate fp32
- * evaluation and not merely a self-consistent one.
+ * stored code: the bf16 value that every later step consumes.  The oracle
+ * takes that decision from the plain definition: y = sum_j w_j x_j in double
+ * (each product of a bf16 input and a bf16 or fp32 weight is exact in double),
+ * SiLU(y) = y / (1 + e^-y) with the C library's exp, and one round-to-nearest-
+ * even of that double to bf16.  The pins check the codes against an exact
+ * (arbitrary-precision) evaluation, including inputs placed next to a bf16
+ * rounding boundary.
  *
  * Readings taken where the pages are silent (each is listed in the design
  * notes of the repository):
@@ -102,85 +95,19 @@ static uint16_t bf16_round(double x) {
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
 /* ------------------------------------------------------------------------- */
-/* The fp32 convolution output, fully specified (see the header)              */
+/* The convolution output                                                     */
 /* ------------------------------------------------------------------------- */
 
-static float f32_from_bits(uint32_t w) {
-    float f;
-    memcpy(&f, &w, sizeof f);
-    return f;
-}
+static double silu(double y) { return y / (1.0 + exp(-y)); }
 
-/* e^x in fp32 for x <= 0: x is clamped below at -104 (e^-104 rounds to 0,
- * so the clamp changes no result); n = round-to-nearest-even of x log2 e,
- * taken from the exact product by adding 1.5 * 2^23 in one fma (the sum's
- * ulp is 1, so the rounding lands on an integer and the low mantissa bits
- * hold n); r = x - n ln2 with ln2 = LN2_HI + LN2_LO (LN2_HI has 15
- * significant bits, so n LN2_HI is exact and each fma rounds once); e^r by
- * the Taylor series to r^7/7! in Horner form (|r| <= 0.347: truncation below
- * 1e-8 relative); then e^x = e^r 2^n1 2^n2 with n1 = floor(n/2) and
- * n2 = n - n1, both >= -75, so the first scaling is exact and the second
- * rounds once (into the subnormal range when n < -126). */
-static float exp_neg_f32(float x) {
-    const float LOG2E = 0x1.715476p+0f;
-    const float SHIFTER = 0x1.8p+23f; /* 1.5 * 2^23 */
-    const float LN2_HI = 0x1.62e4p-1f;
-    const float LN2_LO = 0x1.7f7d1cp-20f;
-    x = fmaxf(x, -104.0f);
-    const float t = fmaf(x, LOG2E, SHIFTER);
-    const float nf = t - SHIFTER;
-    uint32_t tb, sb;
-    memcpy(&tb, &t, sizeof tb);
-    memcpy(&sb, &SHIFTER, sizeof sb);
-    const int n = (int)((int64_t)tb - (int64_t)sb);
-    float r = fmaf(-nf, LN2_HI, x);
-    r = fmaf(-nf, LN2_LO, r);
-    /* 1/k! rounded to fp32, k = 7 .. 2 */
-    float p = 0x1.a01a02p-13f;
-    p = fmaf(p, r, 0x1.6c16c2p-10f);
-    p = fmaf(p, r, 0x1.111112p-7f);
-    p = fmaf(p, r, 0x1.555556p-5f);
-    p = fmaf(p, r, 0x1.555556p-3f);
-    p = fmaf(p, r, 0.5f);
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    const int n1 = n >= 0 ? n / 2 : -((1 - n) / 2); /* floor(n / 2) */
-    const int n2 = n - n1;
-    p = p * f32_from_bits((uint32_t)(n1 + 127) << 23);
-    return p * f32_from_bits((uint32_t)(n2 + 127) << 23);
-}
-
-/* 1/d for d in [1, 2]: r0 = 24/17 - (8/17) d (relative error at most 1/17),
- * then three Newton steps e = 1 - d r, r = r + r e, each two fmas; the error
- * squares each step, so only the fp32 rounding of the last step remains. */
-static float recip_1_2_f32(float d) {
-    float r = fmaf(-0x1.e1e1e2p-2f, d, 0x1.69696ap+0f);
-    for (int i = 0; i < 3; ++i) {
-        const float e = fmaf(-d, r, 1.0f);
-        r = fmaf(r, e, r);
-    }
-    return r;
-}
-
-/* SiLU in fp32: z = e^-|y| (never overflows), sigma(y) = 1/(1+z) for
- * y >= 0 and z/(1+z) below, SiLU = y sigma. */
-static float silu_f32(float y) {
-    const float z = exp_neg_f32(-fabsf(y));
-    const float r = recip_1_2_f32(1.0f + z);
-    const float sigma = (y >= 0.0f ? 1.0f : z) * r;
-    return y * sigma;
-}
-
-/* fp32 -> bf16, nearest even: the fp32 value is exact in double, so one
- * rounding of it is the fp32 -> bf16 rounding. */
-static uint16_t bf16_from_f32(float f) { return bf16_round((double)f); }
-
-/* The conv output code: bf16(SiLU(sum_j w_j x_j)) by the fp32 procedure,
- * taps oldest first, W of them. */
-static uint16_t conv_silu_bf16_f32(const float *w, const float *x, int W) {
-    float y = w[0] * x[0];
-    for (int j = 1; j < W; ++j) y = fmaf(w[j], x[j], y);
-    return bf16_from_f32(silu_f32(y));
+/* [kernels] CuteRecoverSSMVerify.__call__ / [state] deferred_recoverssm_verify
+ * (causal_conv1d_update with activation "silu"): y = sum_j w_j x_j over the W
+ * taps, oldest first (w[W-1] on the newest input), SiLU, and the bf16 code of
+ * the result.  Every product is exact in double. */
+static uint16_t conv_silu_code(const double *w, const double *x, int W) {
+    double y = 0.0;
+    for (int j = 0; j < W; ++j) y += w[j] * x[j];
+    return bf16_round(silu(y));
 }
 
 /* [ops] _kda_gate: gate_input = raw_g + dt_bias; the bounded form is
@@ -237,9 +164,9 @@ static int64_t conv_index(const kda_oracle_verify_args *a, int64_t s, int64_t c,
                              : s * a->conv_slot_stride + j * C + c;
 }
 
-static float conv_weight_value(const kda_oracle_verify_args *a, int64_t c, int j) {
-    if (a->conv_weight_is_fp32) return ((const float *)a->conv_weight)[c * a->W + j];
-    return (float)bf16_value(((const uint16_t *)a->conv_weight)[c * a->W + j]);
+static double conv_weight_value(const kda_oracle_verify_args *a, int64_t c, int j) {
+    if (a->conv_weight_is_fp32) return (double)((const float *)a->conv_weight)[c * a->W + j];
+    return bf16_value(((const uint16_t *)a->conv_weight)[c * a->W + j]);
 }
 
 /* One (request b, head h) of the verify; returns ORACLE_BAD_DATA on an
@@ -282,12 +209,12 @@ static int verify_item(const kda_oracle_verify_args *a, int b, int h) {
             for (int t = 0; t < n; ++t)
                 seq[W - 1 + t] = a->mixed_qkv[(bos + t) * a->qkv_row_stride + c];
             for (int t = 0; t < n; ++t) {
-                float wv[8], xv[8];
+                double wv[8], xv[8];
                 for (int j = 0; j < W; ++j) {
                     wv[j] = conv_weight_value(a, c, j);
-                    xv[j] = (float)bf16_value(seq[t + j]);
+                    xv[j] = bf16_value(seq[t + j]);
                 }
-                post[(size_t)(g * K + i) * n + t] = bf16_value(conv_silu_bf16_f32(wv, xv, W));
+                post[(size_t)(g * K + i) * n + t] = bf16_value(conv_silu_code(wv, xv, W));
             }
             /* rolled state: taps 0 .. W-3+n <- seq[1 .. W-2+n] */
             for (int j = 0; j < W - 2 + n; ++j)
@@ -500,13 +427,7 @@ uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
 double kda_oracle_gate(double raw_g, double dt_bias, double A, int use_lower_bound, double lower_bound) {
     return kda_gate(raw_g, dt_bias, A, use_lower_bound, lower_bound);
 }
-void kda_oracle_exp_neg_f32(const float *x, float *y, int64_t n) {
-    for (int64_t i = 0; i < n; ++i) y[i] = exp_neg_f32(x[i]);
-}
-void kda_oracle_silu_f32(const float *x, float *y, int64_t n) {
-    for (int64_t i = 0; i < n; ++i) y[i] = silu_f32(x[i]);
-}
-/* w, x: [n, W] row-major; out: [n] bf16 codes. */
-void kda_oracle_conv_silu_bf16_f32(const float *w, const float *x, uint16_t *out, int64_t n, int W) {
-    for (int64_t i = 0; i < n; ++i) out[i] = conv_silu_bf16_f32(w + i * W, x + i * W, W);
+/* w, x: [n, W] row-major, taps oldest first; out: [n] bf16 codes. */
+void kda_oracle_conv_silu_bf16(const double *w, const double *x, uint16_t *out, int64_t n, int W) {
+    for (int64_t i = 0; i < n; ++i) out[i] = conv_silu_code(w + i * W, x + i * W, W);
 }

@@ -70,87 +70,98 @@ def test_gate_against_library_routines():
     assert abs(oracle.gate(20.0 + 1e-9, 0, 1) - oracle.gate(20.0 - 1e-9, 0, 1)) < 1e-8
 
 
-def _ulp_f32(v):
-    """fp32 ulp at |v| (v double), the subnormal quantum at the bottom."""
-    f = np.abs(np.asarray(v, np.float64)).astype(np.float32)
-    return np.maximum(np.spacing(f).astype(np.float64), 2.0 ** -149)
-
-
-def test_exp_neg_f32_within_one_ulp_of_exp():
-    rng = np.random.default_rng(5)
-    x = np.concatenate([np.linspace(-103.9, 0.0, 400_001), rng.uniform(-12, 0, 400_000),
-                        -np.abs(rng.standard_normal(200_000) * 3)]).astype(np.float32)
-    got = oracle.exp_neg_f32(x).astype(np.float64)
-    want = np.exp(x.astype(np.float64))
-    assert np.all(np.abs(got - want) <= _ulp_f32(want))
-    # monotone on a sorted grid, and the fixed points of the definition
-    xs = np.sort(x)
-    assert np.all(np.diff(oracle.exp_neg_f32(xs).astype(np.float64)) >= 0)
-    special = oracle.exp_neg_f32(np.array([0.0, -0.0, -104.0, -1e30], np.float32))
-    assert special[0] == 1.0 and special[1] == 1.0
-    assert special[2] == 0.0 and special[3] == 0.0
-    # e^-k for integers k against the correctly rounded constants
-    for k in range(0, 101, 7):
-        assert abs(float(oracle.exp_neg_f32(np.float32(-k))[0]) - math.exp(-k)) <= _ulp_f32(math.exp(-k))
-
-
-def test_silu_f32_within_four_ulp_of_silu():
-    rng = np.random.default_rng(6)
-    x = np.concatenate([np.linspace(-87.0, 88.0, 400_001), rng.standard_normal(300_000) * 4,
-                        rng.uniform(-1e-3, 1e-3, 50_000)]).astype(np.float32)
-    got = oracle.silu_f32(x).astype(np.float64)
-    xd = x.astype(np.float64)
-    want = xd * expit(xd)
-    assert np.all(np.abs(got - want) <= 4 * _ulp_f32(want))
-    # far negative tail: e^y is subnormal, so the error is absolute, far below
-    # bf16's smallest step (2^-133); below -104 the result is -0
-    tail = np.linspace(-104.0, -87.0, 20_001).astype(np.float32)
-    td = tail.astype(np.float64)
-    assert np.all(np.abs(oracle.silu_f32(tail).astype(np.float64) - td * expit(td)) <= 2.0 ** -140)
-    neg = oracle.silu_f32(np.array([-105.0, -1e4], np.float32))
-    assert np.all(neg == 0.0) and np.all(np.signbit(neg))
-    # far positive tail: e^-y vanishes next to 1, SiLU(y) = y
-    big = np.array([90.0, 1e4, 3e38], np.float32)
-    np.testing.assert_array_equal(oracle.silu_f32(big), big)
-    assert oracle.silu_f32(np.float32(0.0))[0] == 0.0
-    assert np.signbit(oracle.silu_f32(np.float32(-0.0))[0])
+def _bf16_bits(v):
+    """bf16 codes (RNE) of float values via torch."""
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
 @pytest.mark.parametrize("fp32_weights", [False, True])
-def test_conv_code_is_the_correct_rounding_but_for_near_ties(fp32_weights):
-    """Codes of the fp32 conv + SiLU against the exact double value rounded once."""
+def test_conv_code_is_the_correct_rounding(fp32_weights):
+    """Codes of conv + SiLU on random taps equal the correctly rounded exact
+    value: double decides where it is unambiguous, 60 digits elsewhere."""
     rng = np.random.default_rng(7 + fp32_weights)
-    n, W = 300_000, 4
+    n, W = 200_000, 4
     gen = torch.Generator().manual_seed(17 + fp32_weights)
-    x = brute.bf16_values(torch.randn(n, W, dtype=torch.float32, generator=gen).mul_(1.5)
-                          .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
-    w = rng.normal(0, 0.5, (n, W)).astype(np.float32)
+    x = brute.bf16_values(_bf16_bits(torch.randn(n, W, dtype=torch.float32, generator=gen).mul_(1.5).numpy()))
+    w = rng.normal(0, 0.5, (n, W)).astype(np.float32).astype(np.float64)
     if not fp32_weights:
-        w = brute.bf16_values(torch.from_numpy(w).to(torch.bfloat16).view(torch.int16)
-                              .numpy().view(np.uint16))
-    codes = oracle.conv_silu_bf16_f32(w, x)
-    y = (w.astype(np.float64) * x.astype(np.float64)).sum(axis=1)
-    mag = np.abs(w.astype(np.float64) * x.astype(np.float64)).sum(axis=1)
-    brute.assert_codes_round_exact(codes, y * expit(y), mag, y, max_frac=2e-3)
+        w = brute.bf16_values(_bf16_bits(w))
+    codes = oracle.conv_silu_bf16(w, x)
+    y = (w * x).sum(axis=1)
+    brute.assert_codes_exact(codes, y)
     # unit taps pick one input: y is that bf16 value exactly
-    onehot = np.zeros((4, W), np.float32)
-    onehot[np.arange(4), np.arange(4)] = 1.0
-    xs = x[:4]
-    got = oracle.conv_silu_bf16_f32(onehot, xs)
-    yy = xs[np.arange(4), np.arange(4)].astype(np.float64)
-    brute.assert_codes_round_exact(got, yy * expit(yy), np.abs(yy), yy)
+    onehot = np.eye(W)
+    got = oracle.conv_silu_bf16(onehot, x[:W])
+    brute.assert_codes_exact(got, np.diag(x[:W]))
 
 
-def test_conv_code_tap_order_is_oldest_first():
-    """fp32 weights, taps whose sum cancels: summing oldest first rounds the
-    running sum at different places than newest first; the codes follow the
-    stated order (w0 x0 first, then fma of each newer tap)."""
-    w = np.array([[1.0, 2.0 ** -30, -1.0, 2.0 ** -30]], np.float32)
-    x = np.array([[1.0, 1.0, 1.0, 1.0]], np.float32)
-    # oldest first: 1 + 2^-30 rounds to 1, - 1 -> 0, + 2^-30 -> 2^-30
-    y = np.float32(2.0 ** -30)
-    want = oracle.bf16_round(float(y) * float(expit(float(y))))
-    assert int(oracle.conv_silu_bf16_f32(w, x)[0]) == want
+def _near_boundary_inputs(count, seed, lo_exp=-45, hi_exp=-30):
+    """Conv inputs whose SiLU lies a chosen distance from a bf16 rounding
+    boundary m: SiLU(y*) = m (1 + d) with |d| = 2^-u, u uniform in
+    (-hi_exp, -lo_exp), solved for y* in 60 digits; y* is split into four fp32
+    pieces (the weights, each times an input 1.0), whose sum is y* to about
+    2^-96.  Returns (w, x, d, lower): lower is the bf16 code on the near-zero
+    side of m, so the correct code is lower + 1 exactly when d > 0."""
+    import mpmath
+    rng = np.random.default_rng(seed)
+    ws, ds, lows = [], [], []
+    with mpmath.workdps(60):
+        for _ in range(count):
+            if rng.random() < 0.7:       # positive branch, SiLU from 1e-3 to 40
+                target = float(np.exp(rng.uniform(np.log(1e-3), np.log(40.0))))
+                lo, hi = 0.0, 60.0
+            else:                        # negative values on the branch y in (-1.278, 0)
+                target = -float(np.exp(rng.uniform(np.log(1e-3), np.log(0.27))))
+                lo, hi = -1.2784645, 0.0
+            code = int(_bf16_bits(np.array([target]))[0])
+            mid = (brute.bf16_values(np.array([code], np.uint16))[0]
+                   + brute.bf16_values(np.array([code + 1], np.uint16))[0]) / 2
+            d = float(rng.choice([-1.0, 1.0]) * 2.0 ** -rng.uniform(-hi_exp, -lo_exp))
+            goal = mpmath.mpf(mid) * (1 + mpmath.mpf(d))
+            f = lambda yy: yy / (1 + mpmath.exp(-yy)) - goal  # noqa: E731
+            r = mpmath.findroot(f, (mpmath.mpf(lo) + 1e-30, mpmath.mpf(hi)), solver="bisect", tol=1e-55)
+            pieces = []
+            for _ in range(4):
+                p = float(np.float32(float(r)))
+                pieces.append(p)
+                r = r - p
+            ws.append(pieces)
+            ds.append(d)
+            lows.append(code)
+    return np.array(ws), np.ones((count, 4)), np.array(ds), np.array(lows, np.uint16)
+
+
+def test_conv_code_next_to_rounding_boundaries():
+    """Adversarial pin: SiLU values placed 2^-45 .. 2^-30 (relative) from a
+    bf16 rounding boundary, where a plain fp32 evaluation picks the wrong
+    neighbour about half the time and double precision still decides.  The
+    oracle's codes must be the exact ones."""
+    pytest.importorskip("mpmath")
+    w, x, d, lower = _near_boundary_inputs(600, seed=23)
+    codes = oracle.conv_silu_bf16(w, x)
+    want = brute.silu_codes_exact(w * x)
+    np.testing.assert_array_equal(codes, want)
+    # the 60-digit reference lands on the side of the boundary the construction chose
+    np.testing.assert_array_equal(want, lower + (d > 0).astype(np.uint16))
+    # the inputs are sharp: fp32 arithmetic gets a good share of them wrong
+    yf = (w * x).sum(axis=1).astype(np.float32)
+    naive = _bf16_bits(yf / (np.float32(1) + np.exp(-yf)))
+    assert np.mean(naive != want) > 0.1
+
+
+def test_silu_codes_exact_against_known_roundings():
+    """The 60-digit reference itself: SiLU(0) = 0, large y rounds like y, and
+    values far from a boundary agree with the double evaluation."""
+    assert int(brute.silu_codes_exact([0.0])[0]) == 0
+    big = np.array([64.0, 100.0, 3.0e4])
+    np.testing.assert_array_equal(brute.silu_codes_exact(big), _bf16_bits(big))
+    yy = np.linspace(-8, 8, 2001)
+    s = yy * expit(yy)
+    far = brute.bf16_midpoint_distance(s) > 1e-9
+    np.testing.assert_array_equal(brute.silu_codes_exact(yy[far]), brute.bf16_rne(s[far]))
+    # the test's own rounding agrees with torch's on fp32-exact values, subnormals included
+    f = np.concatenate([s, s * 2.0 ** -130, -s * 2.0 ** -128]).astype(np.float32)
+    np.testing.assert_array_equal(brute.bf16_rne(f.astype(np.float64)), _bf16_bits(f))
 
 
 # --------------------------------------------------------------------------- brute force
@@ -217,7 +228,7 @@ def test_verify_matches_matrix_form_bruteforce(variant):
                 continue
             sx, mag, y = brute.conv_silu_exact(it["hist"], it["x"], it["w"])
             post = res["post_conv"][it["bos"]: it["bos"] + it["n"]][:, it["chans"]]
-            brute.assert_codes_round_exact(_codes(post), sx, mag, y, max_frac=0.02)
+            brute.assert_codes_exact(_codes(post), y)
             q, k, v = post[:, :K], post[:, K: 2 * K], post[:, 2 * K:]
             o, c, states = brute.window(it["S0"], q, k, v, it["raw_g"], it["raw_beta"],
                                         fresh.dt_bias[h * K:(h + 1) * K].astype(np.float64),
@@ -471,8 +482,7 @@ def test_conv_unit_taps(dim_first):
             seq = np.concatenate([it["hist"], it["x"]], axis=0)
             for t in range(it["n"]):
                 src = seq[t + tap]
-                brute.assert_codes_round_exact(_codes(res["post_conv"][it["bos"] + t, it["chans"]]),
-                                               src * expit(src), np.abs(src), src, max_frac=0.1)
+                brute.assert_codes_exact(_codes(res["post_conv"][it["bos"] + t, it["chans"]]), src)
 
 
 @pytest.mark.parametrize("dim_first", [True, False])

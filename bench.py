@@ -462,7 +462,8 @@ def run_gpu(args, rank, local, world):
             "algorithmic_bytes_per_step": acct["deferred_step_bytes"], "steps": d_steps,
             "schedule": "each layer's verify first folds the previous step's accepted records into the "
                         "checkpoint (kda_verify_fold), no commit launch"},
-        "gpu_launches": args.steps * (L + 1),
+        # each kda_verify is two launches (the conv pass, then the verify kernel)
+        "gpu_launches": args.steps * (2 * L + 1),
         "clocks": clk,
         "cpu_baseline": cpu,
     }

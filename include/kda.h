@@ -88,10 +88,9 @@ enum {
  *      a = clamp(num_accepted_prev[b], 1, Q) (a = 1 when the pointer is NULL);
  *      seq = history followed by mixed_qkv[bos..bos+n, c];
  *      y_t = bf16_rne(silu(sum_j w[c,j] * seq[t+j])), w[c,W-1] on the newest
- *      input, evaluated by one fixed fp32 procedure (taps summed oldest first
- *      with fma, e^-|y| by a Cody-Waite reduction and a degree-7 Taylor
- *      polynomial, 1/(1+z) by three Newton steps), so the code is
- *      reproducible bit for bit on any IEEE-754 machine;
+ *      input, rounded once from the mathematical value (an fp32 evaluation
+ *      with an error bound; the few codes within that bound of a rounding
+ *      boundary are recomputed in float-float or double arithmetic);
  *      the slot then stores seq[1 .. W-2+n] at taps 0 .. W-3+n (in place;
  *      later taps are left as they were).
  *   2. q^ = q * rsqrt(|q|^2 + 1e-6) * K^-1/2, k^ = k * rsqrt(|k|^2 + 1e-6),
@@ -103,6 +102,14 @@ enum {
  *      key_gate[r, h, t, K..2K) = raw_gate[bos+t, h*K ..] (bit copy).
  *      Rows and records of tokens t >= n are not written.
  * T == 0 or B == 0 is a no-op returning KDA_OK.
+ *
+ * Two kernels run, in stream order: the conv pass (one CTA per (request,
+ * head): the codes y_t, packed with the raw gate rows into `scratch`, and the
+ * rolled conv state) and the verify proper (persistent, one CTA per SM).
+ * `scratch` is caller-owned device memory of at least
+ * kda_verify_scratch_bytes(B, H, K, Q) bytes, 16-byte aligned; its contents
+ * between calls are unspecified (calls that may overlap need distinct
+ * scratch buffers).  It may be NULL when T == 0.
  *
  * Supported: K == V in {64, 128}, W == 4, 1 <= Q <= 8.  Alignment: state,
  * corr, key_gate, conv_state, conv_weight, A_log and dt_bias must start on
@@ -149,7 +156,25 @@ typedef struct kda_verify_args {
     const int32_t *record_indices;    /* [B] or NULL (records at the state slot)    */
     const int32_t *num_accepted_prev; /* [B] conv read offset, or NULL (a = 1)      */
     int32_t *workspace;               /* kda_workspace_bytes() bytes, zeroed, or NULL */
+    void *scratch;                    /* device, >= kda_verify_scratch_bytes(), 16-byte aligned */
+    int64_t scratch_bytes;            /* its size in bytes                          */
+    int32_t variant;                  /* kda_verify_variant                         */
 } kda_verify_args;
+
+/* Which kernel computes the products S0 [X | Y] of the verify.  AUTO picks
+ * the faster on GB300 for the window (tensor cores for Q > 4 at K == 128,
+ * CUDA cores otherwise); the others force one (tensor cores need K == 128,
+ * and the fold runs on the CUDA cores whatever is asked). */
+typedef enum kda_verify_variant {
+    KDA_VERIFY_AUTO = 0,
+    KDA_VERIFY_CUDA_CORE = 1,
+    KDA_VERIFY_TCGEN05 = 2
+} kda_verify_variant;
+
+/* Bytes of scratch the verify needs: B * H * Q * 4K bf16 (the conv pass's
+ * output, [Q][2K] rows q | v and [Q][2K] rows k | gate per (request, head)). */
+size_t kda_verify_scratch_bytes(int32_t B, int32_t H, int32_t K, int32_t Q);
+
 
 /*
  * kda_commit -- fold each request's first m accepted verify records into its
@@ -251,12 +276,10 @@ typedef struct kda_align_args {
 
 kda_status kda_commit_align(const kda_commit_args *args, const kda_align_args *align, kda_stream_t stream);
 
-/* Enqueue the verify of one layer.  Returns before the kernel runs.
- * At K == 128 the products S0 [X | Y] run on tcgen05 tensor cores (tf32 with
- * a hi/lo split of the state, same tolerances) for windows Q > 4 and on the
- * CUDA cores for Q <= 4, the faster of the two on GB300 for each; the
- * environment variable KDA_VERIFY_TCGEN05=1 (or =0) at the call forces the
- * tensor cores (or the CUDA cores). */
+/* Enqueue the verify of one layer (the conv pass, then the verify kernel).
+ * Returns before the kernels run.  args->variant selects the products'
+ * kernel (kda_verify_variant): at K == 128 the tcgen05 tensor cores (tf32
+ * with a hi/lo split of the state, same tolerances) or the CUDA cores. */
 kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
 
 /* Enqueue the commit of all layers (one kernel launch). */
@@ -300,7 +323,7 @@ const char *kda_last_error(void);
 /* ABI version of this header (bumped on any layout change). */
 int32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

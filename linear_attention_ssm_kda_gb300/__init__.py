@@ -25,7 +25,7 @@ import torch
 __all__ = [
     "commit_noalloc",
     "KdaError", "lib_path", "load_library", "verify", "CommitContext", "workspace_bytes",
-    "new_workspace", "read_device_error", "last_error",
+    "new_workspace", "read_device_error", "last_error", "verify_scratch_bytes", "new_verify_scratch",
     "DEVERR_SLOT_RANGE", "DEVERR_ROW_RANGE", "DEVERR_TOKEN_RANGE", "DEVERR_TIMEOUT", "DEVERR_MISALIGNED",
 ]
 
@@ -68,7 +68,11 @@ class VerifyArgs(ctypes.Structure):
         ("key_gate", _p), ("kg_row_stride", _i64),
         ("query_start_loc", _p), ("state_indices", _p), ("record_indices", _p),
         ("num_accepted_prev", _p), ("workspace", _p),
+        ("scratch", _p), ("scratch_bytes", _i64), ("variant", _i32),
     ]
+
+
+VARIANTS = {"auto": 0, "cuda_core": 1, "tcgen05": 2}
 
 
 class AlignArgs(ctypes.Structure):
@@ -124,6 +128,8 @@ def load_library():
             lib.kda_commit_noalloc.restype = ctypes.c_int
             lib.kda_workspace_bytes.argtypes = []
             lib.kda_workspace_bytes.restype = ctypes.c_size_t
+            lib.kda_verify_scratch_bytes.argtypes = [_i32, _i32, _i32, _i32]
+            lib.kda_verify_scratch_bytes.restype = ctypes.c_size_t
             lib.kda_read_device_error.argtypes = [_p, _p, ctypes.POINTER(_i32)]
             lib.kda_read_device_error.restype = ctypes.c_int
             lib.kda_last_error.argtypes = []
@@ -145,6 +151,16 @@ def _check(status: int) -> None:
 
 def workspace_bytes() -> int:
     return int(load_library().kda_workspace_bytes())
+
+
+def verify_scratch_bytes(B: int, H: int, K: int, window: int) -> int:
+    """Bytes of device scratch one verify call needs (the conv pass's output)."""
+    return int(load_library().kda_verify_scratch_bytes(B, H, K, window))
+
+
+def new_verify_scratch(B: int, H: int, K: int, window: int, device) -> torch.Tensor:
+    """Device scratch for ``verify`` (allocated by torch on the current stream)."""
+    return torch.empty(max(verify_scratch_bytes(B, H, K, window), 16), dtype=torch.uint8, device=device)
 
 
 def new_workspace(device) -> torch.Tensor:
@@ -197,7 +213,7 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
            key_gate, query_start_loc, state_indices, conv_state, conv_weight, out, window,
            num_accepted_tokens=None, record_indices=None, conv_dim_first=True, null_block_id=0,
            workspace=None, stream=None, fold_query_start_loc=None, fold_num_accepted=None,
-           fold_record_indices=None) -> None:
+           fold_record_indices=None, scratch=None, variant: str = "auto") -> None:
     """Verify ``state_indices.shape[0]`` requests of one KDA layer.
 
     ``mixed_qkv`` [T, 3HK] is the raw projection (before the convolution),
@@ -214,7 +230,13 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
     step's query_start_loc [B+1] and accepted counts [B], and optionally its
     record rows ``fold_record_indices``) this is ``kda_verify_fold``: each
     request's pending records are first folded into its checkpoint, which is
-    written back, and the verify runs on the folded state (windows up to 4)."""
+    written back, and the verify runs on the folded state (windows up to 4).
+
+    ``scratch`` is a device buffer of at least ``verify_scratch_bytes(B, H,
+    K, window)`` bytes for the conv pass's output; when None, one is taken
+    from torch's allocator on the launch stream for this call.  ``variant``
+    ("auto", "cuda_core" or "tcgen05") picks the kernel of the products (the
+    tensor cores need K = 128)."""
     dev = state.device
     if dev.type != "cuda":
         raise ValueError("verify runs on a CUDA device; state is on " + str(dev))
@@ -303,6 +325,18 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
     a.query_start_loc, a.state_indices = query_start_loc.data_ptr(), state_indices.data_ptr()
     a.record_indices, a.num_accepted_prev = _ptr(record_indices), _ptr(num_accepted_tokens)
     a.workspace = _ptr(workspace)
+    if variant not in VARIANTS:
+        raise ValueError(f"variant must be one of {sorted(VARIANTS)}")
+    a.variant = VARIANTS[variant]
+    need = verify_scratch_bytes(B, H, K, window)
+    if scratch is None and T > 0:
+        # tied to the launch stream, so torch reuses it only after this call's kernels
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream(dev)):
+            scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+    if scratch is not None:
+        if scratch.device != dev or not scratch.is_contiguous():
+            raise ValueError("scratch must be a contiguous tensor on the state's device")
+        a.scratch, a.scratch_bytes = scratch.data_ptr(), scratch.numel() * scratch.element_size()
     handle = ctypes.c_void_p(_stream_handle(dev, stream))
     if fold is None:
         _check(load_library().kda_verify(ctypes.byref(a), handle))

@@ -16,7 +16,7 @@
 #include "kda_params.h"
 
 namespace kda {
-cudaError_t launch_verify(const VerifyParams& p, int K, cudaStream_t stream);
+cudaError_t launch_verify(const VerifyParams& p, int K, int variant, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, int K, cudaStream_t stream);
 cudaError_t noalloc_tables(long long** out);
 }  // namespace kda
@@ -54,6 +54,12 @@ extern "C" {
 int32_t kda_abi_version(void) { return KDA_ABI_VERSION; }
 
 size_t kda_workspace_bytes(void) { return 16; }
+
+size_t kda_verify_scratch_bytes(int32_t B, int32_t H, int32_t K, int32_t Q) {
+  if (B <= 0 || H <= 0 || K <= 0 || Q <= 0) return 0;
+  return static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(Q) * 4u * static_cast<size_t>(K) * 2u;
+}
+
 
 const char* kda_last_error(void) { return g_error; }
 
@@ -98,9 +104,22 @@ kda_status verify_params(const kda_verify_args* a, bool fold, kda::VerifyParams&
     return fail(KDA_ERR_INVALID_ARG, "kda_verify: num_slots and num_record_rows must be positive");
   const long long H = a->H, K = a->K, V = a->V, Q = a->Q;
   const long long conv_len = Q + kConvWidth - 2;
-  if (a->qkv_row_stride < 3 * H * K || a->gate_row_stride < H * K || a->beta_row_stride < H ||
-      a->out_row_stride < H * V)
+  // with no token row (a fold-only step) the activations are never read:
+  // their pointers may be NULL and their strides anything
+  if (a->T > 0 && (a->qkv_row_stride < 3 * H * K || a->gate_row_stride < H * K || a->beta_row_stride < H ||
+                   a->out_row_stride < H * V))
     return fail(KDA_ERR_INVALID_ARG, "kda_verify: an activation row stride is shorter than its row");
+  if (a->variant != KDA_VERIFY_AUTO && a->variant != KDA_VERIFY_CUDA_CORE && a->variant != KDA_VERIFY_TCGEN05)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify: variant %d", a->variant);
+  if (a->variant == KDA_VERIFY_TCGEN05 && K != 128)
+    return fail(KDA_ERR_UNSUPPORTED, "kda_verify: the tensor-core variant needs K == 128 (K = %lld)", K);
+  if (a->T > 0) {
+    const size_t need = kda_verify_scratch_bytes(a->B, a->H, a->K, a->Q);
+    if (a->scratch == nullptr || a->scratch_bytes < 0 || static_cast<size_t>(a->scratch_bytes) < need)
+      return fail(KDA_ERR_INVALID_ARG, "kda_verify: scratch of %zu bytes required (got %lld)", need,
+                  static_cast<long long>(a->scratch_bytes));
+    if (!aligned(a->scratch, 16)) return fail(KDA_ERR_MISALIGNED, "kda_verify: scratch must start on 16 bytes");
+  }
   if (a->conv_slot_stride < 3 * H * K * conv_len)
     return fail(KDA_ERR_INVALID_ARG, "kda_verify: conv_slot_stride %lld < 3HK*(Q+W-2) = %lld",
                 (long long)a->conv_slot_stride, 3 * H * K * conv_len);
@@ -138,6 +157,7 @@ kda_status verify_params(const kda_verify_args* a, bool fold, kda::VerifyParams&
   p.record_indices = a->record_indices; p.num_accepted_prev = a->num_accepted_prev;
   p.workspace = a->workspace;
   p.k_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(K)));
+  p.scratch = static_cast<uint16_t*>(a->scratch);
   if ((long long)p.B * p.H > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: B*H too large");
   return KDA_OK;
 }
@@ -151,7 +171,7 @@ kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
   bool noop = false;
   const kda_status st = verify_params(a, false, p, &noop);
   if (st != KDA_OK || noop) return st;
-  cudaError_t e = kda::launch_verify(p, a->K, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = kda::launch_verify(p, a->K, a->variant, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify: launch failed: %s", cudaGetErrorString(e));
   return KDA_OK;
 }
@@ -168,7 +188,7 @@ kda_status kda_verify_fold(const kda_verify_args* a, const kda_fold_args* f, kda
   p.fold_qsl = f->query_start_loc;
   p.fold_num_accepted = f->num_accepted;
   p.fold_record_indices = f->record_indices;
-  cudaError_t e = kda::launch_verify(p, a->K, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = kda::launch_verify(p, a->K, a->variant, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify_fold: launch failed: %s", cudaGetErrorString(e));
   return KDA_OK;
 }

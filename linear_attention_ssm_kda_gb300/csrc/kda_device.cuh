@@ -245,35 +245,42 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 }
 
 // ----------------------------------------------------------------------------
-// The convolution output code.  The conv runs in fp32, as causal_conv1d_update
-// does, and the code stored for every later step is bf16(SiLU(y)).  So that
-// the code does not depend on how a compiler or a math library evaluates it,
-// every step is an IEEE-754 fp32 add, multiply or fma, or integer arithmetic
-// on the bits, in a fixed order, with no branch:
-//   y = w0 x0, then y = fma(wj, xj, y) for the newer taps j = 1 .. W-1;
-//   z = e^-|y|: x = max(-|y|, -104) (e^-104 rounds to 0); n = x log2 e rounded
-//     to nearest even, from the exact product, by one fma with 1.5 * 2^23
-//     (whose ulp is 1, so n sits in the low mantissa bits); Cody-Waite
-//     reduction r = x - n ln2 with ln2 split in a 15-bit head (n times it is
-//     exact) and a tail; e^r by its Taylor series to r^7/7! in Horner form
-//     (|r| <= 0.347, truncation under 1e-8 relative); z = e^r 2^n1 2^n2 with
-//     n1 = floor(n/2), n2 = n - n1 (the first scaling is exact, the second
-//     rounds once);
-//   1/(1+z), 1+z in [1, 2]: r0 = 24/17 - (8/17)(1+z), then three Newton steps;
-//   SiLU(y) = y sigma with sigma = 1/(1+z) for y >= 0 and z/(1+z) below.
-// e^x is within one fp32 ulp of exact, SiLU within four.
+// The convolution output code: bf16_rne(SiLU(y)), y = sum_j w_j x_j over the
+// W = 4 taps, rounded once from the mathematical value
+// ("vllm.models.kimi_k3.nvidia.specialized_decode.recoverssm.state",
+// deferred_recoverssm_verify: causal_conv1d_update with activation "silu",
+// output in the activation dtype).  Three tiers decide it:
+//   1. fp32 (conv_silu_bf16x2, both tokens of a pair on the packed fp32x2
+//      unit): y by an fma chain, SiLU by the procedure in silu_f32x2, and a
+//      bound E on |computed - exact|.  When no bf16 rounding boundary lies
+//      within E of the computed value, the hardware rounding of it is the
+//      correctly rounded code.  Otherwise the code is marked doubtful (about
+//      3 in 10^4 codes on N(0,1) data).
+//   2. float-float (conv_code_exact): y exactly as a pair of floats, e^-|y| by
+//      a 32-entry table and a short series, SiLU by a pair-of-floats quotient,
+//      relative error far below 2^-36; decides every code not within 2^-36 of
+//      a boundary.
+//   3. double: the definition evaluated in fp64 (exact products, the sum in
+//      tap order, y / (1 + e^-y)) and rounded once, for what tier 2 leaves.
 // ----------------------------------------------------------------------------
-// Two codes at once (tokens a and b of one channel) on the packed fp32x2 unit:
-// every half runs exactly the sequence described above, operation by
-// operation (fma(-n, c, x) is computed as fma(n, -c, x), the same exact value).
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
-__device__ __forceinline__ float2 silu_f32x2(float2 y) {
+// SiLU(y) = y sigma(y) in fp32 from IEEE-754 adds, multiplies and fmas:
+//   z = e^-|y|: x = max(-|y|, -104); n = x log2 e rounded to nearest even (one
+//     fma with 1.5 * 2^23, whose ulp is 1, leaves n in the low mantissa bits);
+//     Cody-Waite reduction r = x - n ln2 with ln2 split in a 15-bit head (n
+//     times it is exact) and a tail; e^r by its Taylor series to r^7/7! in
+//     Horner form (|r| <= 0.347); z = e^r 2^n1 2^n2, n1 = floor(n/2), n2 = n - n1;
+//   1/(1+z) for 1+z in [1, 2]: r0 = 24/17 - (8/17)(1+z), then three Newton steps;
+//   sigma = 1/(1+z) for y >= 0 and z/(1+z) below, SiLU = y sigma.
+// Its relative error against the exact SiLU of the fp32 input is at most
+// kSiluRelErr for every y >= -80 (checked over all fp32 inputs).  sigma is
+// returned for the error bound.
+__device__ __forceinline__ float2 silu_f32x2(float2 y, float2& sigma) {
   constexpr float kLog2e = 0x1.715476p+0f;
   constexpr float kShifter = 0x1.8p+23f;
   constexpr float kLn2Hi = 0x1.62e4p-1f;
   constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
-  // z = e^x, x = max(-|y|, -104)
   const float2 x = make_float2(fmaxf(-fabsf(y.x), -104.0f), fmaxf(-fabsf(y.y), -104.0f));
   // n = rint(x log2 e) through the shifter, lane by lane on the scalar unit
   const float ta = __fmaf_rn(x.x, kLog2e, kShifter), tb = __fmaf_rn(x.y, kLog2e, kShifter);
@@ -295,7 +302,6 @@ __device__ __forceinline__ float2 silu_f32x2(float2 y) {
   q = __fmul2_rn(q, make_float2(__int_as_float((na1 + 127) << 23), __int_as_float((nb1 + 127) << 23)));
   const float2 z =
       __fmul2_rn(q, make_float2(__int_as_float((na - na1 + 127) << 23), __int_as_float((nb - nb1 + 127) << 23)));
-  // 1/(1+z), 1+z in [1, 2]: linear start, three Newton steps
   const float2 d = __fadd2_rn(f2(1.0f), z);
   const float2 dn = make_float2(-d.x, -d.y);
   float2 rc = __ffma2_rn(f2(-0x1.e1e1e2p-2f), d, f2(0x1.69696ap+0f));
@@ -304,21 +310,240 @@ __device__ __forceinline__ float2 silu_f32x2(float2 y) {
     const float2 e = __ffma2_rn(dn, rc, f2(1.0f));
     rc = __ffma2_rn(rc, e, rc);
   }
-  const float2 sigma = __fmul2_rn(make_float2(y.x >= 0.0f ? 1.0f : z.x, y.y >= 0.0f ? 1.0f : z.y), rc);
+  sigma = __fmul2_rn(make_float2(y.x >= 0.0f ? 1.0f : z.x, y.y >= 0.0f ? 1.0f : z.y), rc);
   return __fmul2_rn(y, sigma);
 }
 
-// bf16 codes of SiLU(sum_j w_j x_j) for two windows xa, xb of one channel
-// (W = 4 taps, oldest first): the low half holds a, the high half b.
-__device__ __forceinline__ uint32_t conv_silu_bf16x2(const float w[4], const float xa[4], const float xb[4]) {
-  float2 y = __fmul2_rn(f2(w[0]), make_float2(xa[0], xb[0]));
-  y = __ffma2_rn(f2(w[1]), make_float2(xa[1], xb[1]), y);
-  y = __ffma2_rn(f2(w[2]), make_float2(xa[2], xb[2]), y);
-  y = __ffma2_rn(f2(w[3]), make_float2(xa[3], xb[3]), y);
-  const float2 s = silu_f32x2(y);
+// Relative error bound of silu_f32x2 (in units of 2^-24, with margin over the
+// largest error seen across all fp32 inputs >= -80: 4.1) and the lowest y
+// tier 1 serves (below it e^-|y| nears the subnormal range).
+constexpr float kSiluRelErr = 6.0f * 0x1p-24f;
+constexpr float kTier1MinY = -80.0f;
+
+// Tier 1: the bf16 codes of SiLU(sum_j w_j x_j) for two windows xa, xb of one
+// channel (W = 4 taps, oldest first; the low half of the result holds a, the
+// high half b), and in bits 0 / 1 of *doubt whether the code of a / b must be
+// decided by the exact tiers.
+//
+// The fma chain starts from +0, so an exactly zero sum is +0 (SiLU(0) = +0).
+// Its error dy is at most u (|y_2| + |y_3| + |y_4|) over the partial sums y_k,
+// u = 2^-24, plus u |y_1| for fp32 weights (a bf16 weight times a bf16 input
+// is exact; e0 is 1 for fp32 weights and 0 for bf16), so
+// dy^2 <= 4 u^2 (e0 y_1^2 + y_2^2 + y_3^2 + y_4^2).  The conv error moves s by
+// at most slope dy, where |SiLU'| <= 1.1 everywhere and |SiLU'(t)| =
+// |sigma(t) + SiLU(t)(1 - sigma(t))| <= sigma + |SiLU|, which over
+// [y - dy, y + dy] stays below sigma + |s| + 1.35 dy; hence
+// slope^2 <= min(1.21, 4 (sigma^2 + s^2) + 4 dy^2).  With the evaluation error
+// kSiluRelErr |s|, the total error E obeys E^2 <= 2 kSiluRelErr^2 s^2 +
+// 2 slope^2 dy^2.  The code is certain when the square of the distance from s
+// to the midpoint of its bf16 interval exceeds that bound, and the bound stays
+// below 2^-20 s^2 (the next midpoint is at least 2^-10 |s| away).  The
+// constants carry slack for the bound's own rounding; the 2^-126 term makes
+// every |s| below 2^-63 doubtful, where the squares leave the normal range.
+__device__ __forceinline__ uint32_t conv_silu_bf16x2(const float w[4], const float xa[4], const float xb[4], float e0,
+                                                     uint32_t* doubt) {
+  constexpr float k4U2 = 0x1.0001p-46f;                            // 4 u^2
+  constexpr float k2Eps2 = 2.0f * 36.0f * 0x1p-48f * 1.0001f;       // 2 kSiluRelErr^2
+  const float2 y1 = __ffma2_rn(f2(w[0]), make_float2(xa[0], xb[0]), f2(0.0f));
+  const float2 y2 = __ffma2_rn(f2(w[1]), make_float2(xa[1], xb[1]), y1);
+  const float2 y3 = __ffma2_rn(f2(w[2]), make_float2(xa[2], xb[2]), y2);
+  const float2 y = __ffma2_rn(f2(w[3]), make_float2(xa[3], xb[3]), y3);
+  float2 sigma;
+  const float2 s = silu_f32x2(y, sigma);
+  // dy^2 bound
+  float2 q = __fmul2_rn(__fmul2_rn(f2(e0), y1), y1);
+  q = __ffma2_rn(y2, y2, q);
+  q = __ffma2_rn(y3, y3, q);
+  q = __ffma2_rn(y, y, q);
+  const float2 dy2 = __fmul2_rn(f2(k4U2), q);
+  const float2 s2 = __fmul2_rn(s, s);
+  const float2 sl = __ffma2_rn(f2(4.001f), __ffma2_rn(sigma, sigma, s2), __fmul2_rn(f2(4.001f), dy2));
+  const float2 sl2 = make_float2(fminf(1.2101f, sl.x), fminf(1.2101f, sl.y));
+  const float2 bound = __ffma2_rn(f2(k2Eps2), s2, __ffma2_rn(f2(2.001f), __fmul2_rn(sl2, dy2), f2(0x1p-126f)));
+  const float2 mid = make_float2(__uint_as_float((__float_as_uint(s.x) & 0xFFFF0000u) | 0x8000u),
+                                 __uint_as_float((__float_as_uint(s.y) & 0xFFFF0000u) | 0x8000u));
+  const float2 dist = __fadd2_rn(s, make_float2(-mid.x, -mid.y));  // exact: s and mid lie within a factor 2
+  const float2 d2 = __fmul2_rn(dist, dist);
+  const float2 reach = __fmul2_rn(f2(0x1p-20f), s2);
+  const bool da = !(d2.x > bound.x) || !(bound.x < reach.x) || !(y.x >= kTier1MinY);
+  const bool db = !(d2.y > bound.y) || !(bound.y < reach.y) || !(y.y >= kTier1MinY);
+  *doubt = (da ? 1u : 0u) | (db ? 2u : 0u);
   const __nv_bfloat162 b = __floats2bfloat162_rn(s.x, s.y);
   return *reinterpret_cast<const uint32_t*>(&b);
 }
+
+// ---- tiers 2 and 3 ----
+namespace exact_conv {
+
+struct FF {  // h + l, |l| well below ulp(h) after normalisation
+  float h, l;
+};
+
+// error-free transforms (every operation rounds exactly once: no contraction)
+__device__ __forceinline__ FF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ FF fast_two_sum(float a, float b) {  // needs |a| >= |b| or a == 0
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ FF two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+  const FF p = two_prod(a.h, b.h);
+  float e = __fmaf_rn(a.h, b.l, p.l);
+  e = __fmaf_rn(a.l, b.h, e);
+  return fast_two_sum(p.h, e);
+}
+
+// 2^(j/32), j = 0 .. 31, as hi = the nearest fp32 and lo = the nearest fp32
+// to the remainder (Tang's table-driven exponential).
+static __device__ __constant__ float kExp2Hi[32] = {
+    0x1.000000p+0f, 0x1.059b0ep+0f, 0x1.0b5586p+0f, 0x1.11301ep+0f, 0x1.172b84p+0f, 0x1.1d4874p+0f,
+    0x1.2387a6p+0f, 0x1.29e9e0p+0f, 0x1.306fe0p+0f, 0x1.371a74p+0f, 0x1.3dea64p+0f, 0x1.44e086p+0f,
+    0x1.4bfdaep+0f, 0x1.5342b6p+0f, 0x1.5ab07ep+0f, 0x1.6247ecp+0f, 0x1.6a09e6p+0f, 0x1.71f75ep+0f,
+    0x1.7a1148p+0f, 0x1.82589ap+0f, 0x1.8ace54p+0f, 0x1.93737cp+0f, 0x1.9c4918p+0f, 0x1.a5503cp+0f,
+    0x1.ae89fap+0f, 0x1.b7f770p+0f, 0x1.c199bep+0f, 0x1.cb720ep+0f, 0x1.d5818ep+0f, 0x1.dfc974p+0f,
+    0x1.ea4afap+0f, 0x1.f50766p+0f};
+static __device__ __constant__ float kExp2Lo[32] = {
+    0.0f,             -0x1.9d4f52p-25f, 0x1.9f3122p-25f,  -0x1.fdb496p-25f, -0x1.c15742p-27f, -0x1.d2e8cap-25f,
+    0x1.ceac48p-25f,  -0x1.5c0424p-25f, 0x1.4636e2p-25f,  -0x1.18aac6p-25f, 0x1.824684p-25f,  0x1.8624b4p-30f,
+    -0x1.593abcp-25f, -0x1.2c5610p-25f, -0x1.5bd5ecp-27f, -0x1.f8b550p-25f, 0x1.9fcef4p-26f,  0x1.1d8beep-25f,
+    -0x1.829fd0p-25f, -0x1.accc7cp-26f, 0x1.15506ep-27f,  -0x1.e64744p-25f, 0x1.51f848p-27f,  -0x1.b83b54p-25f,
+    -0x1.a94b14p-26f, -0x1.a09438p-25f, -0x1.3d56b2p-27f, -0x1.8837ccp-27f, -0x1.822dbcp-27f, -0x1.908c94p-25f,
+    0x1.52486cp-27f,  -0x1.246eb0p-26f};
+
+// Tier 2.  Returns the code, or -1 when tier 3 must decide.
+//   y = sum_j w_j x_j as a pair (h, l): each product split exactly
+//     (two_prod), the high parts summed with two_sum, the seven low parts
+//     summed with two_sum and their rounding errors gathered; |y - (h + l)|
+//     <= 2^-47 |h| + 2^-61 sum_j |w_j x_j| (+ 2^-145 for subnormal products).
+//   e^x, x = -|y| >= -87: n = rint(32 x / ln2), r = x - n ln2/32 with
+//     ln2/32 = C1 + C2 + C3 (C1 has 12 significant bits, so n C1 is exact for
+//     |n| < 4096), |r| <= ln2/64; e^r = 1 + r + r^2/2 + r^3 (1/6 + r/24 +
+//     r^2/120) with the first three terms as pairs (truncation < 2^-48);
+//     e^x = z' 2^m, z' = e^r 2^((n mod 32)/32), m = floor(n/32).
+//   s = y / (1 + z) (y >= 0), or y z / (1 + z) = 2^m (y z' / (1 + z)) (y < 0),
+//     z = e^-|y|, as a pair: q1 = RN(num / d), q2 from the exact residual
+//     num - q1 d.  For y < 0 the rounding is decided on the unscaled quotient
+//     and the code rescaled by 2^m (|s| >= 87 e^-87 > 2^-126: a normal bf16,
+//     where rounding commutes with the power-of-two scaling).
+//   The code is the rounding of s.h + s.l, decided when the pair lies farther
+//   from the bf16 midpoint than 2^-36 |s| plus the effect of the conv error.
+static __device__ __noinline__ int conv_code_ff(float w0, float w1, float w2, float w3, float x0, float x1, float x2,
+                                                float x3) {
+  const FF p0 = two_prod(w0, x0), p1 = two_prod(w1, x1), p2 = two_prod(w2, x2), p3 = two_prod(w3, x3);
+  const FF a = two_sum(p0.h, p1.h), b = two_sum(p2.h, p3.h), c = two_sum(a.h, b.h);
+  FF t = two_sum(p0.l, p1.l);
+  float err = t.l;
+  t = two_sum(t.h, p2.l);
+  err = __fadd_rn(err, t.l);
+  t = two_sum(t.h, p3.l);
+  err = __fadd_rn(err, t.l);
+  t = two_sum(t.h, a.l);
+  err = __fadd_rn(err, t.l);
+  t = two_sum(t.h, b.l);
+  err = __fadd_rn(err, t.l);
+  t = two_sum(t.h, c.l);
+  err = __fadd_rn(err, t.l);
+  FF y = two_sum(c.h, t.h);
+  y = two_sum(y.h, __fadd_rn(y.l, err));
+  const float mag = fabsf(p0.h) + fabsf(p1.h) + fabsf(p2.h) + fabsf(p3.h);
+  const float dy = __fmaf_rn(0x1p-46f, fabsf(y.h), __fmaf_rn(0x1p-60f, mag, 0x1p-144f));
+  if (y.h == 0.0f) return mag == 0.0f ? 0 : -1;  // an exactly zero sum: SiLU = +0
+  if (!(y.h >= -87.0f)) return -1;
+  const bool neg = y.h < 0.0f;
+  const FF x = neg ? y : FF{-y.h, -y.l};  // -|y|
+  // z' and m
+  constexpr float kShifter = 0x1.8p+23f;
+  constexpr float k32Log2e = 0x1.715476p+5f;
+  constexpr float kC1 = 0x1.62ep-6f, kC2 = 0x1.0bfbe8p-20f, kC3 = 0x1.cf79acp-45f;
+  const float tt = __fmaf_rn(x.h, k32Log2e, kShifter);
+  const float nf = __fsub_rn(tt, kShifter);
+  const int n = __float_as_int(tt) - __float_as_int(kShifter);
+  const float r1 = __fmaf_rn(-nf, kC1, x.h);  // exact: n C1 lies within a factor 2 of x.h
+  const FF pc2 = two_prod(-nf, kC2);
+  FF r = two_sum(r1, pc2.h);
+  r = two_sum(r.h, __fadd_rn(r.l, __fadd_rn(pc2.l, __fmaf_rn(-nf, kC3, x.l))));
+  const FF sq = two_prod(r.h, r.h);
+  const float sql = __fmaf_rn(__fmul_rn(2.0f, r.h), r.l, sq.l);
+  const float poly = __fmaf_rn(__fmaf_rn(r.h, 0x1.111112p-7f, 0x1.555556p-5f), r.h, 0x1.555556p-3f);
+  const float t3 = __fmul_rn(__fmul_rn(sq.h, r.h), poly);
+  const FF e1 = fast_two_sum(1.0f, r.h);
+  const FF e2 = two_sum(e1.h, __fmul_rn(0.5f, sq.h));
+  const float el = __fadd_rn(__fadd_rn(e1.l, e2.l), __fadd_rn(r.l, __fmaf_rn(0.5f, sql, t3)));
+  const FF er = fast_two_sum(e2.h, el);
+  const int j = n & 31;
+  const int m = n >> 5;  // n >= -4020: m >= -126
+  const FF zp = ff_mul(er, FF{kExp2Hi[j], kExp2Lo[j]});
+  const float scale = __int_as_float((m + 127) << 23);
+  // d = 1 + z (z below 2^-24 only touches the low part)
+  FF d = fast_two_sum(1.0f, __fmul_rn(zp.h, scale));
+  d.l = __fadd_rn(d.l, __fmul_rn(zp.l, scale));
+  const FF num = neg ? ff_mul(y, zp) : y;
+  // 1/d.h for d.h in [1, 2]: the hardware approximation and one Newton step;
+  // q1 = num.h / d.h to a few ulp, so num.h - q1 d.h is exact (two_prod and
+  // a subtraction within a factor 2) and q2 = res rc carries the rest
+  float rc;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(d.h));
+  rc = __fmaf_rn(rc, __fmaf_rn(-d.h, rc, 1.0f), rc);
+  const float q1 = __fmul_rn(num.h, rc);
+  const FF pq = two_prod(q1, d.h);
+  const float res = __fadd_rn(__fsub_rn(__fsub_rn(num.h, pq.h), pq.l), __fsub_rn(num.l, __fmul_rn(q1, d.l)));
+  const FF s = two_sum(q1, __fmul_rn(res, rc));
+  if (s.h == 0.0f) return -1;
+  // rounding of s.h + s.l to bf16
+  const uint32_t sb = __float_as_uint(s.h);
+  const float ah = __uint_as_float(sb & 0x7FFFFFFFu);
+  const float al = (sb >> 31) ? -s.l : s.l;
+  const uint32_t tb = sb & 0x7FFF0000u;
+  const float mid = __uint_as_float(tb | 0x8000u);
+  const float diff = __fadd_rn(__fsub_rn(ah, mid), al);  // ah - mid is exact
+  // the conv error's effect on the decided quotient: slope dy, with
+  // |SiLU'| <= 1.1 for y >= 0 and <= sigma + |SiLU| + 2 dy below; for y < 0
+  // the quotient is SiLU 2^-m, so its share is (z'/d + |quotient| + 2 dy 2^-m) dy
+  const float slope = neg ? __fmul_rn(zp.h, rc) * 1.001f + ah + 2.0f * __fmul_rn(dy, __int_as_float((127 - m) << 23))
+                          : 1.1f;
+  const float e = __fmaf_rn(0x1p-36f, ah, __fmaf_rn(__fmul_rn(slope, 1.001f), dy, 0x1p-140f));
+  if (!(fabsf(diff) > e)) return -1;
+  uint32_t code = (tb >> 16) + (diff > 0.0f ? 1u : 0u);  // magnitude bits of the unscaled code
+  if (neg) code += static_cast<uint32_t>(m) << 7;        // times 2^m: exponent field of bf16 (m <= 0)
+  return static_cast<int>(code | ((sb >> 16) & 0x8000u));
+}
+
+// Tier 3: the definition in fp64.  Every product of a bf16 input and a bf16
+// or fp32 weight is exact in double; the sum runs in tap order from +0; the
+// result is rounded once to bf16 (nearest even, subnormal quantum 2^-133).
+static __device__ __noinline__ uint32_t conv_code_f64(float w0, float w1, float w2, float w3, float x0, float x1, float x2,
+                                               float x3) {
+  double y = 0.0;
+  y += static_cast<double>(w0) * static_cast<double>(x0);
+  y += static_cast<double>(w1) * static_cast<double>(x1);
+  y += static_cast<double>(w2) * static_cast<double>(x2);
+  y += static_cast<double>(w3) * static_cast<double>(x3);
+  const double s = y / (1.0 + exp(-y));
+  const double a = fabs(s);
+  if (a == 0.0) return signbit(s) ? 0x8000u : 0u;
+  int e2;
+  (void)frexp(a, &e2);                                   // a = f 2^e2, f in [1/2, 1)
+  const double q = ldexp(1.0, max(e2 - 8, -133));       // bf16 quantum at a
+  const double r = rint(a / q) * q;                      // nearest even multiple: at most 8 significant bits
+  const uint32_t bits = __float_as_uint(static_cast<float>(r)) >> 16;
+  return bits | (signbit(s) ? 0x8000u : 0u);
+}
+
+// The code of one (channel, token) that tier 1 left doubtful.
+static __device__ __noinline__ uint32_t conv_code_exact(float w0, float w1, float w2, float w3, float x0, float x1, float x2,
+                                                 float x3) {
+  const int c = conv_code_ff(w0, w1, w2, w3, x0, x1, x2, x3);
+  return c >= 0 ? static_cast<uint32_t>(c) : conv_code_f64(w0, w1, w2, w3, x0, x1, x2, x3);
+}
+
+}  // namespace exact_conv
 
 // ----------------------------------------------------------------------------
 // KDA gate ("vLLM/vllm/models/kimi_k3/nvidia/ops/recoverssm.py", _kda_gate)

@@ -25,13 +25,9 @@ struct VerifyParams {
   const int* qsl; const int* state_indices; const int* record_indices; const int* num_accepted_prev;
   int* workspace;
   float k_scale;  // K^-1/2
-  // Small-input copies of the verify.  act_mode 0: one bulk copy per 16-byte
-  // hull of each row segment (any 2-byte alignment).  Otherwise tensor copies
-  // (TMA tiles) fetch an item's q | k | v rows (1: with the gate rows, which
-  // then follow v in the same rows; 2: gate rows by tm_gate), its conv taps
-  // (tm_conv) and conv weights (tm_w), built by the host for this call.
-  int act_mode;
-  CUtensorMap tm_act, tm_gate, tm_conv, tm_w;
+  // the conv pass's output: per (request, head) item a block of [Q][2K] bf16
+  // rows q | v, then [Q][2K] rows k | raw gate
+  uint16_t* scratch;
   // fp32 state pool [slots][H V][K] in K-slices of 32 (128-byte swizzle), for
   // the tensor-core path of the verify
   CUtensorMap tm_state;

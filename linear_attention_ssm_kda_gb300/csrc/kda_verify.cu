@@ -4,7 +4,12 @@
 // (_kda_recoverssm_verify_kernel with _kda_recurrent_step and _kda_gate)
 // computes, with the short causal conv of
 // "vllm.models.kimi_k3.nvidia.recoverssm.kernels" (CuteRecoverSSMVerify:
-// conv fused into the verify, rolled conv state of Q + W - 2 taps) in front.
+// rolled conv state of Q + W - 2 taps) in front.  Two launches per layer:
+//   conv_kernel    one CTA per (request, head): the conv + SiLU codes of the
+//                  head's q, k and v channels, correctly rounded to bf16, and
+//                  the rolled conv state; the codes go, with the raw gate
+//                  rows, into the item's block of the caller's scratch;
+//   verify_kernel  the verify proper, below.
 //
 // Math.  The window is applied in closed form rather than step by step.
 // With D_t = prod_{j<=t} e^{g_j} (per key channel),
@@ -15,25 +20,21 @@
 // o = S q^ expanded: the checkpoint S0 is read once (2n FMAs per element) and
 // never written (except by the fold variant, which writes the folded state).
 //
-// Schedule.  One persistent CTA per SM walks the (request, head) items
-// blockIdx.x + i * gridDim.x (local index i) with four roles that meet only
-// at mbarrier rings in shared memory, so the stages of consecutive items
-// overlap:
+// Schedule of the verify kernel.  One persistent CTA per SM walks the
+// (request, head) items blockIdx.x + i * gridDim.x (local index i) with four
+// roles that meet only at mbarrier rings in shared memory, so the stages of
+// consecutive items overlap:
 //   inputs (1 warp)  reads request metadata 32 items per round trip and
-//                    copies each item's small inputs into a ring: TMA tiles
-//                    of its q | k | v (| gate) rows, conv taps and conv
-//                    weights when they are 16-byte aligned, otherwise bulk
-//                    copies of the 16-byte hulls of each row segment (rows
-//                    may start anywhere); dt_bias by a bulk copy;
+//                    copies each item's rows of the conv pass's block
+//                    (q | v, then k | gate) and its head's dt_bias into a
+//                    ring of small slots (bulk copies);
 //   state (1 warp)   streams each live item's 64 KB fp32 state as eight row
 //                    chunks into a ring of chunk slots, running ahead of the
 //                    arithmetic by two to three items;
-//   prep (6 warps)   conv + SiLU of two channels per thread over the window
-//                    (the bf16 codes, the key record, the rolled conv taps
-//                    stored straight to the slot), then one key channel per
-//                    thread: the gates and gate record, the norms and the
-//                    closed-form operands X_t, Y_t, M, N, handed on through a
-//                    ring of operand slots;
+//   prep (6 warps)   one key channel per thread: the key / gate record (one
+//                    bulk store of the block's k | gate rows), the gates,
+//                    the norms and the closed-form operands X_t, Y_t, M, N,
+//                    handed on through a ring of operand slots;
 //   gemv (8 warps)   each on its own row chunk of the state: P | R with
 //                    packed fp32x2 FMAs, then the corrections and outputs of
 //                    its rows.
@@ -47,7 +48,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "kda_device.cuh"
@@ -57,7 +58,7 @@ namespace kda {
 namespace {
 
 constexpr int kConvWidth = 4;
-constexpr int kPrepWarps = 6;  // two conv channels per thread, then one key channel per thread
+constexpr int kPrepWarps = 6;  // one key channel per thread (K = 128: four of them busy)
 constexpr int kGemvWarps = 8;  // one state row chunk (16 rows at K = 128) each
 constexpr int kPrepConvThreads = 32 * kPrepWarps;
 constexpr int kBarPrep = 1;
@@ -103,7 +104,6 @@ struct OpMeta {
 
 template <int KD, int QMAX, int VAR>
 struct Layout {
-  static_assert(7 * QMAX + 10 <= 96, "small-input copies per item exceed three per lane");
   // Tensor-core instantiation (K = 128, windows of 4 or 8 tokens): the state
   // streams as K-slices of 32 (128 rows x 128 bytes, 128-byte swizzle) and the
   // products S0 [X | Y] come from tcgen05 MMAs; otherwise CUDA-core gemv warps.
@@ -114,15 +114,12 @@ struct Layout {
   static constexpr int kThreads = 32 * (kTC ? kMmaWarp + 1 : 2 + kPrepWarps + kGemvWarps);
   static constexpr int RW = KD / kGemvWarps;  // state rows per gemv warp (one chunk)
   static constexpr int kChunk = kTC ? 128 * 32 * 4 : RW * KD * 4;  // bytes per state unit (chunk or K-slice)
-  static constexpr int kLcMax = QMAX + kConvWidth - 2;
-  static constexpr int kSeg = KD * 2 + 16;    // hull of one row segment
   static constexpr int kNumSmall = QMAX <= 4 ? 3 : 2;  // small-input ring
-  // small slot
-  static constexpr int kAct = ru(int(sizeof(SmallMeta<QMAX>)), 128);  // [QMAX][3] hulls
-  static constexpr int kGate = ru(kAct + QMAX * 3 * kSeg, 128);       // [QMAX] hulls
-  static constexpr int kConv = ru(kGate + QMAX * kSeg, 128);           // the head's conv taps
-  static constexpr int kW = ru(kConv + 3 * KD * kLcMax * 2, 128);      // [3][KD][W] weights
-  static constexpr int kDt = ru(kW + 3 * KD * kConvWidth * 4, 128);    // [KD] dt_bias
+  // small slot: the item's rows of the conv pass's block (q | v rows, then
+  // k | gate rows, [QMAX][2K] bf16 each) and its head's dt_bias
+  static constexpr int kQV = ru(int(sizeof(SmallMeta<QMAX>)), 128);
+  static constexpr int kKG = kQV + QMAX * 2 * KD * 2;
+  static constexpr int kDt = kKG + QMAX * 2 * KD * 2;                  // [KD] dt_bias
   // fold variant: the pending records of the item, [QMAX][2K] bf16 key/gate
   // and [QMAX][V] fp32 corrections (V == K)
   static constexpr int kFoldKg = ru(kDt + KD * 4, 128);
@@ -149,15 +146,12 @@ struct Layout {
   // prep runs up to two items ahead of the gemv team; on the tensor-core path
   // an item's slot is also held until its readout, one item later
   static constexpr int kNumOp = kTC ? (QMAX <= 4 ? 4 : 3) : QMAX <= 4 ? 3 : 2;
-  // per-item scratch of the prep team
-  static constexpr int kXs = 2 * QMAX * KD * 4;                        // [2][QMAX][KD] q | k conv outputs
   // per-warp scratch
   static constexpr int kRedPerWarp = kTC ? 0 : 2 * QMAX * RW;         // floats
   static constexpr int kFoldIdx = 2 * QMAX + QMAX * QMAX;  // fold variant: |k_u|^2 of the pending keys
   static constexpr int kPart = ru(kFoldIdx + (kFold ? QMAX : 0), 32);         // reduced values per prep warp
-  static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kXs + kGemvWarps * kRedPerWarp * 4 +
-                                kPrepWarps * kPart * 4 + 32 + (2 * kNumSmall + 2 * kNumOp + 4) * 8 +
-                                (kTC ? 1024 : 0);
+  static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kGemvWarps * kRedPerWarp * 4 +
+                                kPrepWarps * kPart * 4 + 32 + (2 * kNumSmall + 2 * kNumOp + 4) * 8 + (kTC ? 1024 : 0);
   static constexpr int kBarsPerChunk = kTC ? 4 : 2;
   static constexpr int kChunkFit = (kSmemLimit - kFixed - 64 * kBarsPerChunk * 8) / kChunk;
   static constexpr int kNumChunk = kChunkFit > 64 ? 64 : kChunkFit;
@@ -165,8 +159,7 @@ struct Layout {
   static constexpr int oChunks = 0;
   static constexpr int oSmall = oChunks + kNumChunk * kChunk;
   static constexpr int oOp = ru(oSmall + kNumSmall * kSmall, kTC ? 1024 : 128);
-  static constexpr int oXs = oOp + kNumOp * kOp;
-  static constexpr int oRed = oXs + kXs;
+  static constexpr int oRed = oOp + kNumOp * kOp;
   static constexpr int oPart = oRed + kGemvWarps * kRedPerWarp * 4;
   static constexpr int oMisc = oPart + kPrepWarps * kPart * 4;  // int[8]
   static constexpr int oBars = ru(oMisc + 32, 8);
@@ -266,114 +259,127 @@ __device__ __forceinline__ ItemMeta<QMAX> decode_item(const VerifyParams& p, int
   return m;
 }
 
-// Byte offset of a row segment inside its 16-byte-aligned hull.
-__device__ __forceinline__ int hull_offset(const void* src) {
-  return static_cast<int>(reinterpret_cast<uintptr_t>(src) & 15);
-}
-
-// The q-th bulk copy of a live item's small inputs: source, shared-memory
-// destination and size (the 16-byte hull of the region).  Copies are, in
-// order: 3n activation row segments (token t, group g), n gate row segments,
-// the head's conv taps (3 blocks dim-first, 3 (Q+W-2) rows seq-first), three
-// conv-weight blocks and dt_bias.  Returns false past the last copy.
-template <int KD, int QMAX, bool DF, int VAR>
-__device__ __forceinline__ bool small_copy(const VerifyParams& p, int q, int n, int bos, long long s, int h,
-                                           unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
-  using Lay = Layout<KD, QMAX, VAR>;
-  const long long HK = static_cast<long long>(p.H) * KD;
-  const int Lc = p.Q + kConvWidth - 2;
-  const unsigned char* ptr;
-  int len;
-  if (q < 3 * n) {
-    const int t = q / 3, g = q - 3 * (q / 3);
-    ptr = reinterpret_cast<const unsigned char*>(p.mixed_qkv + static_cast<long long>(bos + t) * p.qkv_stride +
-                                                 g * HK + static_cast<long long>(h) * KD);
-    *dst = sl + Lay::kAct + q * Lay::kSeg;
-    len = KD * 2;
-  } else if (q < 4 * n) {
-    const int t = q - 3 * n;
-    ptr = reinterpret_cast<const unsigned char*>(p.raw_gate + static_cast<long long>(bos + t) * p.gate_stride +
-                                                 static_cast<long long>(h) * KD);
-    *dst = sl + Lay::kGate + t * Lay::kSeg;
-    len = KD * 2;
-  } else {
-    q -= 4 * n;
-    const int nconv = DF ? 3 : 3 * Lc;
-    const uint16_t* cs = p.conv_state + s * p.conv_slot_stride;
-    if (q < nconv) {
-      if (DF) {
-        ptr = reinterpret_cast<const unsigned char*>(cs + (q * HK + static_cast<long long>(h) * KD) * Lc);
-        *dst = sl + Lay::kConv + q * KD * Lc * 2;
-        len = KD * Lc * 2;
-      } else {
-        const int j = q / 3, g = q - 3 * (q / 3);
-        ptr = reinterpret_cast<const unsigned char*>(cs + j * 3 * HK + g * HK + static_cast<long long>(h) * KD);
-        *dst = sl + Lay::kConv + q * KD * 2;
-        len = KD * 2;
-      }
-    } else if (q < nconv + 3) {
-      const int g = q - nconv;
-      const int wb = p.conv_weight_fp32 ? 4 : 2;
-      ptr = static_cast<const unsigned char*>(p.conv_weight) + (g * HK + static_cast<long long>(h) * KD) * kConvWidth * wb;
-      *dst = sl + Lay::kW + g * KD * kConvWidth * wb;
-      len = KD * kConvWidth * wb;
-    } else if (q == nconv + 3) {
-      ptr = reinterpret_cast<const unsigned char*>(p.dt_bias + static_cast<long long>(h) * KD);
-      *dst = sl + Lay::kDt;
-      len = KD * 4;
-    } else {
-      return false;
+// ---------------------------------------------------------------- conv pass
+//
+// The short causal conv in front of the verify, as its own launch: one CTA
+// per (request, head) item.  Per channel it reads the W - 1 stored
+// taps from tap a - 1 and the window's inputs, evaluates the bf16 codes of
+// SiLU(conv) (tier 1 of kda_device.cuh; the rare codes it leaves in doubt go
+// to the exact tiers, out of line), and rolls the conv state in place
+// (taps 0 .. W-3+n <- seq[1 .. W-2+n], later taps untouched).  The codes go,
+// with the raw gate rows, into the item's block of the caller's scratch:
+// [Q][2K] bf16 rows q | v, then [Q][2K] rows k | raw gate, rows t < n
+// written.  The second half is the item's key / gate record verbatim.
+// Null items, empty windows and items with bad metadata are skipped here;
+// the verify kernel reports the latter.
+template <int QMAX>
+__device__ __forceinline__ void channel_codes(const float (&w)[kConvWidth], const uint16_t (&seq)[kConvWidth + QMAX],
+                                              int n, float e0, uint16_t (&y)[QMAX]) {
+  uint32_t doubt = 0;
+#pragma unroll
+  for (int pr = 0; pr < (QMAX + 1) / 2; ++pr) {
+    const int t = 2 * pr;
+    y[t] = 0;
+    if (t + 1 < QMAX) y[t + 1] = 0;
+    if (t < n) {
+      const float xa[kConvWidth] = {bf16_to_f32(seq[t]), bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]),
+                                    bf16_to_f32(seq[t + 3])};
+      const float xb[kConvWidth] = {bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]), bf16_to_f32(seq[t + 3]),
+                                    bf16_to_f32(seq[t + 4])};
+      uint32_t d;
+      const uint32_t yy = conv_silu_bf16x2(w, xa, xb, e0, &d);
+      y[t] = static_cast<uint16_t>(yy & 0xffffu);
+      if (t + 1 < QMAX) y[t + 1] = static_cast<uint16_t>(yy >> 16);
+      doubt |= d << t;
     }
   }
-  const int off = hull_offset(ptr);
-  *src = ptr - off;
-  *bytes = static_cast<uint32_t>((off + len + 15) & ~15);
-  return true;
+  doubt &= (1u << n) - 1u;
+  if (doubt) {  // a few codes in 10^4
+#pragma unroll
+    for (int t = 0; t < QMAX; ++t)
+      if ((doubt >> t) & 1u)
+        y[t] = static_cast<uint16_t>(exact_conv::conv_code_exact(w[0], w[1], w[2], w[3], bf16_to_f32(seq[t]),
+                                                                 bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]),
+                                                                 bf16_to_f32(seq[t + 3])));
+  }
 }
 
-// The same copies for the dim-first conv layout when they fit one per lane
-// (4n + 7 <= 32): every lane computes its copy without branches, by
-// selecting a base, a row, a row stride and a column per kind of copy.
-// Kinds by lane q: activation (t = q / 3, g = q % 3) for q < 3n, gate
-// (t = q - 3n) for q < 4n, conv taps of group q - 4n, conv weights of group
-// q - 4n - 3, dt_bias at q = 4n + 6.  Returns false for lanes past the last copy.
-template <int KD, int QMAX, int VAR>
-__device__ __forceinline__ bool small_copy_lane(const VerifyParams& p, int q, int n, int bos, long long s, int h,
-                                                unsigned char* sl, const void** src, void** dst, uint32_t* bytes) {
-  using Lay = Layout<KD, QMAX, VAR>;
+template <int KD, int QMAX, bool DF>
+__global__ void __launch_bounds__(KD) conv_kernel(const __grid_constant__ VerifyParams p) {
+  // Thread k takes channel k of each of q, k and v.  Two dependent memory
+  // round trips: the item's metadata with the channels' weights, then every
+  // tap, input and gate value of the window; then the codes and the stores.
+  const int it = static_cast<int>(blockIdx.x);
+  const int k = static_cast<int>(threadIdx.x);
+  const int h = it - (it / p.H) * p.H;
   const long long HK = static_cast<long long>(p.H) * KD;
+  const long long c0 = static_cast<long long>(h) * KD + k;  // channel of group g: c0 + g HK
+  float w[3][kConvWidth];
+#pragma unroll
+  for (int g = 0; g < 3; ++g) {
+    if (p.conv_weight_fp32) {
+      const float4 wv = __ldg(reinterpret_cast<const float4*>(p.conv_weight) + c0 + g * HK);
+      w[g][0] = wv.x; w[g][1] = wv.y; w[g][2] = wv.z; w[g][3] = wv.w;
+    } else {
+      const uint2 wv = __ldg(reinterpret_cast<const uint2*>(p.conv_weight) + c0 + g * HK);
+      w[g][0] = bf16_to_f32(wv.x & 0xffff); w[g][1] = bf16_to_f32(wv.x >> 16);
+      w[g][2] = bf16_to_f32(wv.y & 0xffff); w[g][3] = bf16_to_f32(wv.y >> 16);
+    }
+  }
+  const ItemMeta<QMAX> im = decode_item<QMAX>(p, it, true, false);
+  if (!(im.flags & kLive) || im.n <= 0) return;
+  const int n = im.n;
   const int Lc = p.Q + kConvWidth - 2;
-  const int wb = p.conv_weight_fp32 ? 4 : 2;
-  const int n3 = 3 * n, n4 = 4 * n;
-  const bool is_act = q < n3, is_gate = !is_act && q < n4, is_conv = q >= n4 && q < n4 + 3;
-  const bool is_w = q >= n4 + 3 && q < n4 + 6, is_dt = q == n4 + 6;
-  const int t_act = q / 3;
-  const int g = is_act ? q - 3 * t_act : (is_conv ? q - n4 : q - n4 - 3);
-  const long long hk = static_cast<long long>(h) * KD;
-  const unsigned char* base = is_act    ? reinterpret_cast<const unsigned char*>(p.mixed_qkv)
-                              : is_gate ? reinterpret_cast<const unsigned char*>(p.raw_gate)
-                              : is_conv ? reinterpret_cast<const unsigned char*>(p.conv_state)
-                              : is_w    ? static_cast<const unsigned char*>(p.conv_weight)
-                                        : reinterpret_cast<const unsigned char*>(p.dt_bias);
-  const long long row = is_act ? bos + t_act : (is_gate ? bos + q - n3 : (is_conv ? s : 0));
-  const long long row_bytes = is_act ? p.qkv_stride * 2 : (is_gate ? p.gate_stride * 2 : (is_conv ? p.conv_slot_stride * 2 : 0));
-  const long long col = is_act ? (g * HK + hk) * 2
-                      : is_gate ? hk * 2
-                      : is_conv ? (g * HK + hk) * Lc * 2
-                      : is_w    ? (g * HK + hk) * kConvWidth * wb
-                                : hk * 4;
-  const int dst_off = is_act    ? Lay::kAct + q * Lay::kSeg
-                      : is_gate ? Lay::kGate + (q - n3) * Lay::kSeg
-                      : is_conv ? Lay::kConv + g * KD * Lc * 2
-                      : is_w    ? Lay::kW + g * KD * kConvWidth * wb
-                                : Lay::kDt;
-  const int len = (is_act || is_gate) ? KD * 2 : (is_conv ? KD * Lc * 2 : (is_w ? KD * kConvWidth * wb : KD * 4));
-  const unsigned char* ptr = base + row * row_bytes + col;
-  const int off = hull_offset(ptr);
-  *src = ptr - off;
-  *dst = sl + dst_off;
-  *bytes = static_cast<uint32_t>((off + len + 15) & ~15);
-  return is_act || is_gate || is_conv || is_w || is_dt;
+  uint16_t* cs = p.conv_state + im.s * p.conv_slot_stride;
+  const uint16_t* x = p.mixed_qkv + static_cast<long long>(im.bos) * p.qkv_stride;
+  // seq[g] = the W - 1 stored taps from tap a - 1, then the window (zero past n)
+  uint16_t seq[3][kConvWidth + QMAX];
+  uint16_t gate[QMAX];
+#pragma unroll
+  for (int g = 0; g < 3; ++g) {
+    const long long c = c0 + g * HK;
+#pragma unroll
+    for (int j = 0; j < kConvWidth - 1; ++j)
+      seq[g][j] = DF ? cs[c * Lc + im.a - 1 + j] : cs[static_cast<long long>(im.a - 1 + j) * 3 * HK + c];
+#pragma unroll
+    for (int t = 0; t < QMAX; ++t)
+      seq[g][kConvWidth - 1 + t] = t < n ? __ldg(x + static_cast<long long>(t) * p.qkv_stride + c) : uint16_t(0);
+    seq[g][kConvWidth - 1 + QMAX] = 0;
+  }
+#pragma unroll
+  for (int t = 0; t < QMAX; ++t)
+    gate[t] = t < n ? __ldg(p.raw_gate + static_cast<long long>(im.bos + t) * p.gate_stride + c0) : uint16_t(0);
+  // the codes: a bf16 weight times a bf16 input is exact in fp32; an fp32 weight's product rounds
+  const float e0 = p.conv_weight_fp32 ? 1.0f : 0.0f;
+  uint16_t y[3][QMAX];
+#pragma unroll
+  for (int g = 0; g < 3; ++g) channel_codes<QMAX>(w[g], seq[g], n, e0, y[g]);
+  // the item's block: q at [t][k], v at [t][K + k], k at [Q + t][k], gate at [Q + t][K + k]
+  uint16_t* blk = p.scratch + static_cast<long long>(it) * (4LL * p.Q * KD) + k;
+  uint16_t* kgr = blk + 2LL * p.Q * KD;
+#pragma unroll
+  for (int t = 0; t < QMAX; ++t) {
+    if (t < n) {
+      blk[t * 2 * KD] = y[0][t];
+      blk[t * 2 * KD + KD] = y[2][t];
+      kgr[t * 2 * KD] = y[1][t];
+      kgr[t * 2 * KD + KD] = gate[t];
+    }
+  }
+  // the rolled taps: 0 .. W-3+n <- seq[1 .. W-2+n], later taps untouched
+#pragma unroll
+  for (int g = 0; g < 3; ++g) {
+    const long long c = c0 + g * HK;
+#pragma unroll
+    for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
+      if (j < kConvWidth - 2 + n) {
+        if (DF)
+          cs[c * Lc + j] = seq[g][j + 1];
+        else
+          cs[static_cast<long long>(j) * 3 * HK + c] = seq[g][j + 1];
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- inputs warp
@@ -391,7 +397,7 @@ __device__ __forceinline__ void fold_copies(const VerifyParams& p, unsigned char
   bulk_g2s(sl + Lay::kFoldC, c, static_cast<uint32_t>(m) * KD * 4, bar);
 }
 
-template <int KD, int QMAX, bool DF, int VAR>
+template <int KD, int QMAX, int VAR>
 __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
   using Lay = Layout<KD, QMAX, VAR>;
   Bars<KD, QMAX, VAR> bars(smem);
@@ -427,9 +433,7 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
     for (int j = 0; j < count && ok; ++j) {
       const int i = i0 + j;
       const int jflags = __shfl_sync(0xffffffffu, im.flags, j);
-      const int jbos = __shfl_sync(0xffffffffu, im.bos, j);
       const int jn = __shfl_sync(0xffffffffu, im.n, j);
-      const long long js = shfl_ll(im.s, j);
       const int jh = __shfl_sync(0xffffffffu, im.h, j);
       const int jfm = Lay::kFold ? __shfl_sync(0xffffffffu, im.fold_m, j) : 0;
       const long long jfr = Lay::kFold ? shfl_ll(im.fold_r, j) : 0;
@@ -441,55 +445,24 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
       unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
       if (lane == j) *reinterpret_cast<SmallMeta<QMAX>*>(sl) = own;
       __syncwarp();  // orders lane j's header before lane 0's arrival on sm_full
-      if ((jflags & kLive) && p.act_mode != 0) {
-        // four or five tensor / bulk copies, all from lane 0
+      if (jflags & kLive) {
+        // the item's rows of the conv pass's block (q | v, then k | gate), its
+        // head's dt_bias and, in the fold variant, its pending records: a few
+        // bulk copies from lane 0
         if (lane == 0) {
-          const int Lc = p.Q + kConvWidth - 2;
-          const int wb = p.conv_weight_fp32 ? 4 : 2;
-          const int G = p.act_mode == 1 ? 4 : 3;
-          const uint32_t total = KD * G * p.Q * 2 + (p.act_mode == 2 ? KD * p.Q * 2 : 0) + 3 * KD * Lc * 2 +
-                                 3 * KD * kConvWidth * wb + KD * 4 + fold_bytes;
+          const uint32_t rows = static_cast<uint32_t>(jn) * 2 * KD * 2;
           uint64_t* bar = &bars.sm_full[slot];
-          mbar_arrive_expect_tx(bar, total);
+          mbar_arrive_expect_tx(bar, 2 * rows + KD * 4 + fold_bytes);
           if (fold_bytes) fold_copies<KD, QMAX, VAR>(p, sl, jh, jfm, jfr, bar);
-          tma_load_3d(sl + Lay::kAct, &p.tm_act, jh * KD, 0, jbos, bar);
-          if (p.act_mode == 2) tma_load_2d(sl + Lay::kGate, &p.tm_gate, jh * KD, jbos, bar);
-          if (DF)
-            tma_load_4d(sl + Lay::kConv, &p.tm_conv, 0, jh * KD * Lc / 128, 0, static_cast<int>(js), bar);
-          else
-            tma_load_4d(sl + Lay::kConv, &p.tm_conv, jh * KD, 0, 0, static_cast<int>(js), bar);
-          tma_load_3d(sl + Lay::kW, &p.tm_w, 0, jh * KD * kConvWidth / 128, 0, bar);
+          if (rows) {  // (a fold-only item has no window)
+            const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            const uint16_t* blk = p.scratch + static_cast<long long>(it) * (4LL * p.Q * KD);
+            bulk_g2s(sl + Lay::kQV, blk, rows, bar);
+            bulk_g2s(sl + Lay::kKG, blk + 2LL * p.Q * KD, rows, bar);
+          }
           bulk_g2s(sl + Lay::kDt, p.dt_bias + static_cast<long long>(jh) * KD, KD * 4, bar);
         }
         __syncwarp();
-      } else if (jflags & kLive) {
-        // at most 7 QMAX + 10 copies, three per lane; the barrier expects every
-        // byte before the first copy can land
-        const void* src[3];
-        void* dst[3];
-        uint32_t bytes[3] = {0, 0, 0};
-        uint32_t mine = 0;
-        if (DF && 4 * QMAX + 7 <= 32) {  // one copy per lane, computed without branches
-          if (!small_copy_lane<KD, QMAX, VAR>(p, lane, jn, jbos, js, jh, sl, &src[0], &dst[0], &bytes[0]))
-            bytes[0] = 0;
-          mine = bytes[0];
-        } else {
-#pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            if (!small_copy<KD, QMAX, DF, VAR>(p, lane + 32 * c, jn, jbos, js, jh, sl, &src[c], &dst[c], &bytes[c]))
-              bytes[c] = 0;
-            mine += bytes[c];
-          }
-        }
-        mine = __reduce_add_sync(0xffffffffu, mine) + fold_bytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars.sm_full[slot], mine);
-          if (fold_bytes) fold_copies<KD, QMAX, VAR>(p, sl, jh, jfm, jfr, &bars.sm_full[slot]);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 3; ++c)
-          if (bytes[c]) bulk_g2s(dst[c], src[c], bytes[c], &bars.sm_full[slot]);
       } else {
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.sm_full[slot]);
@@ -555,115 +528,7 @@ __device__ __forceinline__ void reduce_scatter_stage(float* acc, int mask, bool 
   }
 }
 
-// Conv + SiLU of one channel (group g of q | k | v, key index k) over the
-// window, in three steps so that a thread's channels run interleaved:
-// conv_load reads the weights, the W - 1 stored taps and the window inputs
-// (zero past n); conv_pairs evaluates NP token pairs on the packed fp32x2 unit
-// without branches; conv_roll stores the rolled taps to the slot in global
-// memory (taps 0 .. W-3+n <- seq[1 .. W-2+n]; later taps are left as they are).
-template <int QMAX>
-struct ConvIn {
-  float w[kConvWidth];
-  uint16_t seq[kConvWidth - 1 + QMAX + 1];
-};
-
-template <int KD, int QMAX, bool DF, int VAR>
-__device__ __forceinline__ void conv_load(const VerifyParams& p, const unsigned char* sl, int g, int k, int n, int a,
-                                          int Lc, uint32_t act_lo, ConvIn<QMAX>& in) {
-  using Lay = Layout<KD, QMAX, VAR>;
-  const uint16_t* conv = reinterpret_cast<const uint16_t*>(sl + Lay::kConv);
-  if (p.conv_weight_fp32) {
-    const float4 wv = reinterpret_cast<const float4*>(sl + Lay::kW)[g * KD + k];
-    in.w[0] = wv.x; in.w[1] = wv.y; in.w[2] = wv.z; in.w[3] = wv.w;
-  } else {
-    const uint2 wv = reinterpret_cast<const uint2*>(sl + Lay::kW)[g * KD + k];
-    in.w[0] = bf16_to_f32(wv.x & 0xffff); in.w[1] = bf16_to_f32(wv.x >> 16);
-    in.w[2] = bf16_to_f32(wv.y & 0xffff); in.w[3] = bf16_to_f32(wv.y >> 16);
-  }
-  in.seq[kConvWidth - 1 + QMAX] = 0;
-#pragma unroll
-  for (int j = 0; j < kConvWidth - 1; ++j)
-    in.seq[j] = DF ? conv[(g * KD + k) * Lc + a - 1 + j] : conv[((a - 1 + j) * 3 + g) * KD + k];
-#pragma unroll
-  for (int t = 0; t < QMAX; ++t) {
-    uint16_t x;
-    if (p.act_mode == 0) {
-      // the activation hull of (token t, group g) starts act_lo + 16-byte
-      // multiples before the segment: the segment's offset is its address mod 16
-      const uint32_t off = (act_lo + static_cast<uint32_t>(t) * static_cast<uint32_t>(p.qkv_stride) * 2u +
-                            static_cast<uint32_t>(g) * static_cast<uint32_t>(p.H) * KD * 2u) & 15u;
-      x = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + (t * 3 + g) * Lay::kSeg + off + 2 * k);
-    } else {  // tensor tile [t][q | k | v (| gate)][K]
-      const int G = p.act_mode == 1 ? 4 : 3;
-      x = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * G + g) * KD + k) * 2);
-    }
-    in.seq[kConvWidth - 1 + t] = t < n ? x : static_cast<uint16_t>(0);  // slots past n hold no token
-  }
-}
-
-template <int NP, int QMAX>
-__device__ __forceinline__ void conv_pairs(const ConvIn<QMAX>& in, uint16_t (&y)[QMAX]) {
-#pragma unroll
-  for (int t = 0; t < QMAX; ++t) y[t] = 0;
-#pragma unroll
-  for (int pr = 0; pr < NP; ++pr) {
-    const int t = 2 * pr;
-    const float xa[kConvWidth] = {bf16_to_f32(in.seq[t]), bf16_to_f32(in.seq[t + 1]), bf16_to_f32(in.seq[t + 2]),
-                                  bf16_to_f32(in.seq[t + 3])};
-    const float xb[kConvWidth] = {bf16_to_f32(in.seq[t + 1]), bf16_to_f32(in.seq[t + 2]),
-                                  bf16_to_f32(in.seq[t + 3]), bf16_to_f32(in.seq[t + 4])};
-    const uint32_t yy = conv_silu_bf16x2(in.w, xa, xb);
-    y[t] = static_cast<uint16_t>(yy & 0xffffu);
-    y[t + 1] = static_cast<uint16_t>(yy >> 16);
-  }
-}
-
-template <int KD, int QMAX, bool DF, int VAR>
-__device__ __forceinline__ void conv_roll(const VerifyParams& p, const ConvIn<QMAX>& in, int g, int k, int n, int Lc,
-                                          uint16_t* gconv, long long hk) {
-  const long long HK = static_cast<long long>(p.H) * KD;
-  const long long c = g * HK + hk + k;
-#pragma unroll
-  for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
-    if (j < kConvWidth - 2 + n) {
-      if (DF)
-        gconv[c * Lc + j] = in.seq[j + 1];
-      else
-        gconv[j * 3 * HK + c] = in.seq[j + 1];
-    }
-  }
-}
-
-// Both channels of a prep thread, their pairs interleaved: np = ceil(n / 2)
-// pairs each, the codes of tokens past n zeroed.
-template <int QMAX>
-__device__ __forceinline__ void conv_two(const ConvIn<QMAX>& in0, const ConvIn<QMAX>& in1, int n,
-                                         uint16_t (&y0)[QMAX], uint16_t (&y1)[QMAX]) {
-  const int np = (n + 1) >> 1;
-  if (QMAX <= 4) {
-    if (np <= 1) {
-      conv_pairs<1, QMAX>(in0, y0);
-      conv_pairs<1, QMAX>(in1, y1);
-    } else {
-      conv_pairs<(QMAX + 1) / 2, QMAX>(in0, y0);
-      conv_pairs<(QMAX + 1) / 2, QMAX>(in1, y1);
-    }
-  } else {
-    switch (np) {
-      case 1: conv_pairs<1, QMAX>(in0, y0); conv_pairs<1, QMAX>(in1, y1); break;
-      case 2: conv_pairs<2, QMAX>(in0, y0); conv_pairs<2, QMAX>(in1, y1); break;
-      case 3: conv_pairs<3, QMAX>(in0, y0); conv_pairs<3, QMAX>(in1, y1); break;
-      default: conv_pairs<(QMAX + 1) / 2, QMAX>(in0, y0); conv_pairs<(QMAX + 1) / 2, QMAX>(in1, y1); break;
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < QMAX; ++t) {
-    y0[t] = t < n ? y0[t] : static_cast<uint16_t>(0);
-    y1[t] = t < n ? y1[t] : static_cast<uint16_t>(0);
-  }
-}
-
-template <int KD, int QMAX, bool DF, int VAR>
+template <int KD, int QMAX, int VAR>
 __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatile int* misc) {
   using Lay = Layout<KD, QMAX, VAR>;
   constexpr int NREDP = Lay::kPart;  // |q_t|^2, |k_t|^2, raw M / N grid, padded to 32
@@ -671,13 +536,9 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
   Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   float* part = reinterpret_cast<float*>(smem + Lay::oPart);
-  float* xs = reinterpret_cast<float*>(smem + Lay::oXs);  // [2][QMAX][KD] q | k
   const int warp = pt >> 5;
   const int lane = pt & 31;
   const int nloc = local_items(p.B * p.H);
-  const int Lc = p.Q + kConvWidth - 2;
-  const uint32_t qkv_lo = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.mixed_qkv));
-  const uint32_t gate_lo = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.raw_gate));
   for (int i = 0; i < nloc; ++i) {
     const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
     const int h = it - (it / p.H) * p.H;
@@ -691,10 +552,9 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
     const SmallMeta<QMAX> m = *reinterpret_cast<const SmallMeta<QMAX>*>(sl);
     const bool live = ok && (m.flags & kLive);
     const int n = m.n;
-    const uint32_t hoff = static_cast<uint32_t>(h) * KD * 2u;
-    uint16_t* kg = p.key_gate + m.r * p.kg_stride + static_cast<long long>(h) * p.Q * 2 * KD;
+    const uint16_t* qv_rows = reinterpret_cast<const uint16_t*>(sl + Lay::kQV);  // [QMAX][2K] q | v
+    const uint16_t* kg_rows = reinterpret_cast<const uint16_t*>(sl + Lay::kKG);  // [QMAX][2K] k | gate
 
-    // ---- conv: channels pt and pt + 192 of the head's 3K (q | k | v) ----
     if (ok && (m.flags & kNull)) {  // null slot: zero outputs, nothing else
       for (int e = pt; e < n * KD; e += kPrepConvThreads) {
         const int t = e / KD;
@@ -702,78 +562,38 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       }
     }
     if (live && n > 0) {  // (a fold-only item of the fold variant has no window)
-      const uint32_t act_lo = qkv_lo + static_cast<uint32_t>(m.bos) * static_cast<uint32_t>(p.qkv_stride) * 2u + hoff;
-      uint16_t* gconv = p.conv_state + m.s * p.conv_slot_stride;
-      const long long hk = static_cast<long long>(h) * KD;
-      // channels c0 = pt and c1 = pt + 192 of the head's 3K (q | k | v)
-      const int c0 = pt, c1 = pt + kPrepConvThreads;
-      const bool has1 = c1 < 3 * KD;
-      const int g0 = c0 / KD, k0 = c0 - g0 * KD;
-      const int g1 = c1 / KD, k1 = c1 - g1 * KD;
-      ConvIn<QMAX> in0, in1;
-      conv_load<KD, QMAX, DF, VAR>(p, sl, g0, k0, n, m.a, Lc, act_lo, in0);
-      if (has1) {
-        conv_load<KD, QMAX, DF, VAR>(p, sl, g1, k1, n, m.a, Lc, act_lo, in1);
-      } else {
-#pragma unroll
-        for (int j = 0; j < kConvWidth; ++j) in1.w[j] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kConvWidth + QMAX; ++j) in1.seq[j] = 0;
+      // the key / gate record of the window is the block's k | gate rows as
+      // they are: one bulk store (its read of the slot is awaited before the
+      // slot is released)
+      if (pt == 0) {
+        bulk_s2g(p.key_gate + m.r * p.kg_stride + static_cast<long long>(h) * p.Q * 2 * KD, kg_rows,
+                 static_cast<uint32_t>(n) * 2 * KD * 2);
+        bulk_commit();
       }
-      uint16_t y0[QMAX], y1[QMAX];
-      conv_two<QMAX>(in0, in1, n, y0, y1);
-      conv_roll<KD, QMAX, DF, VAR>(p, in0, g0, k0, n, Lc, gconv, hk);
-      if (has1) conv_roll<KD, QMAX, DF, VAR>(p, in1, g1, k1, n, Lc, gconv, hk);
+      // v_t for the gemv team's solve
+      if (pt < KD) {
+        float* opv = reinterpret_cast<float*>(op + Lay::kOpV);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        if (cc == 1 && !has1) break;
-        const int g = cc == 0 ? g0 : g1;
-        const int k = cc == 0 ? k0 : k1;
-        const uint16_t(&y)[QMAX] = cc == 0 ? y0 : y1;
-        if (g < 2) {
-#pragma unroll
-          for (int t = 0; t < QMAX; ++t) xs[(g * QMAX + t) * KD + k] = bf16_to_f32(y[t]);
-          if (g == 1) {
-#pragma unroll
-            for (int t = 0; t < QMAX; ++t)
-              if (t < n) kg[t * 2 * KD + k] = y[t];  // key record: the bf16 conv output
-          }
-        } else {
-          float* opv = reinterpret_cast<float*>(op + Lay::kOpV);
-#pragma unroll
-          for (int t = 0; t < QMAX; ++t)
-            if (t < n) opv[t * KD + k] = bf16_to_f32(y[t]);
-        }
+        for (int t = 0; t < QMAX; ++t)
+          if (t < n) opv[t * KD + pt] = bf16_to_f32(qv_rows[t * 2 * KD + KD + pt]);
       }
     }
-    named_barrier(kBarPrep, kPrepConvThreads);
-    if (misc[kMiscPrepFail]) break;  // every prep thread sees the same flag here
 
-    // ---- gates, gate record and the per-channel partial sums: key channel k = pt ----
+    // ---- gates and the per-channel partial sums: key channel k = pt ----
     float qv[QMAX], kv[QMAX], eg[QMAX];
     if (live && pt < KD) {
       const int k = pt;
       const float dtb = reinterpret_cast<const float*>(sl + Lay::kDt)[k];
 #pragma unroll
       for (int t = 0; t < QMAX; ++t) {
-        qv[t] = xs[t * KD + k];  // zero past n
-        kv[t] = xs[(QMAX + t) * KD + k];
-        // every slot of the window is read (rows past n hold other tokens,
-        // zeros or stale bytes) and the gate of a missing token is discarded,
-        // so the QMAX gates evaluate side by side without branches
-        uint16_t rg;
-        if (p.act_mode == 0) {
-          const uint32_t goff =
-              (gate_lo + static_cast<uint32_t>(m.bos + t) * static_cast<uint32_t>(p.gate_stride) * 2u + hoff) & 15u;
-          rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + t * Lay::kSeg + goff + 2 * k);
-        } else if (p.act_mode == 1) {  // gate rows follow v in the q | k | v | gate tile
-          rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kAct + ((t * 4 + 3) * KD + k) * 2);
-        } else {
-          rg = *reinterpret_cast<const uint16_t*>(sl + Lay::kGate + (t * KD + k) * 2);
-        }
+        // every row of the window is read (rows past n hold stale bytes) and
+        // the values of a missing token are discarded by selects, so the
+        // QMAX gates evaluate side by side without branches
+        qv[t] = t < n ? bf16_to_f32(qv_rows[t * 2 * KD + k]) : 0.0f;
+        kv[t] = t < n ? bf16_to_f32(kg_rows[t * 2 * KD + k]) : 0.0f;
+        const uint16_t rg = kg_rows[t * 2 * KD + KD + k];
         const float e = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
         eg[t] = t < n ? e : 0.0f;
-        if (t < n) kg[t * 2 * KD + KD + k] = rg;  // gate record: bit copy
       }
       // vals: [t] |q_t|^2, [QMAX + t] |k_t|^2, [2QMAX + t QMAX + u] k_u D_{u+1..t} k_t (u < t),
       //       [2QMAX + u QMAX + t] k_u D_{u+1..t} q_t (u <= t); zero past n (qv = kv = 0 there).
@@ -838,7 +658,11 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       for (int v = 0; v < PER; ++v) part[warp * NREDP + lane * PER + v] = vals[v];
     }
     named_barrier(kBarPrep, kPrepConvThreads);
-    if (pt == 0) mbar_arrive(&bars.sm_empty[slot]);  // the small inputs are consumed
+    if (misc[kMiscPrepFail]) break;  // every prep thread sees the same flag here
+    if (pt == 0) {  // the small inputs are consumed (and read by the record store)
+      bulk_wait_read();
+      mbar_arrive(&bars.sm_empty[slot]);
+    }
 
     // ---- norms, the operands X_t = D_t k^_t, Y_t = D_t q^_t, M and N ----
     if (live && pt < KD) {
@@ -932,6 +756,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
     named_barrier(kBarPrep, kPrepConvThreads);
     if (pt == 0) mbar_arrive(&bars.op_full[oslot]);
   }
+  if (pt == 0) bulk_wait_all();  // the record stores have completed
   if (misc[kMiscPrepFail] && pt == 0) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
@@ -1362,9 +1187,9 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
   }
 }
 
-// Readout team (4 warps, warp q of the CTA's last warpgroup reads tensor-memory
-// lanes 32 q .. 32 q + 31): each lane owns one state row; it sums the hi and
-// lo columns into P_t | R_t and runs the row's solve.
+// Readout team (4 warps; warp w of the CTA reads tensor-memory lanes
+// 32 (w mod 4) .. 32 (w mod 4) + 31): each lane owns one state row; it sums
+// the hi and lo columns into P_t | R_t and runs the row's solve.
 template <int KD, int QMAX, int N, int VAR>
 __device__ __forceinline__ void tc_solve(const VerifyParams& p, const OpMeta<QMAX>& m, const unsigned char* op, int h,
                                          int row, const float* d) {
@@ -1449,7 +1274,9 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
   Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   const int lane = st & 31;
-  const int wq = st >> 5;
+  // tcgen05.ld reaches the tensor-memory lanes of the warp's quadrant of the
+  // CTA (warp index mod 4): this warp reads out rows 32 wq .. 32 wq + 31
+  const int wq = static_cast<int>(threadIdx.x >> 5) & 3;
   const int nloc = local_items(p.B * p.H);
   const uint32_t taddr = static_cast<uint32_t>(misc[kMiscTaddr]);
   uint32_t g = 0, live = 0;
@@ -1503,7 +1330,7 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
   }
 }
 
-template <int KD, int QMAX, bool DF, int VAR>
+template <int KD, int QMAX, int VAR>
 __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
   using Lay = Layout<KD, QMAX, VAR>;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -1553,14 +1380,14 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
   __syncthreads();
   if constexpr (Lay::kTC) tmem_fence_after();
   if (warp == 0) {
-    produce_inputs<KD, QMAX, DF, VAR>(p, smem, tid & 31, misc + kMiscAbort);
+    produce_inputs<KD, QMAX, VAR>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp == 1) {
     if constexpr (Lay::kTC)
       tc_produce_state<KD, QMAX, VAR>(p, smem, tid & 31, misc + kMiscAbort);
     else
       produce_state<KD, QMAX, VAR>(p, smem, tid & 31, misc + kMiscAbort);
   } else if (warp < 2 + kPrepWarps) {
-    prep<KD, QMAX, DF, VAR>(p, smem, tid - 64, misc);
+    prep<KD, QMAX, VAR>(p, smem, tid - 64, misc);
   } else if constexpr (Lay::kTC) {
     if (warp < kMmaWarp)
       tc_split<KD, QMAX, VAR>(p, smem, tid - 32 * (2 + kPrepWarps), misc);
@@ -1613,19 +1440,6 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor maps for the small inputs when every start and stride they need is
-// 16-byte aligned; otherwise act_mode stays 0 (per-segment hull copies).
-//   q | k | v (| gate): dims {HK, 3 or 4 groups, T}, box {K, groups, Q}, at
-//     {h K, 0, bos}; rows past T arrive as zeros;
-//   gate (separate): dims {HK, T}, box {K, Q}, at {h K, bos};
-//   conv taps, dim-first [slots][3HK][Lc]: dims {128, HK Lc / 128, 3, slots},
-//     box {128, K Lc / 128, 3, 1}, at {0, h K Lc / 128, 0, s};
-//     seq-first [slots][Lc][3HK]: dims {HK, 3, Lc, slots}, box {K, 3, Lc, 1},
-//     at {h K, 0, 0, s};
-//   conv weights [3HK][W]: dims {128, HK W / 128, 3}, box {128, K W / 128, 3},
-//     at {0, h K W / 128, 0}.
-// Every box lands in the layout the hull copies would give, except q | k | v
-// (| gate), which lands as [t][group][K].
 // The fp32 state pool for the tensor-core path, [slots][H K][K] with the slot
 // stride given: dims {K, H K, slots}, box {32, 128, 1} with the 128-byte
 // swizzle, at {32 kb, h K, s}: K-slice kb of head h's state.
@@ -1638,117 +1452,71 @@ bool build_state_map(VerifyParams& p, int KD) {
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-void build_tensor_maps(VerifyParams& p, int KD) {
-  p.act_mode = 0;
-  const cuuint64_t H = static_cast<cuuint64_t>(p.H), K = static_cast<cuuint64_t>(KD), HK = H * K;
-  const cuuint64_t T = static_cast<cuuint64_t>(p.T), Q = static_cast<cuuint64_t>(p.Q);
-  const cuuint64_t Lc = Q + kConvWidth - 2, W = kConvWidth;
-  const cuuint64_t wb = p.conv_weight_fp32 ? 4 : 2;
-  auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
-  if (!al16(p.mixed_qkv) || (p.qkv_stride * 2) % 16 != 0) return;
-  int mode;
-  if (p.raw_gate == p.mixed_qkv + 3 * HK && p.gate_stride == p.qkv_stride &&
-      static_cast<cuuint64_t>(p.qkv_stride) >= 4 * HK)
-    mode = 1;
-  else if (al16(p.raw_gate) && (p.gate_stride * 2) % 16 == 0)
-    mode = 2;
-  else
-    return;
-  if (p.conv_dim_first && (K * Lc) % 128 != 0) return;
-  if ((K * W) % 128 != 0 || !al16(p.conv_state) || (p.conv_slot_stride * 2) % 16 != 0 || !al16(p.conv_weight)) return;
-  const cuuint64_t groups = mode == 1 ? 4 : 3;
-  {
-    const cuuint64_t dims[3] = {HK, groups, T};
-    const cuuint64_t strides[2] = {HK * 2, static_cast<cuuint64_t>(p.qkv_stride) * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(K), static_cast<cuuint32_t>(groups), static_cast<cuuint32_t>(Q)};
-    if (!encode_map(&p.tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.mixed_qkv, dims, strides, box)) return;
-  }
-  if (mode == 2) {
-    const cuuint64_t dims[2] = {HK, T};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.gate_stride) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(K), static_cast<cuuint32_t>(Q)};
-    if (!encode_map(&p.tm_gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.raw_gate, dims, strides, box)) return;
-  }
-  const cuuint64_t slots = static_cast<cuuint64_t>(p.num_slots);
-  if (p.conv_dim_first) {
-    const cuuint64_t dims[4] = {128, HK * Lc / 128, 3, slots};
-    const cuuint64_t strides[3] = {256, HK * Lc * 2, static_cast<cuuint64_t>(p.conv_slot_stride) * 2};
-    const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(K * Lc / 128), 3, 1};
-    if (!encode_map(&p.tm_conv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.conv_state, dims, strides, box)) return;
-  } else {
-    const cuuint64_t dims[4] = {HK, 3, Lc, slots};
-    const cuuint64_t strides[3] = {HK * 2, 3 * HK * 2, static_cast<cuuint64_t>(p.conv_slot_stride) * 2};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(K), 3, static_cast<cuuint32_t>(Lc), 1};
-    if (!encode_map(&p.tm_conv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.conv_state, dims, strides, box)) return;
-  }
-  {
-    const cuuint64_t dims[3] = {128, HK * W / 128, 3};
-    const cuuint64_t strides[2] = {128 * wb, HK * W * wb};
-    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(K * W / 128), 3};
-    const CUtensorMapDataType dt = p.conv_weight_fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!encode_map(&p.tm_w, dt, 3, p.conv_weight, dims, strides, box)) return;
-  }
-  p.act_mode = mode;
-}
-
 // Which verify runs the products at K = 128.  An M = 128 tf32 MMA costs about
 // the same whatever N is, and fp32 accuracy takes a second (low-part) pass,
 // so the tensor cores win only when the window brings many operand vectors:
 // measured on GB300, the tcgen05 verify is faster for windows of 8 (C3) and
-// slower for windows of 4 (C2), so that is the default split.
-// KDA_VERIFY_TCGEN05=1 forces the tensor cores, =0 the CUDA-core gemv.
-bool use_tcgen05(bool window_up_to_4) {
-  const char* v = std::getenv("KDA_VERIFY_TCGEN05");
-  if (v != nullptr && v[0] == '1' && v[1] == '\0') return true;
-  if (v != nullptr && v[0] == '0' && v[1] == '\0') return false;
+// slower for windows of 4 (C2), so that is the automatic choice.
+bool use_tcgen05(int variant, bool window_up_to_4) {
+  if (variant == KDA_VERIFY_TCGEN05) return true;
+  if (variant == KDA_VERIFY_CUDA_CORE) return false;
   return !window_up_to_4;
 }
 
 int sm_count() {
-  static int cached[64] = {0};
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices];  // zero-initialised: static storage
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
-template <int KD, int QMAX, bool DF, int VAR>
+template <int KD, int QMAX, int VAR>
 cudaError_t launch(const VerifyParams& p, cudaStream_t stream) {
   constexpr int bytes = Layout<KD, QMAX, VAR>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, DF, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const int items = p.B * p.H;
   const int grid = items < sm_count() ? items : sm_count();
-  verify_kernel<KD, QMAX, DF, VAR><<<grid, Layout<KD, QMAX, VAR>::kThreads, bytes, stream>>>(p);
+  verify_kernel<KD, QMAX, VAR><<<grid, Layout<KD, QMAX, VAR>::kThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int KD, int QMAX, bool DF>
+cudaError_t launch_conv(const VerifyParams& p, cudaStream_t stream) {
+  conv_kernel<KD, QMAX, DF><<<p.B * p.H, KD, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_verify(const VerifyParams& params, int K, cudaStream_t stream) {
+cudaError_t launch_verify(const VerifyParams& params, int K, int variant, cudaStream_t stream) {
   VerifyParams p = params;
-  build_tensor_maps(p, K);
-  // the conv-state layout is a template parameter: straight-line tap addressing
   const bool q4 = p.Q <= 4;
+  // the conv pass (nothing to convolve when every window is empty)
+  if (p.T > 0) {
+    cudaError_t e;
+    if (K == 128)
+      e = q4 ? (p.conv_dim_first ? launch_conv<128, 4, true>(p, stream) : launch_conv<128, 4, false>(p, stream))
+             : (p.conv_dim_first ? launch_conv<128, 8, true>(p, stream) : launch_conv<128, 8, false>(p, stream));
+    else
+      e = q4 ? (p.conv_dim_first ? launch_conv<64, 4, true>(p, stream) : launch_conv<64, 4, false>(p, stream))
+             : (p.conv_dim_first ? launch_conv<64, 8, true>(p, stream) : launch_conv<64, 8, false>(p, stream));
+    if (e != cudaSuccess) return e;
+  }
   if (p.fold_qsl != nullptr) {  // the host accepts the fold for windows up to 4 only
     if (!q4) return cudaErrorInvalidValue;
-    if (K == 128) return p.conv_dim_first ? launch<128, 4, true, kVarFold>(p, stream) : launch<128, 4, false, kVarFold>(p, stream);
-    return p.conv_dim_first ? launch<64, 4, true, kVarFold>(p, stream) : launch<64, 4, false, kVarFold>(p, stream);
+    return K == 128 ? launch<128, 4, kVarFold>(p, stream) : launch<64, 4, kVarFold>(p, stream);
   }
-  if (K == 128 && use_tcgen05(q4) && build_state_map(p, K)) {
-    if (q4) return p.conv_dim_first ? launch<128, 4, true, kVarTcgen05>(p, stream) : launch<128, 4, false, kVarTcgen05>(p, stream);
-    return p.conv_dim_first ? launch<128, 8, true, kVarTcgen05>(p, stream) : launch<128, 8, false, kVarTcgen05>(p, stream);
-  }
-  if (p.conv_dim_first) {
-    if (K == 128) return q4 ? launch<128, 4, true, kVarPlain>(p, stream) : launch<128, 8, true, kVarPlain>(p, stream);
-    return q4 ? launch<64, 4, true, kVarPlain>(p, stream) : launch<64, 8, true, kVarPlain>(p, stream);
-  }
-  if (K == 128) return q4 ? launch<128, 4, false, kVarPlain>(p, stream) : launch<128, 8, false, kVarPlain>(p, stream);
-  return q4 ? launch<64, 4, false, kVarPlain>(p, stream) : launch<64, 8, false, kVarPlain>(p, stream);
+  if (K == 128 && use_tcgen05(variant, q4) && build_state_map(p, K))
+    return q4 ? launch<128, 4, kVarTcgen05>(p, stream) : launch<128, 8, kVarTcgen05>(p, stream);
+  if (K == 128) return q4 ? launch<128, 4, kVarPlain>(p, stream) : launch<128, 8, kVarPlain>(p, stream);
+  return q4 ? launch<64, 4, kVarPlain>(p, stream) : launch<64, 8, kVarPlain>(p, stream);
 }
 
 }  // namespace kda

@@ -97,6 +97,9 @@ def _valid_verify_args():
     a.state_slot_stride = H * K * K
     a.corr_row_stride = H * Q * K
     a.kg_row_stride = H * Q * 2 * K
+    a.scratch = FAKE
+    a.scratch_bytes = 2 * H * Q * 4 * K * 2
+    a.variant = 0
     return a
 
 
@@ -129,6 +132,12 @@ def test_verify_rejects_before_launch(lib):
         (dict(key_gate=FAKE + 8), kda.KDA_ERR_MISALIGNED),
         (dict(conv_state=FAKE + 2), kda.KDA_ERR_MISALIGNED),
         (dict(out=FAKE + 1), kda.KDA_ERR_MISALIGNED),
+        (dict(scratch=0), kda.KDA_ERR_INVALID_ARG),
+        (dict(scratch_bytes=2 * 4 * 4 * 4 * 64 * 2 - 16), kda.KDA_ERR_INVALID_ARG),
+        (dict(scratch=FAKE + 8), kda.KDA_ERR_MISALIGNED),
+        (dict(variant=3), kda.KDA_ERR_INVALID_ARG),
+        (dict(variant=-1), kda.KDA_ERR_INVALID_ARG),
+        (dict(variant=2), kda.KDA_ERR_UNSUPPORTED),    # the tensor-core verify needs K == 128
     ]
     for change, want in cases:
         a = _valid_verify_args()
@@ -142,6 +151,30 @@ def test_verify_rejects_before_launch(lib):
     assert _call_verify(lib, a) == kda.KDA_ERR_INVALID_ARG
     # activation rows at odd element offsets are accepted by validation (handled in-kernel):
     # not launched here, so only checked through the MISALIGNED path not triggering above.
+
+
+def test_verify_scratch_bytes(lib):
+    # [Q][2K] rows q | v and [Q][2K] rows k | gate, bf16, per (request, head)
+    assert lib.kda_verify_scratch_bytes(256, 32, 128, 4) == 256 * 32 * 4 * 4 * 128 * 2
+    assert lib.kda_verify_scratch_bytes(3, 5, 64, 7) == 3 * 5 * 7 * 4 * 64 * 2
+    assert lib.kda_verify_scratch_bytes(0, 32, 128, 4) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="passes validation and would launch on fake pointers")
+def test_fold_only_step_takes_null_activations(lib):
+    """A fold-only step (T == 0) reads no activation and no scratch: NULL
+    pointers with zero strides pass validation (here the launch then fails
+    for want of a GPU, never with an argument error)."""
+    a = _valid_verify_args()
+    a.T = 0
+    for name in ("mixed_qkv", "raw_gate", "raw_beta", "out", "scratch"):
+        setattr(a, name, 0)
+    a.qkv_row_stride = a.gate_row_stride = a.beta_row_stride = a.out_row_stride = 0
+    a.scratch_bytes = 0
+    f = kda.FoldArgs()
+    f.query_start_loc, f.num_accepted = FAKE, FAKE
+    st = lib.kda_verify_fold(ctypes.byref(a), ctypes.byref(f), None)
+    assert st in (kda.KDA_OK, kda.KDA_ERR_CUDA), kda.last_error()
 
 
 def test_verify_empty_is_a_no_op(lib):

@@ -128,7 +128,7 @@ def check_commit_layer(prob, l, hl, exact, meta, before=None, mask=None):
     return None
 
 
-def run_and_check(prob, *, commit=True, mask=None, layers=None):
+def run_and_check(prob, *, commit=True, mask=None, layers=None, variant="auto"):
     """Verify every layer on the GPU, then (optionally) commit all layers in one
     launch; compare each with the oracle run on host copies of the inputs."""
     cfg = prob.cfg
@@ -141,7 +141,7 @@ def run_and_check(prob, *, commit=True, mask=None, layers=None):
     ws = kda.new_workspace(DEV)
     dm = device_meta(meta, DEV)
     for l in range(cfg.L):
-        verify_layer(prob, l, dm, workspace=ws)
+        verify_layer(prob, l, dm, workspace=ws, variant=variant)
     assert kda.read_device_error(ws) == 0
     stats = []
     for l in layers:

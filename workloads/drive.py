@@ -36,14 +36,26 @@ def conv_state_view(prob: Problem, l: int) -> torch.Tensor:
     return prob.conv_state[l]
 
 
+def problem_scratch(prob: Problem) -> torch.Tensor:
+    """The verify's device scratch for this workload, allocated once (every
+    layer's verify reuses it in stream order)."""
+    sc = prob.extra.get("scratch")
+    if sc is None:
+        cfg = prob.cfg
+        sc = kda.new_verify_scratch(cfg.B, cfg.H, cfg.K, cfg.Q, prob.fused.device)
+        prob.extra["scratch"] = sc
+    return sc
+
+
 def verify_layer(prob: Problem, l: int, dm: DeviceMeta, *, out=None, workspace=None, stream=None,
-                 fused=None, fold: DeviceMeta | None = None) -> None:
+                 fused=None, fold: DeviceMeta | None = None, variant: str = "auto") -> None:
     """One layer's verify.  With ``fold`` (the previous step's metadata) the
     previous step's accepted records are folded into the checkpoints first,
     in the same launch (``kda_verify_fold``)."""
     cfg = prob.cfg
     H, K = cfg.H, cfg.K
     f = prob.fused[l] if fused is None else fused
+    scratch = problem_scratch(prob) if f.is_cuda else None
     kda.verify(
         mixed_qkv=f[:, : 3 * H * K], raw_gate=f[:, 3 * H * K: 4 * H * K],
         raw_beta=f[:, 4 * H * K: 4 * H * K + H],
@@ -56,7 +68,8 @@ def verify_layer(prob: Problem, l: int, dm: DeviceMeta, *, out=None, workspace=N
         workspace=workspace, stream=stream,
         fold_query_start_loc=None if fold is None else fold.query_start_loc,
         fold_num_accepted=None if fold is None else fold.num_accepted,
-        fold_record_indices=None if fold is None else fold.record_indices)
+        fold_record_indices=None if fold is None else fold.record_indices,
+        scratch=scratch, variant=variant)
 
 
 def commit_context(prob: Problem) -> kda.CommitContext:

@@ -224,11 +224,12 @@ def workload_config(c, acct) -> dict:
 
 # --------------------------------------------------------------------------- oracle timing (CPU)
 
-def time_oracle(cfg_name: str, steps: int, warmup: int, sample_layers: int = 1, threads: int | None = None):
-    """The CPU oracle as it stands on a bounded sample of the workload: the
-    full request batch of ``sample_layers`` layers (verify, then commit).
-    Returns (tokens/s scaled to the full layer count, seconds per full step,
-    sample description, threads)."""
+def time_oracle(cfg_name: str, steps: int, warmup: int, threads: int | None = None, layers: int | None = None):
+    """The CPU oracle as it stands, timed on full steps of the workload: per
+    step, the full request batch's verify and commit, L times (one layer's
+    inputs, re-used for every layer: the oracle's work does not depend on the
+    values, and L distinct C2 layers would need about 24 GiB of host memory).
+    Returns (tokens/s, seconds per step, sample description, threads, accounting)."""
     tests = os.path.join(ROOT, "tests")
     if tests not in sys.path:
         sys.path.insert(0, tests)
@@ -236,15 +237,17 @@ def time_oracle(cfg_name: str, steps: int, warmup: int, sample_layers: int = 1, 
     from workloads import CONFIGS, make_problem
 
     cfg = CONFIGS[cfg_name]
+    if layers:
+        cfg = cfg.replace(L=layers)
     threads = threads or len(os.sched_getaffinity(0))
-    prob = make_problem(cfg, "cpu", L=sample_layers)
+    prob = make_problem(cfg, "cpu", L=1)
     acct = step_accounting(cfg, prob.meta)
-    base = [host_layer(prob, l) for l in range(sample_layers)]
+    hl = host_layer(prob, 0)
 
     def one_step():
-        # a decode step on the sampled layers: the verify rolls the conv state and
-        # writes records in place, the commit advances the state in place
-        for hl in base:
+        # a decode step: every layer's verify rolls the conv state and writes
+        # records in place, its commit advances the state in place
+        for _ in range(cfg.L):
             run_verify(prob, hl, num_threads=threads)
             run_commit(prob, hl, num_threads=threads)
 
@@ -253,11 +256,10 @@ def time_oracle(cfg_name: str, steps: int, warmup: int, sample_layers: int = 1, 
     t0 = time.perf_counter()
     for _ in range(steps):
         one_step()
-    dt = (time.perf_counter() - t0) / steps
-    per_full_step = dt * cfg.L / sample_layers
-    sample = (f"{cfg_name} request batch (B={cfg.B}, H={cfg.H}) over {sample_layers} of {cfg.L} layers, "
-              f"verify + commit, {steps} steps; scaled to {cfg.L} layers")
-    return acct["tokens"] / per_full_step, per_full_step, sample, threads, acct
+    per_step = (time.perf_counter() - t0) / steps
+    sample = (f"{cfg_name} full steps: the request batch (B={cfg.B}, H={cfg.H}), verify + commit of {cfg.L} "
+              f"layers per step (one layer's inputs re-used), {steps} timed steps after {warmup}")
+    return acct["tokens"] / per_step, per_step, sample, threads, acct
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -423,7 +425,8 @@ def run_gpu(args, rank, local, world):
     traffic = profiled_traffic("verify" if dom == "kda_verify" else "commit", workload)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cv, cstep, sample, threads, _ = time_oracle(args.config, steps=args.cpu_steps, warmup=1)
+        cv, cstep, sample, threads, _ = time_oracle(args.config, steps=args.cpu_steps, warmup=1,
+                                                    layers=args.layers)  # bounded: ~10-20 s
         cpu = {"value": cv, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample,
                "s_per_full_step": cstep}
     line = {
@@ -477,8 +480,11 @@ def run_reference(args, rank, world):
     oracle.build()
     from workloads import CONFIGS
     cfg = CONFIGS[args.config]
-    steps = min(args.steps, args.cpu_steps)  # each oracle step is a bounded sample (one layer)
-    value, per_step, sample, threads, acct = time_oracle(args.config, steps=steps, warmup=min(args.warmup, 3))
+    if args.layers:
+        cfg = cfg.replace(L=args.layers)
+    steps = args.steps
+    value, per_step, sample, threads, acct = time_oracle(args.config, steps=steps, warmup=args.warmup,
+                                                         layers=args.layers)
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -486,7 +492,7 @@ def run_reference(args, rank, world):
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": steps,
-        "warmup": min(args.warmup, 3),
+        "warmup": args.warmup,
         "ms_per_step": per_step * 1e3,
         "higher_is_better": True,
         "scaling": "weak",
@@ -502,12 +508,12 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default="C2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-steps", type=int, default=200)
+    ap.add_argument("--cpu-steps", type=int, default=8, help="full oracle steps of the cpu_baseline sample")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (small cases for profiling; not a bench line)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -515,6 +521,14 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    launched = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and launched == 1:
+        ap.error(f"--gpus {args.gpus}: one process per GPU; launch with "
+                 f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus} ...")
+    if launched > 1 and launched != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {launched}")
     rank, local, world = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, rank, world)

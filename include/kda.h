@@ -232,8 +232,11 @@ typedef struct kda_commit_args {
  * state[s] (so args->state is WRITTEN by this call), and the verify of this
  * step then runs on it as kda_verify does.  The pending records are read
  * before this step's records are written, so r' may equal this step's record
- * row.  A request with n = 0 and m > 0 is folded only.  The result equals
- * kda_commit with the fold arguments followed by kda_verify, up to fp32
+ * row.  It must not be another request's record row of this step: the
+ * requests are verified concurrently, and that request's new records could
+ * overwrite row r' before it is read.  A request with n = 0 and m > 0 is
+ * folded only.  The result equals kda_commit with the fold arguments
+ * followed by kda_verify, up to fp32
  * rounding.  The fold pointers are device arrays ([B+1], [B], [B] or NULL);
  * fold == NULL or fold->query_start_loc == NULL runs the plain verify.  With
  * T == 0 (every window empty) only the folds run, and the activation
@@ -282,20 +285,46 @@ kda_status kda_commit_align(const kda_commit_args *args, const kda_align_args *a
  * with a hi/lo split of the state, same tolerances) or the CUDA cores. */
 kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
 
+/*
+ * kda_verify_debug -- kda_verify on the CUDA cores with its failure handling
+ * exercised, for tests: no device wait is unbounded, and this entry point
+ * makes one run out.  The pages have no counterpart.
+ *   - wait_limit_ns (> 0) replaces the one-second limit of every device wait
+ *     of the verify kernel for this call;
+ *   - withhold_item (-1: none; else an item b * H + h) is an item whose
+ *     inputs the verify kernel's inputs warp never delivers: no copy is
+ *     issued and its slot never fills.  The kernel's wait for it gives up
+ *     after wait_limit_ns, KDA_DEVERR_TIMEOUT is set in the workspace, the
+ *     CTA that owns the item stops (its later items are left unwritten) and
+ *     the kernel returns; the other CTAs' items are verified as by kda_verify.
+ * Everything else is as for kda_verify (the conv pass runs for every item).
+ */
+typedef struct kda_debug_args {
+    int64_t wait_limit_ns;   /* > 0                                      */
+    int32_t withhold_item;   /* -1, or an item in [0, B * H)            */
+} kda_debug_args;
+
+kda_status kda_verify_debug(const kda_verify_args *args, const kda_debug_args *debug, kda_stream_t stream);
+
 /* Enqueue the commit of all layers (one kernel launch). */
 kda_status kda_commit(const kda_commit_args *args, kda_stream_t stream);
 
 /* Allocation-free commit.  The pages have no counterpart to this entry point:
  * their commit context keeps the per-layer tables in device memory it
  * allocates once (KDARecoverSSMCommitContext.create).  It serves callers that
- * cannot allocate device memory.
+ * cannot allocate device memory: code running where a device allocator is
+ * not available or not allowed (inside an allocator callback, a memory pool
+ * that must not grow, or an embedding runtime that owns all device memory).
  *
  * args is read as for kda_commit, except that the six per-layer tables
  * (state_base, state_slot_stride, corr_base, corr_row_stride, kg_base,
- * kg_row_stride) are HOST arrays of L entries, read during the call.  The
- * call copies them, in stream order, into a library-owned static device
- * scratch of KDA_NOALLOC_MAX_LAYERS layers (6 x 64 int64 = 3 KB) and runs the
- * kda_commit kernel on it.  It allocates nothing, on the host or the device.
+ * kg_row_stride) are HOST arrays of L entries, read during the call into the
+ * launch parameters of a small kernel that writes them, in stream order, into
+ * a library-owned static device scratch of KDA_NOALLOC_MAX_LAYERS layers
+ * (6 x 64 int64 = 3 KB); then the kda_commit kernel runs on it.  Two kernel
+ * launches, no copy from host memory: the call allocates nothing, on the host
+ * or the device, keeps no pointer to the host tables and does not wait for
+ * the stream.
  *   - L > KDA_NOALLOC_MAX_LAYERS: KDA_ERR_UNSUPPORTED, nothing enqueued.
  *   - The first call on a device does the set-up: it resolves the scratch's
  *     device address (cudaGetSymbolAddress), which may load the module.  Make
@@ -303,9 +332,9 @@ kda_status kda_commit(const kda_commit_args *args, kda_stream_t stream);
  *   - Nothing in the scratch has to start at zero: each call writes every
  *     table entry its kernel reads, before the kernel, in stream order.  The
  *     optional workspace is the caller's and is used as for kda_commit.
- *   - There is one scratch per device and process: calls whose copies and
- *     kernels can overlap (different streams, or threads without a common
- *     stream order) race on it.  Serialise them. */
+ *   - There is one scratch per device and process: calls whose kernels can
+ *     overlap (different streams, or threads without a common stream order)
+ *     race on it.  Serialise them. */
 #define KDA_NOALLOC_MAX_LAYERS 64
 kda_status kda_commit_noalloc(const kda_commit_args *args, kda_stream_t stream);
 

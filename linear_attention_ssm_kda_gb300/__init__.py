@@ -75,6 +75,11 @@ class VerifyArgs(ctypes.Structure):
 VARIANTS = {"auto": 0, "cuda_core": 1, "tcgen05": 2}
 
 
+class DebugArgs(ctypes.Structure):
+    """Mirror of ``kda_debug_args``."""
+    _fields_ = [("wait_limit_ns", _i64), ("withhold_item", _i32)]
+
+
 class AlignArgs(ctypes.Structure):
     """Mirror of ``kda_align_args``."""
     _fields_ = [("final_state_indices", _p), ("boundary_state_indices", _p), ("boundary_recovery_lens", _p)]
@@ -120,6 +125,8 @@ def load_library():
             lib.kda_verify.restype = ctypes.c_int
             lib.kda_verify_fold.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(FoldArgs), _p]
             lib.kda_verify_fold.restype = ctypes.c_int
+            lib.kda_verify_debug.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(DebugArgs), _p]
+            lib.kda_verify_debug.restype = ctypes.c_int
             lib.kda_commit.argtypes = [ctypes.POINTER(CommitArgs), _p]
             lib.kda_commit.restype = ctypes.c_int
             lib.kda_commit_align.argtypes = [ctypes.POINTER(CommitArgs), ctypes.POINTER(AlignArgs), _p]
@@ -213,7 +220,7 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
            key_gate, query_start_loc, state_indices, conv_state, conv_weight, out, window,
            num_accepted_tokens=None, record_indices=None, conv_dim_first=True, null_block_id=0,
            workspace=None, stream=None, fold_query_start_loc=None, fold_num_accepted=None,
-           fold_record_indices=None, scratch=None, variant: str = "auto") -> None:
+           fold_record_indices=None, scratch=None, variant: str = "auto", debug=None) -> None:
     """Verify ``state_indices.shape[0]`` requests of one KDA layer.
 
     ``mixed_qkv`` [T, 3HK] is the raw projection (before the convolution),
@@ -236,7 +243,11 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
     K, window)`` bytes for the conv pass's output; when None, one is taken
     from torch's allocator on the launch stream for this call.  ``variant``
     ("auto", "cuda_core" or "tcgen05") picks the kernel of the products (the
-    tensor cores need K = 128)."""
+    tensor cores need K = 128).
+
+    ``debug`` = (withhold_item, wait_limit_ns) calls ``kda_verify_debug``
+    instead: the item's inputs are withheld and every device wait gives up
+    after wait_limit_ns (a test of the bounded waits; CUDA cores, no fold)."""
     dev = state.device
     if dev.type != "cuda":
         raise ValueError("verify runs on a CUDA device; state is on " + str(dev))
@@ -338,7 +349,13 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
             raise ValueError("scratch must be a contiguous tensor on the state's device")
         a.scratch, a.scratch_bytes = scratch.data_ptr(), scratch.numel() * scratch.element_size()
     handle = ctypes.c_void_p(_stream_handle(dev, stream))
-    if fold is None:
+    if debug is not None:
+        if fold is not None:
+            raise ValueError("debug runs the plain verify (no fold)")
+        d = DebugArgs()
+        d.withhold_item, d.wait_limit_ns = int(debug[0]), int(debug[1])
+        _check(load_library().kda_verify_debug(ctypes.byref(a), ctypes.byref(d), handle))
+    elif fold is None:
         _check(load_library().kda_verify(ctypes.byref(a), handle))
     else:
         _check(load_library().kda_verify_fold(ctypes.byref(a), ctypes.byref(fold), handle))

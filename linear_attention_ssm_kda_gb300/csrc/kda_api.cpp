@@ -19,6 +19,7 @@ namespace kda {
 cudaError_t launch_verify(const VerifyParams& p, int K, int variant, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, int K, cudaStream_t stream);
 cudaError_t noalloc_tables(long long** out);
+cudaError_t noalloc_fill(const int64_t* const src[6], int L, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -158,6 +159,8 @@ kda_status verify_params(const kda_verify_args* a, bool fold, kda::VerifyParams&
   p.workspace = a->workspace;
   p.k_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(K)));
   p.scratch = static_cast<uint16_t*>(a->scratch);
+  p.wait_limit_ns = 1000000000ull;  // every device wait gives up after about a second
+  p.withhold_item = -1;
   if ((long long)p.B * p.H > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: B*H too large");
   return KDA_OK;
 }
@@ -190,6 +193,23 @@ kda_status kda_verify_fold(const kda_verify_args* a, const kda_fold_args* f, kda
   p.fold_record_indices = f->record_indices;
   cudaError_t e = kda::launch_verify(p, a->K, a->variant, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify_fold: launch failed: %s", cudaGetErrorString(e));
+  return KDA_OK;
+}
+
+kda_status kda_verify_debug(const kda_verify_args* a, const kda_debug_args* d, kda_stream_t stream) {
+  if (d == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify_debug: debug args are NULL");
+  if (d->wait_limit_ns <= 0) return fail(KDA_ERR_INVALID_ARG, "kda_verify_debug: wait_limit_ns must be positive");
+  kda::VerifyParams p;
+  bool noop = false;
+  const kda_status st = verify_params(a, false, p, &noop);
+  if (st != KDA_OK || noop) return st;
+  if (d->withhold_item < -1 || static_cast<long long>(d->withhold_item) >= static_cast<long long>(a->B) * a->H)
+    return fail(KDA_ERR_INVALID_ARG, "kda_verify_debug: withhold_item %d is not -1 or an item", d->withhold_item);
+  p.wait_limit_ns = static_cast<unsigned long long>(d->wait_limit_ns);
+  p.withhold_item = d->withhold_item;
+  // the CUDA-core verify: the path whose abort sequence this hook exercises
+  cudaError_t e = kda::launch_verify(p, a->K, KDA_VERIFY_CUDA_CORE, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify_debug: launch failed: %s", cudaGetErrorString(e));
   return KDA_OK;
 }
 
@@ -274,16 +294,15 @@ kda_status kda_commit_noalloc(const kda_commit_args* a, kda_stream_t stream) {
   cudaError_t e = kda::noalloc_tables(&tables);
   if (e != cudaSuccess)
     return fail(KDA_ERR_CUDA, "kda_commit_noalloc: scratch set-up failed: %s", cudaGetErrorString(e));
-  // host staging on the stack: table j of layer l at [j * kMax + l]
-  long long host[6 * kMax];
+  // the host tables travel by value in the parameters of a small kernel that
+  // writes them into the scratch, in stream order (table j of layer l at
+  // [j * kMax + l])
   const int64_t* src[6] = {a->state_base, a->state_slot_stride, a->corr_base,
                            a->corr_row_stride, a->kg_base, a->kg_row_stride};
-  for (int j = 0; j < 6; ++j)
-    for (int l = 0; l < kMax; ++l) host[j * kMax + l] = l < a->L ? static_cast<long long>(src[j][l]) : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  e = cudaMemcpyAsync(tables, host, sizeof host, cudaMemcpyHostToDevice, s);
+  e = kda::noalloc_fill(src, a->L, s);
   if (e != cudaSuccess)
-    return fail(KDA_ERR_CUDA, "kda_commit_noalloc: table copy failed: %s", cudaGetErrorString(e));
+    return fail(KDA_ERR_CUDA, "kda_commit_noalloc: table fill failed: %s", cudaGetErrorString(e));
 
   kda::CommitParams p{};
   p.L = a->L; p.B = a->B; p.H = a->H; p.Q = a->Q; p.null_block_id = a->null_block_id;

@@ -79,12 +79,13 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 
-// Wait for phase `parity` of `bar` to complete, giving up after about a second.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete, giving up after limit_ns
+// (about a second unless a caller sets a shorter limit).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
   while (!mbar_try_wait_suspend(bar, parity)) {
-    if (global_timer_ns() - start > kWaitLimitNs) return false;
+    if (global_timer_ns() - start > limit_ns) return false;
   }
   return true;
 }
@@ -95,12 +96,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 // Like mbar_wait_bounded, but also gives up as soon as *abort is set (another
 // role of the CTA has timed out and the pipeline is being torn down).
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
   while (!mbar_try_wait_suspend(bar, parity)) {
     if (*abort) return false;
-    if (global_timer_ns() - start > kWaitLimitNs) return false;
+    if (global_timer_ns() - start > limit_ns) return false;
   }
   return true;
 }

@@ -35,6 +35,11 @@ struct VerifyParams {
   // (query_start_loc, accepted counts, record rows or NULL for the state slot)
   // folded into its checkpoint first; fold_qsl == nullptr: plain verify
   const int* fold_qsl; const int* fold_num_accepted; const int* fold_record_indices;
+  // bounded waits: the limit (about a second; kda_verify_debug may shorten
+  // it) and the item whose inputs the inputs warp withholds (kda_verify_debug;
+  // -1: none)
+  unsigned long long wait_limit_ns;
+  int withhold_item;
 };
 
 struct CommitParams {

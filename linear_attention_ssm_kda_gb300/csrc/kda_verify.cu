@@ -151,7 +151,8 @@ struct Layout {
   static constexpr int kFoldIdx = 2 * QMAX + QMAX * QMAX;  // fold variant: |k_u|^2 of the pending keys
   static constexpr int kPart = ru(kFoldIdx + (kFold ? QMAX : 0), 32);         // reduced values per prep warp
   static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kGemvWarps * kRedPerWarp * 4 +
-                                kPrepWarps * kPart * 4 + 32 + (2 * kNumSmall + 2 * kNumOp + 4) * 8 + (kTC ? 1024 : 0);
+                                kPrepWarps * kPart * 4 + 32 + 64 + (2 * kNumSmall + 2 * kNumOp + 4) * 8 +
+                                (kTC ? 1024 : 0);
   static constexpr int kBarsPerChunk = kTC ? 4 : 2;
   static constexpr int kChunkFit = (kSmemLimit - kFixed - 64 * kBarsPerChunk * 8) / kChunk;
   static constexpr int kNumChunk = kChunkFit > 64 ? 64 : kChunkFit;
@@ -162,13 +163,15 @@ struct Layout {
   static constexpr int oRed = oOp + kNumOp * kOp;
   static constexpr int oPart = oRed + kGemvWarps * kRedPerWarp * 4;
   static constexpr int oMisc = oPart + kPrepWarps * kPart * 4;  // int[8]
-  static constexpr int oBars = ru(oMisc + 32, 8);
+  static constexpr int oArm = oMisc + 32;                      // uint8[64]: last armed phase per chunk slot
+  static constexpr int oBars = ru(oArm + 64, 8);
   static constexpr int kNumBars = kBarsPerChunk * kNumChunk + 2 * kNumSmall + 2 * kNumOp + 4;
   static constexpr int kBytes = oBars + kNumBars * 8;
   static_assert(kBytes <= kSmemLimit, "shared memory budget");
   // at least six K-slices (tensor cores), 1.5 items of chunks (fold variant,
   // whose slots carry the pending records) or two items of chunks in flight
   static_assert(kNumChunk >= (kTC ? 6 : kFold ? 3 * kGemvWarps / 2 : 2 * kGemvWarps), "state in flight");
+  static_assert(kNumChunk <= 64, "one record of the last armed phase per chunk slot");
 };
 
 template <int KD, int QMAX, int VAR>
@@ -201,9 +204,10 @@ __device__ __forceinline__ long long shfl_ll(long long v, int src) {
 }
 
 // Warp-wide bounded wait by lane 0; every lane then holds the acquire.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane, const volatile int* abort_flag) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane, const volatile int* abort_flag,
+                                          uint64_t limit_ns) {
   bool ok = true;
-  if (lane == 0) ok = mbar_wait_or_abort(bar, parity, abort_flag);
+  if (lane == 0) ok = mbar_wait_or_abort(bar, parity, abort_flag, limit_ns);
   ok = __all_sync(0xffffffffu, ok);
   if (ok && lane != 0) mbar_acquire_seen(bar, parity);
   return ok;
@@ -403,6 +407,9 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
   Bars<KD, QMAX, VAR> bars(smem);
   const int nloc = local_items(p.B * p.H);
   bool ok = true;
+  // per small slot: whether this warp has armed a phase of its full barrier,
+  // and that phase's parity (the copies behind it are waited for at exit)
+  uint32_t armed = 0, armed_parity = 0;
   for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
     // metadata of up to 32 items, one per lane, in two round trips
     const int it = static_cast<int>(blockIdx.x) + (i0 + lane) * static_cast<int>(gridDim.x);
@@ -440,9 +447,14 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
       // fold variant: the item's pending key/gate and correction records
       const uint32_t fold_bytes = (jflags & kLive) ? static_cast<uint32_t>(jfm) * (2 * KD * 2 + KD * 4) : 0u;
       const int slot = i % Lay::kNumSmall;
-      ok = warp_wait(&bars.sm_empty[slot], ((i / Lay::kNumSmall) & 1) ^ 1, lane, abort_flag);
+      ok = warp_wait(&bars.sm_empty[slot], ((i / Lay::kNumSmall) & 1) ^ 1, lane, abort_flag, p.wait_limit_ns);
       if (!ok) break;
       unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
+      // kda_verify_debug: this item's inputs are withheld (no copy, no
+      // arrival), so the prep team's bounded wait on them runs out
+      if (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x) == p.withhold_item) continue;
+      armed |= 1u << slot;
+      armed_parity = (armed_parity & ~(1u << slot)) | (static_cast<uint32_t>((i / Lay::kNumSmall) & 1) << slot);
       if (lane == j) *reinterpret_cast<SmallMeta<QMAX>*>(sl) = own;
       __syncwarp();  // orders lane j's header before lane 0's arrival on sm_full
       if (jflags & kLive) {
@@ -473,6 +485,12 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
   }
+  // no copy may land after the CTA is gone: wait (bounded) for the last armed
+  // phase of every slot (a phase the prep team already consumed is complete)
+  if (lane == 0) {
+    for (int sl_i = 0; sl_i < Lay::kNumSmall; ++sl_i)
+      if ((armed >> sl_i) & 1u) (void)mbar_wait_bounded(&bars.sm_full[sl_i], (armed_parity >> sl_i) & 1u, p.wait_limit_ns);
+  }
 }
 
 // ---------------------------------------------------------------- state warp
@@ -484,6 +502,12 @@ __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int la
   const int nloc = local_items(p.B * p.H);
   uint32_t ch_cnt = 0;
   bool ok = true;
+  // per chunk slot, the last armed phase: 0 never, 1 + its parity (shared
+  // memory, written by the arming lane; waited for at exit)
+  volatile uint8_t* arm = reinterpret_cast<volatile uint8_t*>(smem + Lay::oArm);
+  if (lane < Lay::kNumChunk) arm[lane] = 0;
+  if (lane + 32 < Lay::kNumChunk) arm[lane + 32] = 0;
+  __syncwarp();
   for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
     const int it = static_cast<int>(blockIdx.x) + (i0 + lane) * static_cast<int>(gridDim.x);
     const ItemMeta<QMAX> im = decode_item<QMAX>(p, it, i0 + lane < nloc, false);
@@ -496,8 +520,9 @@ __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int la
       if (lane < kGemvWarps) {
         const uint32_t cc = ch_cnt + lane;
         const int pos = cc % Lay::kNumChunk;
-        ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((cc / Lay::kNumChunk) & 1) ^ 1, abort_flag);
+        ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((cc / Lay::kNumChunk) & 1) ^ 1, abort_flag, p.wait_limit_ns);
         if (ok) {
+          arm[pos] = static_cast<uint8_t>(1 + ((cc / Lay::kNumChunk) & 1));
           const float* src = p.state + js * p.state_slot_stride + static_cast<long long>(jh) * KD * KD;
           mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
           bulk_g2s(smem + Lay::oChunks + pos * Lay::kChunk, src + lane * Lay::RW * KD, Lay::kChunk,
@@ -511,6 +536,13 @@ __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int la
   if (!ok && lane == 0) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
+  }
+  // no copy may land after the CTA is gone: wait (bounded) for the last
+  // armed phase of every chunk slot (complete once its copy has landed)
+  __syncwarp();
+  if (lane == 0) {
+    for (int pos = 0; pos < Lay::kNumChunk; ++pos)
+      if (arm[pos]) (void)mbar_wait_bounded(&bars.ch_full[pos], arm[pos] - 1u, p.wait_limit_ns);
   }
 }
 
@@ -546,8 +578,8 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
     const int oslot = i % Lay::kNumOp;
     unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
     unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
-    const bool ok = warp_wait(&bars.sm_full[slot], (i / Lay::kNumSmall) & 1, lane, abort_flag) &&
-                    warp_wait(&bars.op_empty[oslot], ((i / Lay::kNumOp) & 1) ^ 1, lane, abort_flag);
+    const bool ok = warp_wait(&bars.sm_full[slot], (i / Lay::kNumSmall) & 1, lane, abort_flag, p.wait_limit_ns) &&
+                    warp_wait(&bars.op_empty[oslot], ((i / Lay::kNumOp) & 1) ^ 1, lane, abort_flag, p.wait_limit_ns);
     if (!ok && lane == 0) misc[kMiscPrepFail] = 1;
     const SmallMeta<QMAX> m = *reinterpret_cast<const SmallMeta<QMAX>*>(sl);
     const bool live = ok && (m.flags & kLive);
@@ -939,7 +971,7 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
     const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
     const int h = it - (it / p.H) * p.H;
     const int oslot = i % Lay::kNumOp;
-    ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag);
+    ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag, p.wait_limit_ns);
     if (!ok) break;
     const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
     const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta);
@@ -947,7 +979,7 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
       const int n = m.n;
       const uint32_t pc = live * kGemvWarps + gw;
       const int pos = pc % Lay::kNumChunk;
-      ok = warp_wait(&bars.ch_full[pos], (pc / Lay::kNumChunk) & 1, lane, abort_flag);
+      ok = warp_wait(&bars.ch_full[pos], (pc / Lay::kNumChunk) & 1, lane, abort_flag, p.wait_limit_ns);
       if (!ok) break;
       float* st = reinterpret_cast<float*>(smem + Lay::oChunks + pos * Lay::kChunk);
       const float* vec = reinterpret_cast<const float*>(op + Lay::kOpVec);
@@ -1080,7 +1112,7 @@ __device__ void tc_produce_state(const VerifyParams& p, unsigned char* smem, int
       for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
         const int pos = static_cast<int>(g % Lay::kNumChunk);
         if (lane == 0) {
-          ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((g / Lay::kNumChunk) & 1) ^ 1, abort_flag);
+          ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((g / Lay::kNumChunk) & 1) ^ 1, abort_flag, p.wait_limit_ns);
           if (ok) {
             mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
             tma_load_3d(smem + Lay::oChunks + pos * Lay::kChunk, &p.tm_state, kb * 32, jh * KD, js, &bars.ch_full[pos]);
@@ -1098,7 +1130,7 @@ __device__ void tc_produce_state(const VerifyParams& p, unsigned char* smem, int
   // the CTA (and its shared memory) goes away
   if (lane == 0) {
     for (uint32_t e = 0; e < static_cast<uint32_t>(Lay::kNumChunk); ++e, ++g)
-      (void)mbar_wait_bounded(&bars.ch_empty[g % Lay::kNumChunk], ((g / Lay::kNumChunk) & 1) ^ 1);
+      (void)mbar_wait_bounded(&bars.ch_empty[g % Lay::kNumChunk], ((g / Lay::kNumChunk) & 1) ^ 1, p.wait_limit_ns);
   }
 }
 
@@ -1118,13 +1150,13 @@ struct LoPending {
 
 template <int KD, int QMAX, int VAR>
 __device__ __forceinline__ bool tc_issue_lo(unsigned char* smem, uint32_t taddr, LoPending& lp,
-                                            const volatile int* abort_flag) {
+                                            const volatile int* abort_flag, uint64_t limit_ns) {
   using Lay = Layout<KD, QMAX, VAR>;
   constexpr uint32_t kIdesc = umma_idesc_tf32(128, Layout<KD, QMAX, VAR>::kMmaN);
   Bars<KD, QMAX, VAR> bars(smem);
   if (!lp.valid) return true;
   lp.valid = false;
-  if (!mbar_wait_or_abort(&bars.lo_full[lp.pos], (lp.g / Lay::kNumChunk) & 1, abort_flag)) return false;
+  if (!mbar_wait_or_abort(&bars.lo_full[lp.pos], (lp.g / Lay::kNumChunk) & 1, abort_flag, limit_ns)) return false;
   tmem_fence_after();
   const uint64_t a = umma_desc_sw128(smem + Lay::oChunks + lp.pos * Lay::kChunk);
   const uint32_t d = taddr + lp.db * Lay::kDCols;
@@ -1152,22 +1184,22 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
   for (int i = 0; i < nloc && ok; ++i) {
     const int oslot = i % Lay::kNumOp;
     const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
-    ok = mbar_wait_or_abort(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, abort_flag);
+    ok = mbar_wait_or_abort(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, abort_flag, p.wait_limit_ns);
     if (!ok) break;
     if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
       // finish the previous item first: its operand slot may be the next one
       // the prep team needs
-      ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag);
+      ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag, p.wait_limit_ns);
       mbar_arrive(&bars.op_empty[oslot]);
       continue;
     }
     const uint32_t db = live & 1;
-    ok = mbar_wait_or_abort(&bars.d_empty[db], ((live >> 1) & 1) ^ 1, abort_flag);
+    ok = mbar_wait_or_abort(&bars.d_empty[db], ((live >> 1) & 1) ^ 1, abort_flag, p.wait_limit_ns);
     const uint64_t b = umma_desc_sw128(op);
     const uint32_t d = taddr + db * Lay::kDCols;
     for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
       const int pos = static_cast<int>(g % Lay::kNumChunk);
-      ok = mbar_wait_or_abort(&bars.ch_full[pos], (g / Lay::kNumChunk) & 1, abort_flag);
+      ok = mbar_wait_or_abort(&bars.ch_full[pos], (g / Lay::kNumChunk) & 1, abort_flag, p.wait_limit_ns);
       if (!ok) break;
       tmem_fence_after();
       const uint64_t a = umma_desc_sw128(smem + Lay::oChunks + pos * Lay::kChunk);
@@ -1175,12 +1207,12 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) umma_tf32(d, a + 2 * ks, bk + 2 * ks, kIdesc, kb > 0 || ks > 0);
       umma_commit(&bars.hi_done[pos]);
-      ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag);
+      ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag, p.wait_limit_ns);
       lp = LoPending{true, kb == 3, pos, oslot, g, db, bk};
     }
     ++live;
   }
-  if (ok) ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag);
+  if (ok) ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag, p.wait_limit_ns);
   if (!ok) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
     *abort_flag = 1;
@@ -1227,7 +1259,7 @@ __device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char*
   const int oslot = i % Lay::kNumOp;
   const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
   const uint32_t db = live & 1;
-  if (!warp_wait(&bars.d_full[db], (live >> 1) & 1, lane, abort_flag)) return false;
+  if (!warp_wait(&bars.d_full[db], (live >> 1) & 1, lane, abort_flag, p.wait_limit_ns)) return false;
   tmem_fence_after();
   float d[Lay::kDCols];
   const uint32_t ta = taddr + db * Lay::kDCols + (static_cast<uint32_t>(wq * 32) << 16);
@@ -1285,7 +1317,7 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
   for (int i = 0; i < nloc && ok; ++i) {
     const int oslot = i % Lay::kNumOp;
     const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
-    ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag);
+    ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag, p.wait_limit_ns);
     if (!ok) break;
     if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
       // read the pending item out now: with no live item to follow soon, its
@@ -1298,8 +1330,8 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
     }
     for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
       const int pos = static_cast<int>(g % Lay::kNumChunk);
-      ok = warp_wait(&bars.ch_full[pos], (g / Lay::kNumChunk) & 1, lane, abort_flag) &&
-           warp_wait(&bars.hi_done[pos], (g / Lay::kNumChunk) & 1, lane, abort_flag);
+      ok = warp_wait(&bars.ch_full[pos], (g / Lay::kNumChunk) & 1, lane, abort_flag, p.wait_limit_ns) &&
+           warp_wait(&bars.hi_done[pos], (g / Lay::kNumChunk) & 1, lane, abort_flag, p.wait_limit_ns);
       if (!ok) break;
       float4* s4 = reinterpret_cast<float4*>(smem + Lay::oChunks + pos * Lay::kChunk);
 #pragma unroll 4

@@ -177,6 +177,18 @@ def test_fold_only_step_takes_null_activations(lib):
     assert st in (kda.KDA_OK, kda.KDA_ERR_CUDA), kda.last_error()
 
 
+def test_verify_debug_rejects_before_launch(lib):
+    a = _valid_verify_args()
+    d = kda.DebugArgs()
+    assert lib.kda_verify_debug(ctypes.byref(a), None, None) == kda.KDA_ERR_INVALID_ARG
+    d.wait_limit_ns, d.withhold_item = 0, -1
+    assert lib.kda_verify_debug(ctypes.byref(a), ctypes.byref(d), None) == kda.KDA_ERR_INVALID_ARG
+    d.wait_limit_ns, d.withhold_item = 1000, a.B * a.H
+    assert lib.kda_verify_debug(ctypes.byref(a), ctypes.byref(d), None) == kda.KDA_ERR_INVALID_ARG
+    d.withhold_item = -2
+    assert lib.kda_verify_debug(ctypes.byref(a), ctypes.byref(d), None) == kda.KDA_ERR_INVALID_ARG
+
+
 def test_verify_empty_is_a_no_op(lib):
     for change in (dict(B=0, T=0), dict(T=0)):
         a = _valid_verify_args()

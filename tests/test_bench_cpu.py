@@ -1,5 +1,5 @@
-"""bench.py on CPU: the reference arm's JSON line (the oracle timed on a
-bounded sample) and the byte accounting of the two schedules."""
+"""bench.py on CPU: the reference arm's JSON line (the oracle timed on full
+steps), the --gpus contract and the byte accounting of the two schedules."""
 from __future__ import annotations
 
 import json
@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_reference_arm_prints_one_contract_line():
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
-                        "--cpu-steps", "1"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3",
+                        "--layers", "1"], cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     line = json.loads(lines[-1])
@@ -27,6 +27,15 @@ def test_reference_arm_prints_one_contract_line():
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"].startswith("C2")
+    # measured on whole steps with the requested warm-up, not scaled from a sample
+    assert line["steps"] == 2 and line["warmup"] == 3
+    assert "scaled" not in line["cpu_baseline"]["sample"]
+
+
+def test_more_gpus_need_one_process_each():
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--steps", "1", "--warmup", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=120, env={**os.environ, "WORLD_SIZE": "1"})
+    assert r.returncode != 0 and "one process per GPU" in r.stderr
 
 
 def test_deferred_schedule_saves_one_state_read_per_folded_item():

@@ -48,7 +48,7 @@ def problem_scratch(prob: Problem) -> torch.Tensor:
 
 
 def verify_layer(prob: Problem, l: int, dm: DeviceMeta, *, out=None, workspace=None, stream=None,
-                 fused=None, fold: DeviceMeta | None = None, variant: str = "auto") -> None:
+                 fused=None, fold: DeviceMeta | None = None, variant: str = "auto", debug=None) -> None:
     """One layer's verify.  With ``fold`` (the previous step's metadata) the
     previous step's accepted records are folded into the checkpoints first,
     in the same launch (``kda_verify_fold``)."""
@@ -69,7 +69,7 @@ def verify_layer(prob: Problem, l: int, dm: DeviceMeta, *, out=None, workspace=N
         fold_query_start_loc=None if fold is None else fold.query_start_loc,
         fold_num_accepted=None if fold is None else fold.num_accepted,
         fold_record_indices=None if fold is None else fold.record_indices,
-        scratch=scratch, variant=variant)
+        scratch=scratch, variant=variant, debug=debug)
 
 
 def commit_context(prob: Problem) -> kda.CommitContext:

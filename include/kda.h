@@ -25,7 +25,8 @@
  *   - Errors that only the device can see (a slot or record row out of range,
  *     a decreasing query_start_loc, a token range past T) skip the affected
  *     (request, head) work item and OR a KDA_DEVERR_* bit into workspace[0];
- *     kda_read_device_error() fetches it.  workspace may be NULL (no report).
+ *     kda_read_device_error() fetches it.  A commit's workspace may be NULL
+ *     (no report); the verify entry points require one (below).
  *   - No device wait is unbounded: a wait that exceeds about one second sets
  *     KDA_DEVERR_TIMEOUT and the work item returns.
  */
@@ -104,8 +105,10 @@ enum {
  * T == 0 or B == 0 is a no-op returning KDA_OK.
  *
  * Two kernels run, in stream order: the conv pass (one CTA per (request,
- * head): the codes y_t, packed with the raw gate rows into `scratch`, and the
- * rolled conv state) and the verify proper (persistent, one CTA per SM).
+ * head): the codes y_t, packed with the raw gate rows and the beta gates
+ * sigmoid(raw_beta) into `scratch`, and the rolled conv state) and the
+ * verify proper (persistent, one CTA per SM; it may start while the conv
+ * pass drains and waits for it before reading `scratch`).
  * `scratch` is caller-owned device memory of at least
  * kda_verify_scratch_bytes(B, H, K, Q) bytes, 16-byte aligned; its contents
  * between calls are unspecified (calls that may overlap need distinct
@@ -155,7 +158,7 @@ typedef struct kda_verify_args {
     const int32_t *state_indices;     /* [B]                                        */
     const int32_t *record_indices;    /* [B] or NULL (records at the state slot)    */
     const int32_t *num_accepted_prev; /* [B] conv read offset, or NULL (a = 1)      */
-    int32_t *workspace;               /* kda_workspace_bytes() bytes, zeroed, or NULL */
+    int32_t *workspace;               /* kda_workspace_bytes() bytes, zeroed: required */
     void *scratch;                    /* device, >= kda_verify_scratch_bytes(), 16-byte aligned */
     int64_t scratch_bytes;            /* its size in bytes                          */
     int32_t variant;                  /* kda_verify_variant                         */
@@ -171,8 +174,9 @@ typedef enum kda_verify_variant {
     KDA_VERIFY_TCGEN05 = 2
 } kda_verify_variant;
 
-/* Bytes of scratch the verify needs: B * H * Q * 4K bf16 (the conv pass's
- * output, [Q][2K] rows q | v and [Q][2K] rows k | gate per (request, head)). */
+/* Bytes of scratch the verify needs: B * H blocks of Q * 8K + 32 bytes (the
+ * conv pass's output per (request, head): [Q][2K] bf16 rows q | v, [Q][2K]
+ * rows k | gate, then 8 fp32 beta gates). */
 size_t kda_verify_scratch_bytes(int32_t B, int32_t H, int32_t K, int32_t Q);
 
 
@@ -282,13 +286,17 @@ kda_status kda_commit_align(const kda_commit_args *args, const kda_align_args *a
 /* Enqueue the verify of one layer (the conv pass, then the verify kernel).
  * Returns before the kernels run.  args->variant selects the products'
  * kernel (kda_verify_variant): at K == 128 the tcgen05 tensor cores (tf32
- * with a hi/lo split of the state, same tolerances) or the CUDA cores. */
+ * with a hi/lo split of the state, same tolerances) or the CUDA cores.
+ * The verify kernel deals its (request, head) items to its CTAs at run time
+ * from a ticket counter in args->workspace, which every launch leaves at
+ * zero: verify launches that may run at the same time (different streams)
+ * need different workspaces. */
 kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
 
 /*
- * kda_verify_debug -- kda_verify on the CUDA cores with its failure handling
- * exercised, for tests: no device wait is unbounded, and this entry point
- * makes one run out.  The pages have no counterpart.
+ * kda_verify_debug -- kda_verify with two test hooks: the failure handling
+ * exercised, and the schedule's balance timed.  The pages have no
+ * counterpart.
  *   - wait_limit_ns (> 0) replaces the one-second limit of every device wait
  *     of the verify kernel for this call;
  *   - withhold_item (-1: none; else an item b * H + h) is an item whose
@@ -297,11 +305,18 @@ kda_status kda_verify(const kda_verify_args *args, kda_stream_t stream);
  *     after wait_limit_ns, KDA_DEVERR_TIMEOUT is set in the workspace, the
  *     CTA that owns the item stops (its later items are left unwritten) and
  *     the kernel returns; the other CTAs' items are verified as by kda_verify.
+ *     Withholding runs the CUDA-core verify whatever args->variant says;
+ *   - cta_times (NULL: none) is a device array of at least 2 * B * H
+ *     entries: verify-kernel CTA i writes the global timer (ns) at its start
+ *     to entry 2 i and at its finish (after all its roles) to 2 i + 1.  The
+ *     kernel has min(B * H, the device's SM count) CTAs; later entries are
+ *     left as they were.
  * Everything else is as for kda_verify (the conv pass runs for every item).
  */
 typedef struct kda_debug_args {
     int64_t wait_limit_ns;   /* > 0                                      */
     int32_t withhold_item;   /* -1, or an item in [0, B * H)            */
+    uint64_t *cta_times;     /* NULL, or device [>= 2 * B * H], 8-aligned */
 } kda_debug_args;
 
 kda_status kda_verify_debug(const kda_verify_args *args, const kda_debug_args *debug, kda_stream_t stream);
@@ -338,8 +353,9 @@ kda_status kda_commit(const kda_commit_args *args, kda_stream_t stream);
 #define KDA_NOALLOC_MAX_LAYERS 64
 kda_status kda_commit_noalloc(const kda_commit_args *args, kda_stream_t stream);
 
-/* Bytes of device workspace for the error report (int32-aligned, zeroed by
- * the caller before first use; the library only ORs bits into it). */
+/* Bytes of device workspace (int32-aligned, zeroed by the caller before
+ * first use): the error report, into which the kernels OR bits, and the
+ * verify's ticket counter, which each verify launch returns to zero. */
 size_t kda_workspace_bytes(void);
 
 /* Synchronise `stream`, copy workspace[0] into *flags, and return KDA_OK if

@@ -77,7 +77,7 @@ VARIANTS = {"auto": 0, "cuda_core": 1, "tcgen05": 2}
 
 class DebugArgs(ctypes.Structure):
     """Mirror of ``kda_debug_args``."""
-    _fields_ = [("wait_limit_ns", _i64), ("withhold_item", _i32)]
+    _fields_ = [("wait_limit_ns", _i64), ("withhold_item", _i32), ("cta_times", _p)]
 
 
 class AlignArgs(ctypes.Structure):
@@ -171,7 +171,8 @@ def new_verify_scratch(B: int, H: int, K: int, window: int, device) -> torch.Ten
 
 
 def new_workspace(device) -> torch.Tensor:
-    """A zeroed device workspace for the error report."""
+    """A zeroed device workspace: the error report and the verify's ticket
+    counter (allocated by torch on the current stream)."""
     return torch.zeros((workspace_bytes() + 3) // 4, dtype=torch.int32, device=device)
 
 
@@ -243,11 +244,17 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
     K, window)`` bytes for the conv pass's output; when None, one is taken
     from torch's allocator on the launch stream for this call.  ``variant``
     ("auto", "cuda_core" or "tcgen05") picks the kernel of the products (the
-    tensor cores need K = 128).
+    tensor cores need K = 128).  ``workspace`` (``new_workspace``) holds the
+    device error report and the ticket counter that deals the items to the
+    kernel's CTAs; when None, a fresh one is allocated for this call.  Calls
+    that may overlap on different streams need different workspaces.
 
-    ``debug`` = (withhold_item, wait_limit_ns) calls ``kda_verify_debug``
-    instead: the item's inputs are withheld and every device wait gives up
-    after wait_limit_ns (a test of the bounded waits; CUDA cores, no fold)."""
+    ``debug`` = (withhold_item, wait_limit_ns[, cta_times]) calls
+    ``kda_verify_debug`` instead (no fold): item ``withhold_item`` (-1: none)
+    has its inputs withheld and every device wait gives up after
+    wait_limit_ns (a test of the bounded waits, on the CUDA cores); an int64
+    ``cta_times`` [>= 2 B H] receives each verify CTA's start and finish on
+    the GPU's global timer (ns)."""
     dev = state.device
     if dev.type != "cuda":
         raise ValueError("verify runs on a CUDA device; state is on " + str(dev))
@@ -298,6 +305,12 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
                 raise ValueError(f"{name} must be contiguous with at least B entries")
     if workspace is not None:
         _need(workspace, "workspace", torch.int32, dev)
+        if workspace.numel() * 4 < workspace_bytes() or not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous with at least workspace_bytes() bytes")
+    else:
+        # the verify's ticket counter needs one; tied to the launch stream
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream(dev)):
+            workspace = new_workspace(dev)
     fold = None
     if fold_query_start_loc is not None:
         if fold_num_accepted is None:
@@ -354,6 +367,12 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
             raise ValueError("debug runs the plain verify (no fold)")
         d = DebugArgs()
         d.withhold_item, d.wait_limit_ns = int(debug[0]), int(debug[1])
+        if len(debug) > 2 and debug[2] is not None:
+            times = debug[2]
+            if times.device != dev or times.dtype != torch.int64 or not times.is_contiguous() \
+                    or times.numel() < 2 * B * H:
+                raise ValueError("cta_times must be a contiguous int64 tensor of >= 2*B*H on the state's device")
+            d.cta_times = times.data_ptr()
         _check(load_library().kda_verify_debug(ctypes.byref(a), ctypes.byref(d), handle))
     elif fold is None:
         _check(load_library().kda_verify(ctypes.byref(a), handle))

@@ -54,11 +54,11 @@ extern "C" {
 
 int32_t kda_abi_version(void) { return KDA_ABI_VERSION; }
 
-size_t kda_workspace_bytes(void) { return 16; }
+size_t kda_workspace_bytes(void) { return kda::kWsWords * sizeof(int32_t); }
 
 size_t kda_verify_scratch_bytes(int32_t B, int32_t H, int32_t K, int32_t Q) {
   if (B <= 0 || H <= 0 || K <= 0 || Q <= 0) return 0;
-  return static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(Q) * 4u * static_cast<size_t>(K) * 2u;
+  return static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(kda::scratch_item_elems(Q, K)) * 2u;
 }
 
 
@@ -79,6 +79,9 @@ kda_status verify_params(const kda_verify_args* a, bool fold, kda::VerifyParams&
   if (a->W != kConvWidth) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: conv width %d, supported %d", a->W, kConvWidth);
   if ((long long)a->T > (long long)a->B * a->Q)
     return fail(KDA_ERR_INVALID_ARG, "kda_verify: %d token rows exceed B*Q = %lld", a->T, (long long)a->B * a->Q);
+  // the ticket counter of the verify's schedule lives in the workspace
+  if (a->workspace == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify: workspace is NULL (required)");
+  if (!aligned(a->workspace, 4)) return fail(KDA_ERR_MISALIGNED, "kda_verify: workspace must be 4-byte aligned");
   // the fold still has work when no token row is left
   if (a->B == 0 || (a->T == 0 && !fold)) {
     *noop = true;
@@ -161,7 +164,9 @@ kda_status verify_params(const kda_verify_args* a, bool fold, kda::VerifyParams&
   p.scratch = static_cast<uint16_t*>(a->scratch);
   p.wait_limit_ns = 1000000000ull;  // every device wait gives up after about a second
   p.withhold_item = -1;
-  if ((long long)p.B * p.H > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: B*H too large");
+  p.cta_times = nullptr;
+  // the ticket counter runs to B*H plus one ticket per CTA
+  if ((long long)p.B * p.H > 0x7fff0000LL) return fail(KDA_ERR_UNSUPPORTED, "kda_verify: B*H too large");
   return KDA_OK;
 }
 
@@ -205,10 +210,13 @@ kda_status kda_verify_debug(const kda_verify_args* a, const kda_debug_args* d, k
   if (st != KDA_OK || noop) return st;
   if (d->withhold_item < -1 || static_cast<long long>(d->withhold_item) >= static_cast<long long>(a->B) * a->H)
     return fail(KDA_ERR_INVALID_ARG, "kda_verify_debug: withhold_item %d is not -1 or an item", d->withhold_item);
+  if (!aligned(d->cta_times, 8)) return fail(KDA_ERR_MISALIGNED, "kda_verify_debug: cta_times must be 8-byte aligned");
   p.wait_limit_ns = static_cast<unsigned long long>(d->wait_limit_ns);
   p.withhold_item = d->withhold_item;
-  // the CUDA-core verify: the path whose abort sequence this hook exercises
-  cudaError_t e = kda::launch_verify(p, a->K, KDA_VERIFY_CUDA_CORE, reinterpret_cast<cudaStream_t>(stream));
+  p.cta_times = reinterpret_cast<unsigned long long*>(d->cta_times);
+  // withholding exercises the abort sequence of the CUDA-core verify
+  const int variant = d->withhold_item >= 0 ? KDA_VERIFY_CUDA_CORE : a->variant;
+  cudaError_t e = kda::launch_verify(p, a->K, variant, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "kda_verify_debug: launch failed: %s", cudaGetErrorString(e));
   return KDA_OK;
 }

@@ -236,6 +236,15 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // Order this thread's generic shared-memory writes before later async-proxy reads.
 __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch: wait until the grid launched before this one
+// in the stream has completed with its memory visible (a no-op when this grid
+// was launched without the attribute), then order that view before this
+// thread's later bulk copies, which read through the async proxy.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------
 // bf16 conversions
 // ----------------------------------------------------------------------------
@@ -252,7 +261,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 // ("vllm.models.kimi_k3.nvidia.specialized_decode.recoverssm.state",
 // deferred_recoverssm_verify: causal_conv1d_update with activation "silu",
 // output in the activation dtype).  Three tiers decide it:
-//   1. fp32 (conv_silu_bf16x2, both tokens of a pair on the packed fp32x2
+//   1. fp32 (conv_silu_bf16x2, two codes at once on the packed fp32x2
 //      unit): y by an fma chain, SiLU by the procedure in silu_f32x2, and a
 //      bound E on |computed - exact|.  When no bf16 rounding boundary lies
 //      within E of the computed value, the hardware rounding of it is the
@@ -322,10 +331,11 @@ __device__ __forceinline__ float2 silu_f32x2(float2 y, float2& sigma) {
 constexpr float kSiluRelErr = 6.0f * 0x1p-24f;
 constexpr float kTier1MinY = -80.0f;
 
-// Tier 1: the bf16 codes of SiLU(sum_j w_j x_j) for two windows xa, xb of one
-// channel (W = 4 taps, oldest first; the low half of the result holds a, the
-// high half b), and in bits 0 / 1 of *doubt whether the code of a / b must be
-// decided by the exact tiers.
+// Tier 1: the bf16 codes of SiLU(sum_j w_j x_j) for two windows a and b,
+// each with its own weights (W = 4 taps, oldest first): two channels at one
+// token, or two tokens of one channel.  The low half of the result holds a,
+// the high half b; bits 0 / 1 of *doubt tell whether the code of a / b must
+// be decided by the exact tiers.
 //
 // The fma chain starts from +0, so an exactly zero sum is +0 (SiLU(0) = +0).
 // Its error dy is at most u (|y_2| + |y_3| + |y_4|) over the partial sums y_k,
@@ -342,14 +352,14 @@ constexpr float kTier1MinY = -80.0f;
 // below 2^-20 s^2 (the next midpoint is at least 2^-10 |s| away).  The
 // constants carry slack for the bound's own rounding; the 2^-126 term makes
 // every |s| below 2^-63 doubtful, where the squares leave the normal range.
-__device__ __forceinline__ uint32_t conv_silu_bf16x2(const float w[4], const float xa[4], const float xb[4], float e0,
-                                                     uint32_t* doubt) {
+__device__ __forceinline__ uint32_t conv_silu_bf16x2(const float wa[4], const float wb[4], const float xa[4],
+                                                     const float xb[4], float e0, uint32_t* doubt) {
   constexpr float k4U2 = 0x1.0001p-46f;                            // 4 u^2
   constexpr float k2Eps2 = 2.0f * 36.0f * 0x1p-48f * 1.0001f;       // 2 kSiluRelErr^2
-  const float2 y1 = __ffma2_rn(f2(w[0]), make_float2(xa[0], xb[0]), f2(0.0f));
-  const float2 y2 = __ffma2_rn(f2(w[1]), make_float2(xa[1], xb[1]), y1);
-  const float2 y3 = __ffma2_rn(f2(w[2]), make_float2(xa[2], xb[2]), y2);
-  const float2 y = __ffma2_rn(f2(w[3]), make_float2(xa[3], xb[3]), y3);
+  const float2 y1 = __ffma2_rn(make_float2(wa[0], wb[0]), make_float2(xa[0], xb[0]), f2(0.0f));
+  const float2 y2 = __ffma2_rn(make_float2(wa[1], wb[1]), make_float2(xa[1], xb[1]), y1);
+  const float2 y3 = __ffma2_rn(make_float2(wa[2], wb[2]), make_float2(xa[2], xb[2]), y2);
+  const float2 y = __ffma2_rn(make_float2(wa[3], wb[3]), make_float2(xa[3], xb[3]), y3);
   float2 sigma;
   const float2 s = silu_f32x2(y, sigma);
   // dy^2 bound

@@ -7,6 +7,24 @@
 
 namespace kda {
 
+// Workspace words (int32): [0] the error bits, [1] the item of the last
+// report, [kWsTicket] the verify's next work item and [kWsDone] its finished
+// CTAs (both zero between launches).
+constexpr int kWsTicket = 8;
+constexpr int kWsDone = 9;
+constexpr int kWsWords = 16;
+
+// The conv pass's block per (request, head) item in the scratch: [Q][2K] bf16
+// rows q | v, [Q][2K] rows k | raw gate, then 8 fp32 sigmoid(raw beta) (of
+// which the first n are written).  In uint16 elements.
+constexpr int kScratchBetaBytes = 32;
+#if defined(__CUDACC__)
+__host__ __device__
+#endif
+constexpr long long scratch_item_elems(int Q, int K) {
+  return 4LL * Q * K + kScratchBetaBytes / 2;
+}
+
 struct VerifyParams {
   int B, H, Q, T, null_block_id;
   long long num_slots, num_record_rows;
@@ -25,8 +43,8 @@ struct VerifyParams {
   const int* qsl; const int* state_indices; const int* record_indices; const int* num_accepted_prev;
   int* workspace;
   float k_scale;  // K^-1/2
-  // the conv pass's output: per (request, head) item a block of [Q][2K] bf16
-  // rows q | v, then [Q][2K] rows k | raw gate
+  // the conv pass's output: per (request, head) item a block of
+  // scratch_item_elems(Q, K) uint16 (layout above)
   uint16_t* scratch;
   // fp32 state pool [slots][H V][K] in K-slices of 32 (128-byte swizzle), for
   // the tensor-core path of the verify
@@ -40,6 +58,9 @@ struct VerifyParams {
   // -1: none)
   unsigned long long wait_limit_ns;
   int withhold_item;
+  // kda_verify_debug: per CTA the global timer at its start and finish, or
+  // nullptr
+  unsigned long long* cta_times;
 };
 
 struct CommitParams {

@@ -8,8 +8,12 @@
 //   conv_kernel    one CTA per (request, head): the conv + SiLU codes of the
 //                  head's q, k and v channels, correctly rounded to bf16, and
 //                  the rolled conv state; the codes go, with the raw gate
-//                  rows, into the item's block of the caller's scratch;
-//   verify_kernel  the verify proper, below.
+//                  rows and the beta gates, into the item's block of the
+//                  caller's scratch;
+//   verify_kernel  the verify proper, below, launched as the conv pass's
+//                  programmatic dependent: its CTAs set up and stream state
+//                  while the conv pass drains, and wait for it before the
+//                  first read of the scratch.
 //
 // Math.  The window is applied in closed form rather than step by step.
 // With D_t = prod_{j<=t} e^{g_j} (per key channel),
@@ -20,14 +24,16 @@
 // o = S q^ expanded: the checkpoint S0 is read once (2n FMAs per element) and
 // never written (except by the fold variant, which writes the folded state).
 //
-// Schedule of the verify kernel.  One persistent CTA per SM walks the
-// (request, head) items blockIdx.x + i * gridDim.x (local index i) with four
-// roles that meet only at mbarrier rings in shared memory, so the stages of
-// consecutive items overlap:
-//   inputs (1 warp)  reads request metadata 32 items per round trip and
-//                    copies each item's rows of the conv pass's block
-//                    (q | v, then k | gate) and its head's dt_bias into a
-//                    ring of small slots (bulk copies);
+// Schedule of the verify kernel.  One persistent CTA per SM takes
+// (request, head) items from a ticket counter until none are left (the
+// schedule, at the inputs warp) and works them with four roles that meet
+// only at mbarrier rings in shared memory, so the stages of consecutive items
+// overlap:
+//   inputs (1 warp)  draws the tickets, decodes each item's request metadata
+//                    a few items ahead (a ring of headers, which the state
+//                    warp follows) and copies each item's rows of the conv
+//                    pass's block (q | v, then k | gate) and its head's
+//                    dt_bias into a ring of small slots (bulk copies);
 //   state (1 warp)   streams each live item's 64 KB fp32 state as eight row
 //                    chunks into a ring of chunk slots, running ahead of the
 //                    arithmetic by two to three items;
@@ -73,28 +79,28 @@ constexpr int kMmaWarp = 2 + kPrepWarps + kSplitWarps;  // warp 12 issues the MM
 constexpr int ru(int x, int a) { return (x + a - 1) / a * a; }
 
 // Kernel variants: the CUDA-core verify, the tcgen05 verify (K = 128: the
-// default for windows of 8, forced by KDA_VERIFY_TCGEN05), and the
+// default for windows of 8; kda_verify_args.variant chooses), and the
 // CUDA-core verify that first folds each request's pending records of the
 // previous step into its checkpoint.
 enum : int { kVarPlain = 0, kVarTcgen05 = 1, kVarFold = 2 };
 
-enum : int { kLive = 1, kNull = 2 };
+// Item flags.  kEnd marks the end of a CTA's item sequence: the tickets ran out.
+enum : int { kLive = 1, kNull = 2, kEnd = 4 };
 
-// Inputs warp -> prep, per item.
+// Inputs warp -> state warp (ticket ring) and -> prep (small slot header),
+// per item: the decoded request metadata of item `item` = b H + h.
 template <int QMAX>
 struct SmallMeta {
-  int flags, bos, n, a;
-  long long s, r;
+  int flags, item, bos, n, a;
+  int fold_m;  // fold variant: pending records to fold, and their row
+  long long s, r, fold_r;
   float A, pad;
-  float beta[QMAX];
-  int fold_m, pad2;  // fold variant: pending records to fold, their row
-  long long fold_r;
 };
 
 // Prep -> gemv, per item (head of an operand slot).
 template <int QMAX>
 struct OpMeta {
-  int flags, bos, n, pad;
+  int flags, bos, n, h;
   long long r;
   float beta[QMAX];
   int fold_m, pad2;   // fold variant: pending records folded into the chunk,
@@ -109,20 +115,30 @@ struct Layout {
   // products S0 [X | Y] come from tcgen05 MMAs; otherwise CUDA-core gemv warps.
   static_assert(VAR != kVarTcgen05 || (KD == 128 && (QMAX == 4 || QMAX == 8)), "the tensor-core path covers K = 128");
   static_assert(VAR != kVarFold || QMAX <= 4, "the fold variant covers windows up to 4");
+  static_assert(QMAX * 4 <= kScratchBetaBytes, "the block's beta area holds a window");
   static constexpr bool kTC = VAR == kVarTcgen05;
   static constexpr bool kFold = VAR == kVarFold;
   static constexpr int kThreads = 32 * (kTC ? kMmaWarp + 1 : 2 + kPrepWarps + kGemvWarps);
   static constexpr int RW = KD / kGemvWarps;  // state rows per gemv warp (one chunk)
   static constexpr int kChunk = kTC ? 128 * 32 * 4 : RW * KD * 4;  // bytes per state unit (chunk or K-slice)
   static constexpr int kNumSmall = QMAX <= 4 ? 3 : 2;  // small-input ring
+  // ticket ring (inputs warp -> state warp): the inputs warp keeps kLead
+  // items drawn and decoded ahead of its copies, in batches of up to
+  // kMaxBatch; an entry is free again once both producer warps have read it
+  static constexpr int kLead = 3;
+  static constexpr int kMaxBatch = 8;
+  static constexpr int kTick = 16;
+  static constexpr int kTickBytes = ru(int(sizeof(SmallMeta<QMAX>)), 16);
   // small slot: the item's rows of the conv pass's block (q | v rows, then
   // k | gate rows, [QMAX][2K] bf16 each) and its head's dt_bias
   static constexpr int kQV = ru(int(sizeof(SmallMeta<QMAX>)), 128);
   static constexpr int kKG = kQV + QMAX * 2 * KD * 2;
   static constexpr int kDt = kKG + QMAX * 2 * KD * 2;                  // [KD] dt_bias
+  static constexpr int kBeta = kDt + KD * 4;  // [8] fp32 sigmoid(raw beta), from the conv pass's block
+  static constexpr int kBetaBytes = kScratchBetaBytes;
   // fold variant: the pending records of the item, [QMAX][2K] bf16 key/gate
   // and [QMAX][V] fp32 corrections (V == K)
-  static constexpr int kFoldKg = ru(kDt + KD * 4, 128);
+  static constexpr int kFoldKg = ru(kBeta + kBetaBytes, 128);
   static constexpr int kFoldC = kFoldKg + (kFold ? QMAX * 2 * KD * 2 : 0);
   static constexpr int kSmall = ru(kFoldC + (kFold ? QMAX * KD * 4 : 0), 128);
   // operand slot (prep -> gemv).  Tensor-core path: first the MMA's B operand,
@@ -151,8 +167,8 @@ struct Layout {
   static constexpr int kFoldIdx = 2 * QMAX + QMAX * QMAX;  // fold variant: |k_u|^2 of the pending keys
   static constexpr int kPart = ru(kFoldIdx + (kFold ? QMAX : 0), 32);         // reduced values per prep warp
   static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kGemvWarps * kRedPerWarp * 4 +
-                                kPrepWarps * kPart * 4 + 32 + 64 + (2 * kNumSmall + 2 * kNumOp + 4) * 8 +
-                                (kTC ? 1024 : 0);
+                                kPrepWarps * kPart * 4 + 32 + 64 + kTick * kTickBytes +
+                                (2 * kNumSmall + 2 * kNumOp + 4 + 2 * kTick) * 8 + (kTC ? 1024 : 0);
   static constexpr int kBarsPerChunk = kTC ? 4 : 2;
   static constexpr int kChunkFit = (kSmemLimit - kFixed - 64 * kBarsPerChunk * 8) / kChunk;
   static constexpr int kNumChunk = kChunkFit > 64 ? 64 : kChunkFit;
@@ -164,19 +180,23 @@ struct Layout {
   static constexpr int oPart = oRed + kGemvWarps * kRedPerWarp * 4;
   static constexpr int oMisc = oPart + kPrepWarps * kPart * 4;  // int[8]
   static constexpr int oArm = oMisc + 32;                      // uint8[64]: last armed phase per chunk slot
-  static constexpr int oBars = ru(oArm + 64, 8);
-  static constexpr int kNumBars = kBarsPerChunk * kNumChunk + 2 * kNumSmall + 2 * kNumOp + 4;
+  static constexpr int oTick = ru(oArm + 64, 16);               // SmallMeta[kTick]: the ticket ring
+  static constexpr int oBars = ru(oTick + kTick * kTickBytes, 8);
+  static constexpr int kNumBars = kBarsPerChunk * kNumChunk + 2 * kNumSmall + 2 * kNumOp + 4 + 2 * kTick;
   static constexpr int kBytes = oBars + kNumBars * 8;
   static_assert(kBytes <= kSmemLimit, "shared memory budget");
   // at least six K-slices (tensor cores), 1.5 items of chunks (fold variant,
   // whose slots carry the pending records) or two items of chunks in flight
   static_assert(kNumChunk >= (kTC ? 6 : kFold ? 3 * kGemvWarps / 2 : 2 * kGemvWarps), "state in flight");
   static_assert(kNumChunk <= 64, "one record of the last armed phase per chunk slot");
+  static_assert(kTick >= kLead + kMaxBatch + 1, "the ticket ring holds the drawer's lead and a batch");
+  static_assert(kMaxBatch <= 32, "one lane per item of a batch");
 };
 
 template <int KD, int QMAX, int VAR>
 struct Bars {
   uint64_t *ch_full, *ch_empty, *sm_full, *sm_empty, *op_full, *op_empty, *d_full, *d_empty, *hi_done, *lo_full;
+  uint64_t *tk_full, *tk_empty;
   __device__ explicit Bars(unsigned char* smem) {
     using Lay = Layout<KD, QMAX, VAR>;
     uint64_t* b = reinterpret_cast<uint64_t*>(smem + Lay::oBars);
@@ -188,7 +208,9 @@ struct Bars {
     op_empty = op_full + Lay::kNumOp;
     d_full = op_empty + Lay::kNumOp;   // [2] tensor-core path
     d_empty = d_full + 2;              // [2]
-    hi_done = d_empty + 2;             // [kNumChunk]
+    tk_full = d_empty + 2;             // [kTick]
+    tk_empty = tk_full + Lay::kTick;   // [kTick]
+    hi_done = tk_empty + Lay::kTick;   // [kNumChunk] tensor-core path
     lo_full = hi_done + Lay::kNumChunk;  // [kNumChunk]
   }
 };
@@ -213,12 +235,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
   return ok;
 }
 
-// Number of local items of this CTA.
-__device__ __forceinline__ int local_items(int items) {
-  const int base = static_cast<int>(blockIdx.x);
-  return base < items ? (items - base + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 0;
-}
-
 // Per-item request metadata, decoded by one lane (both producer warps decode
 // identically; only the inputs warp reports device errors).
 template <int QMAX>
@@ -229,22 +245,49 @@ struct ItemMeta {
   long long fold_r;
 };
 
+// The raw request values an item's metadata is made of: one round of
+// independent loads (it < 0: none).
+struct ItemLoads {
+  int it, q0, q1, si, ri, nap, fq0, fq1, fna, fri;
+  float alog;
+};
+
+__device__ __forceinline__ ItemLoads load_item(const VerifyParams& p, int it) {
+  ItemLoads l{it, 0, 0, 0, 0, 1, 0, 0, 0, 0, 0.0f};
+  if (it < 0) return l;
+  const int b = it / p.H;
+  l.q0 = p.qsl[b];
+  l.q1 = p.qsl[b + 1];
+  l.si = p.state_indices[b];
+  l.ri = p.record_indices ? p.record_indices[b] : l.si;
+  l.nap = p.num_accepted_prev ? p.num_accepted_prev[b] : 1;
+  if (p.fold_qsl != nullptr) {
+    l.fq0 = p.fold_qsl[b];
+    l.fq1 = p.fold_qsl[b + 1];
+    l.fna = p.fold_num_accepted[b];
+    l.fri = p.fold_record_indices ? p.fold_record_indices[b] : l.si;
+  }
+  l.alog = p.A_log[it - b * p.H];
+  return l;
+}
+
 template <int QMAX>
-__device__ __forceinline__ ItemMeta<QMAX> decode_item(const VerifyParams& p, int it, bool valid, bool report_errors) {
+__device__ __forceinline__ ItemMeta<QMAX> item_meta(const VerifyParams& p, const ItemLoads& l, bool report_errors) {
   ItemMeta<QMAX> m{0, 0, 0, 0, 1, 0, 0, 0, 0};
-  if (!valid) return m;
+  if (l.it < 0) return m;
+  const int it = l.it;
   const int b = it / p.H;
   m.h = it - b * p.H;
-  m.bos = p.qsl[b];
-  const int len = p.qsl[b + 1] - m.bos;
-  m.s = p.state_indices[b];
-  m.r = p.record_indices ? static_cast<long long>(p.record_indices[b]) : m.s;
-  m.a = p.num_accepted_prev ? min(max(p.num_accepted_prev[b], 1), p.Q) : 1;
+  m.bos = l.q0;
+  const int len = l.q1 - m.bos;
+  m.s = l.si;
+  m.r = l.ri;
+  m.a = min(max(l.nap, 1), p.Q);
   m.n = min(max(len, 0), p.Q);
   if (p.fold_qsl != nullptr) {  // the previous step's pending records, folded first
-    const int plen = p.fold_qsl[b + 1] - p.fold_qsl[b];
-    m.fold_m = min(max(p.fold_num_accepted[b], 0), min(max(plen, 0), p.Q));
-    m.fold_r = p.fold_record_indices ? static_cast<long long>(p.fold_record_indices[b]) : m.s;
+    const int plen = l.fq1 - l.fq0;
+    m.fold_m = min(max(l.fna, 0), min(max(plen, 0), p.Q));
+    m.fold_r = l.fri;
   }
   if (len < 0 || (m.n > 0 && (m.bos < 0 || m.bos + m.n > p.T))) {
     if (report_errors) report(p.workspace, KDA_DEVERR_TOKEN_RANGE, it);
@@ -266,123 +309,172 @@ __device__ __forceinline__ ItemMeta<QMAX> decode_item(const VerifyParams& p, int
 // ---------------------------------------------------------------- conv pass
 //
 // The short causal conv in front of the verify, as its own launch: one CTA
-// per (request, head) item.  Per channel it reads the W - 1 stored
+// per (request, head) item, 3K/2 threads, each on two adjacent channels of
+// one of the head's q, k and v groups.  Per channel it reads the W - 1 stored
 // taps from tap a - 1 and the window's inputs, evaluates the bf16 codes of
-// SiLU(conv) (tier 1 of kda_device.cuh; the rare codes it leaves in doubt go
-// to the exact tiers, out of line), and rolls the conv state in place
-// (taps 0 .. W-3+n <- seq[1 .. W-2+n], later taps untouched).  The codes go,
-// with the raw gate rows, into the item's block of the caller's scratch:
-// [Q][2K] bf16 rows q | v, then [Q][2K] rows k | raw gate, rows t < n
-// written.  The second half is the item's key / gate record verbatim.
-// Null items, empty windows and items with bad metadata are skipped here;
-// the verify kernel reports the latter.
+// SiLU(conv) (tier 1 of kda_device.cuh, both channels of the pair at once;
+// the rare codes it leaves in doubt go to the exact tiers, out of line), and
+// rolls the conv state in place (taps 0 .. W-3+n <- seq[1 .. W-2+n], later
+// taps untouched).  The codes go, with the raw gate rows, into the item's
+// block of the caller's scratch: [Q][2K] bf16 rows q | v, then [Q][2K] rows
+// k | raw gate, rows t < n written, then the window's beta gates
+// sigmoid(raw beta) in fp32.  The k | gate rows are the item's key / gate
+// record verbatim.  Null items, empty windows and items with bad metadata are
+// skipped here; the verify kernel reports the latter.
+//
+// A pair's values travel as 32-bit words, channel c in the low half and
+// c + 1 in the high half: that is the layout of the activations, the seq-first
+// conv state and the scratch rows, so a pair costs one access where the rows
+// allow it (an even stride from a 4-byte aligned start, checked once per
+// launch; two 16-bit accesses otherwise).
+
+__device__ __forceinline__ float lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two adjacent bf16 values from a row; w32: the pair sits on 4 bytes.
+__device__ __forceinline__ uint32_t load_pair(const uint16_t* ptr, bool w32) {
+  if (w32) return __ldg(reinterpret_cast<const unsigned int*>(ptr));
+  return static_cast<uint32_t>(__ldg(ptr)) | (static_cast<uint32_t>(__ldg(ptr + 1)) << 16);
+}
+
+__device__ __forceinline__ void store_pair(uint16_t* ptr, uint32_t v, bool w32) {
+  if (w32) {
+    *reinterpret_cast<uint32_t*>(ptr) = v;
+  } else {
+    ptr[0] = static_cast<uint16_t>(v & 0xffffu);
+    ptr[1] = static_cast<uint16_t>(v >> 16);
+  }
+}
+
+// The codes of one channel pair: sq[j] holds both channels' sequence value j
+// (the W - 1 taps, then the window); y[t] the two codes of token t.
 template <int QMAX>
-__device__ __forceinline__ void channel_codes(const float (&w)[kConvWidth], const uint16_t (&seq)[kConvWidth + QMAX],
-                                              int n, float e0, uint16_t (&y)[QMAX]) {
+__device__ __forceinline__ void pair_codes(const float (&wa)[kConvWidth], const float (&wb)[kConvWidth],
+                                           const uint32_t (&sq)[kConvWidth - 1 + QMAX], int n, float e0,
+                                           uint32_t (&y)[QMAX]) {
   uint32_t doubt = 0;
 #pragma unroll
-  for (int pr = 0; pr < (QMAX + 1) / 2; ++pr) {
-    const int t = 2 * pr;
+  for (int t = 0; t < QMAX; ++t) {
     y[t] = 0;
-    if (t + 1 < QMAX) y[t + 1] = 0;
     if (t < n) {
-      const float xa[kConvWidth] = {bf16_to_f32(seq[t]), bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]),
-                                    bf16_to_f32(seq[t + 3])};
-      const float xb[kConvWidth] = {bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]), bf16_to_f32(seq[t + 3]),
-                                    bf16_to_f32(seq[t + 4])};
+      const float xa[kConvWidth] = {lo_f32(sq[t]), lo_f32(sq[t + 1]), lo_f32(sq[t + 2]), lo_f32(sq[t + 3])};
+      const float xb[kConvWidth] = {hi_f32(sq[t]), hi_f32(sq[t + 1]), hi_f32(sq[t + 2]), hi_f32(sq[t + 3])};
       uint32_t d;
-      const uint32_t yy = conv_silu_bf16x2(w, xa, xb, e0, &d);
-      y[t] = static_cast<uint16_t>(yy & 0xffffu);
-      if (t + 1 < QMAX) y[t + 1] = static_cast<uint16_t>(yy >> 16);
-      doubt |= d << t;
+      y[t] = conv_silu_bf16x2(wa, wb, xa, xb, e0, &d);
+      doubt |= d << (2 * t);
     }
   }
-  doubt &= (1u << n) - 1u;
   if (doubt) {  // a few codes in 10^4
 #pragma unroll
-    for (int t = 0; t < QMAX; ++t)
-      if ((doubt >> t) & 1u)
-        y[t] = static_cast<uint16_t>(exact_conv::conv_code_exact(w[0], w[1], w[2], w[3], bf16_to_f32(seq[t]),
-                                                                 bf16_to_f32(seq[t + 1]), bf16_to_f32(seq[t + 2]),
-                                                                 bf16_to_f32(seq[t + 3])));
+    for (int t = 0; t < QMAX; ++t) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if ((doubt >> (2 * t + half)) & 1u) {
+          const int sh = 16 * half;
+          const float* w = half ? wb : wa;
+          const uint32_t code = static_cast<uint32_t>(exact_conv::conv_code_exact(
+              w[0], w[1], w[2], w[3], bf16_to_f32((sq[t] >> sh) & 0xffffu), bf16_to_f32((sq[t + 1] >> sh) & 0xffffu),
+              bf16_to_f32((sq[t + 2] >> sh) & 0xffffu), bf16_to_f32((sq[t + 3] >> sh) & 0xffffu)));
+          y[t] = (y[t] & (0xffff0000u >> sh)) | (code << sh);
+        }
+      }
+    }
   }
 }
 
 template <int KD, int QMAX, bool DF>
-__global__ void __launch_bounds__(KD) conv_kernel(const __grid_constant__ VerifyParams p) {
-  // Thread k takes channel k of each of q, k and v.  Two dependent memory
-  // round trips: the item's metadata with the channels' weights, then every
-  // tap, input and gate value of the window; then the codes and the stores.
+__global__ void __launch_bounds__(3 * KD / 2) conv_kernel(const __grid_constant__ VerifyParams p) {
+  // The verify kernel may start now: it waits for this grid before it reads
+  // the scratch, and its other work (state streaming) does not depend on it.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Two dependent memory round trips: the item's metadata with the pair's
+  // weights, then every tap, input and gate value of the window; then the
+  // codes and the stores.  Groups (q, k, v) are K/2 threads: whole warps.
   const int it = static_cast<int>(blockIdx.x);
-  const int k = static_cast<int>(threadIdx.x);
+  const int g = (2 * static_cast<int>(threadIdx.x)) / KD;  // 0: q, 1: k, 2: v
+  const int k = 2 * static_cast<int>(threadIdx.x) - g * KD;
   const int h = it - (it / p.H) * p.H;
   const long long HK = static_cast<long long>(p.H) * KD;
-  const long long c0 = static_cast<long long>(h) * KD + k;  // channel of group g: c0 + g HK
-  float w[3][kConvWidth];
-#pragma unroll
-  for (int g = 0; g < 3; ++g) {
-    if (p.conv_weight_fp32) {
-      const float4 wv = __ldg(reinterpret_cast<const float4*>(p.conv_weight) + c0 + g * HK);
-      w[g][0] = wv.x; w[g][1] = wv.y; w[g][2] = wv.z; w[g][3] = wv.w;
-    } else {
-      const uint2 wv = __ldg(reinterpret_cast<const uint2*>(p.conv_weight) + c0 + g * HK);
-      w[g][0] = bf16_to_f32(wv.x & 0xffff); w[g][1] = bf16_to_f32(wv.x >> 16);
-      w[g][2] = bf16_to_f32(wv.y & 0xffff); w[g][3] = bf16_to_f32(wv.y >> 16);
-    }
+  const long long c = g * HK + static_cast<long long>(h) * KD + k;  // the pair's first channel (even)
+  float wa[kConvWidth], wb[kConvWidth];
+  if (p.conv_weight_fp32) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p.conv_weight) + c);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p.conv_weight) + c + 1);
+    wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
+    wb[0] = b.x; wb[1] = b.y; wb[2] = b.z; wb[3] = b.w;
+  } else {
+    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(p.conv_weight) + c / 2);
+    wa[0] = lo_f32(wv.x); wa[1] = hi_f32(wv.x); wa[2] = lo_f32(wv.y); wa[3] = hi_f32(wv.y);
+    wb[0] = lo_f32(wv.z); wb[1] = hi_f32(wv.z); wb[2] = lo_f32(wv.w); wb[3] = hi_f32(wv.w);
   }
-  const ItemMeta<QMAX> im = decode_item<QMAX>(p, it, true, false);
+  const ItemMeta<QMAX> im = item_meta<QMAX>(p, load_item(p, it), false);
   if (!(im.flags & kLive) || im.n <= 0) return;
   const int n = im.n;
   const int Lc = p.Q + kConvWidth - 2;
+  const bool x32 = (p.qkv_stride & 1) == 0 && (reinterpret_cast<uintptr_t>(p.mixed_qkv) & 3u) == 0;
+  const bool g32 = (p.gate_stride & 1) == 0 && (reinterpret_cast<uintptr_t>(p.raw_gate) & 3u) == 0;
   uint16_t* cs = p.conv_state + im.s * p.conv_slot_stride;
-  const uint16_t* x = p.mixed_qkv + static_cast<long long>(im.bos) * p.qkv_stride;
-  // seq[g] = the W - 1 stored taps from tap a - 1, then the window (zero past n)
-  uint16_t seq[3][kConvWidth + QMAX];
-  uint16_t gate[QMAX];
+  const uint16_t* x = p.mixed_qkv + static_cast<long long>(im.bos) * p.qkv_stride + c;
+  // sq[j]: the W - 1 stored taps from tap a - 1, then the window (zero past n)
+  uint32_t sq[kConvWidth - 1 + QMAX];
+  uint32_t gate[QMAX];
 #pragma unroll
-  for (int g = 0; g < 3; ++g) {
-    const long long c = c0 + g * HK;
-#pragma unroll
-    for (int j = 0; j < kConvWidth - 1; ++j)
-      seq[g][j] = DF ? cs[c * Lc + im.a - 1 + j] : cs[static_cast<long long>(im.a - 1 + j) * 3 * HK + c];
-#pragma unroll
-    for (int t = 0; t < QMAX; ++t)
-      seq[g][kConvWidth - 1 + t] = t < n ? __ldg(x + static_cast<long long>(t) * p.qkv_stride + c) : uint16_t(0);
-    seq[g][kConvWidth - 1 + QMAX] = 0;
+  for (int j = 0; j < kConvWidth - 1; ++j) {
+    if (DF) {  // rows of Lc taps per channel: the pair's taps are Lc apart
+      const uint16_t* r = cs + c * Lc + im.a - 1 + j;
+      sq[j] = static_cast<uint32_t>(r[0]) | (static_cast<uint32_t>(r[Lc]) << 16);
+    } else {  // the slot is 16-byte aligned and rows are 3HK (even) wide
+      sq[j] = *reinterpret_cast<const uint32_t*>(cs + static_cast<long long>(im.a - 1 + j) * 3 * HK + c);
+    }
   }
+#pragma unroll
+  for (int t = 0; t < QMAX; ++t) sq[kConvWidth - 1 + t] = t < n ? load_pair(x + t * p.qkv_stride, x32) : 0u;
+  if (g == 1) {
+    const uint16_t* gr = p.raw_gate + static_cast<long long>(im.bos) * p.gate_stride + h * KD + k;
+#pragma unroll
+    for (int t = 0; t < QMAX; ++t) gate[t] = t < n ? load_pair(gr + t * p.gate_stride, g32) : 0u;
+  }
+  // thread t < n of the q group: the gate sigmoid(raw beta) of token t
+  const int tb = static_cast<int>(threadIdx.x);
+  const uint16_t rbeta = tb < n ? p.raw_beta[static_cast<long long>(im.bos + tb) * p.beta_stride + h] : uint16_t(0);
+  // the codes: a bf16 weight times a bf16 input is exact in fp32; an fp32 weight's product rounds
+  uint32_t y[QMAX];
+  pair_codes<QMAX>(wa, wb, sq, n, p.conv_weight_fp32 ? 1.0f : 0.0f, y);
+  // the item's block: q at [t][k], v at [t][K + k], k at [Q + t][k], gate at [Q + t][K + k]
+  uint16_t* blk = p.scratch + static_cast<long long>(it) * scratch_item_elems(p.Q, KD) + k;
+  uint16_t* dst = g == 0 ? blk : g == 2 ? blk + KD : blk + 2LL * p.Q * KD;
 #pragma unroll
   for (int t = 0; t < QMAX; ++t)
-    gate[t] = t < n ? __ldg(p.raw_gate + static_cast<long long>(im.bos + t) * p.gate_stride + c0) : uint16_t(0);
-  // the codes: a bf16 weight times a bf16 input is exact in fp32; an fp32 weight's product rounds
-  const float e0 = p.conv_weight_fp32 ? 1.0f : 0.0f;
-  uint16_t y[3][QMAX];
+    if (t < n) *reinterpret_cast<uint32_t*>(dst + t * 2 * KD) = y[t];
+  if (g == 1) {
 #pragma unroll
-  for (int g = 0; g < 3; ++g) channel_codes<QMAX>(w[g], seq[g], n, e0, y[g]);
-  // the item's block: q at [t][k], v at [t][K + k], k at [Q + t][k], gate at [Q + t][K + k]
-  uint16_t* blk = p.scratch + static_cast<long long>(it) * (4LL * p.Q * KD) + k;
-  uint16_t* kgr = blk + 2LL * p.Q * KD;
-#pragma unroll
-  for (int t = 0; t < QMAX; ++t) {
-    if (t < n) {
-      blk[t * 2 * KD] = y[0][t];
-      blk[t * 2 * KD + KD] = y[2][t];
-      kgr[t * 2 * KD] = y[1][t];
-      kgr[t * 2 * KD + KD] = gate[t];
-    }
+    for (int t = 0; t < QMAX; ++t)
+      if (t < n) *reinterpret_cast<uint32_t*>(dst + t * 2 * KD + KD) = gate[t];
   }
+  if (tb < n)
+    reinterpret_cast<float*>(p.scratch + static_cast<long long>(it) * scratch_item_elems(p.Q, KD) + 4LL * p.Q * KD)[tb] =
+        sigmoid_fast(bf16_to_f32(rbeta));
   // the rolled taps: 0 .. W-3+n <- seq[1 .. W-2+n], later taps untouched
+  if (DF) {
+    // rows c and c + 1 start Lc apart; c Lc is even, so row c takes 32-bit
+    // stores of tap pairs, and row c + 1 too when Lc is even
+    uint16_t* r0 = cs + c * Lc;
+    uint16_t* r1 = r0 + Lc;
+    const bool l32 = (Lc & 1) == 0;
 #pragma unroll
-  for (int g = 0; g < 3; ++g) {
-    const long long c = c0 + g * HK;
-#pragma unroll
-    for (int j = 0; j < kConvWidth - 2 + QMAX; ++j) {
-      if (j < kConvWidth - 2 + n) {
-        if (DF)
-          cs[c * Lc + j] = seq[g][j + 1];
-        else
-          cs[static_cast<long long>(j) * 3 * HK + c] = seq[g][j + 1];
+    for (int j = 0; j < kConvWidth - 2 + QMAX; j += 2) {
+      if (j + 1 < kConvWidth - 2 + n) {
+        store_pair(r0 + j, __byte_perm(sq[j + 1], sq[j + 2], 0x5410), true);
+        store_pair(r1 + j, __byte_perm(sq[j + 1], sq[j + 2], 0x7632), l32);
+      } else if (j < kConvWidth - 2 + n) {
+        r0[j] = static_cast<uint16_t>(sq[j + 1] & 0xffffu);
+        r1[j] = static_cast<uint16_t>(sq[j + 1] >> 16);
       }
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kConvWidth - 2 + QMAX; ++j)
+      if (j < kConvWidth - 2 + n) *reinterpret_cast<uint32_t*>(cs + static_cast<long long>(j) * 3 * HK + c) = sq[j + 1];
   }
 }
 
@@ -401,84 +493,150 @@ __device__ __forceinline__ void fold_copies(const VerifyParams& p, unsigned char
   bulk_g2s(sl + Lay::kFoldC, c, static_cast<uint32_t>(m) * KD * 4, bar);
 }
 
+// The schedule.  Items are dealt out at run time from a ticket counter in the
+// workspace: the inputs warp of each CTA takes the next item number with one
+// atomic, until the numbers run out, so a CTA that starts late (behind the
+// conv pass) or runs slow takes fewer items and the CTAs finish within about
+// an item of each other.  The last CTA to finish zeroes the counter for the
+// next launch (end of verify_kernel).
+//
+// The inputs warp draws and decodes kLead items ahead of its copies and puts
+// each item's header into the ticket ring, from which the state warp takes
+// its items (no metadata loads of its own) and from which the header later
+// goes into the item's small slot for the prep team.  After the last item,
+// an entry with item -1 ends the state warp's sequence and a header flagged
+// kEnd ends the prep team's, which forwards it to the gemv team.
+
+// The header of an item from its loads (item -1: none, the end mark); the
+// lane that decodes an item reports its metadata errors.
+template <int QMAX>
+__device__ __forceinline__ SmallMeta<QMAX> item_header(const VerifyParams& p, const ItemLoads& l) {
+  SmallMeta<QMAX> m;
+  const ItemMeta<QMAX> im = item_meta<QMAX>(p, l, l.it >= 0);
+  m.flags = l.it >= 0 ? im.flags : kEnd;
+  m.item = l.it;
+  m.bos = im.bos;
+  m.n = im.n;
+  m.a = im.a;
+  m.fold_m = im.fold_m;
+  m.s = im.s;
+  m.r = im.r;
+  m.fold_r = im.fold_r;
+  m.A = l.it >= 0 ? expf(l.alog) : 0.0f;
+  m.pad = 0.0f;
+  return m;
+}
+
 template <int KD, int QMAX, int VAR>
-__device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
+__device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int lane, volatile int* misc) {
   using Lay = Layout<KD, QMAX, VAR>;
+  using Meta = SmallMeta<QMAX>;
   Bars<KD, QMAX, VAR> bars(smem);
-  const int nloc = local_items(p.B * p.H);
+  volatile int* abort_flag = misc + kMiscAbort;
+  unsigned char* ring = smem + Lay::oTick;
+  const int items = p.B * p.H;
+  const int grid = static_cast<int>(gridDim.x);
+  int* counter = p.workspace + kWsTicket;
   bool ok = true;
+  int drawn = 0;       // ring entries written
+  bool ended = false;  // the entry with item -1 is written
+  int seen = 0;        // the counter's value at this CTA's last draw
+  // One draw: a batch of consecutive tickets sized from what is left (about
+  // a half of this CTA's fair share of the rest, at least one and at most
+  // kMaxBatch), decoded one item per lane in one round of loads, and its
+  // entries published; an empty draw publishes the end mark.  Large batches
+  // early keep the decode's code and round trips rare; single tickets at
+  // the end even out the CTAs' finish.
+  auto draw = [&]() {
+    int t0 = 0, k = 1;
+    if (lane == 0) {
+      k = min(max((items - seen) / (2 * grid), 1), Lay::kMaxBatch);
+      t0 = atomicAdd(counter, k);
+    }
+    t0 = __shfl_sync(0xffffffffu, t0, 0);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    seen = t0 + k;
+    const int nb = t0 < items ? min(k, items - t0) : 0;
+    const int count = nb > 0 ? nb : 1;
+    // the entries' slots are free once the last of them is (readers go in order)
+    const int last = drawn + count - 1;
+    ok = warp_wait(&bars.tk_empty[last % Lay::kTick], ((last / Lay::kTick) & 1) ^ 1, lane, abort_flag,
+                   p.wait_limit_ns);
+    if (!ok) return;
+    const int it = lane < nb ? t0 + lane : -1;
+    const Meta m = item_header<QMAX>(p, load_item(p, it));
+    if (lane < count) {
+      const int e = (drawn + lane) % Lay::kTick;
+      *reinterpret_cast<Meta*>(ring + e * Lay::kTickBytes) = m;
+      mbar_arrive(&bars.tk_full[e]);
+    }
+    __syncwarp();
+    drawn += count;
+    ended = nb == 0;
+  };
   // per small slot: whether this warp has armed a phase of its full barrier,
   // and that phase's parity (the copies behind it are waited for at exit)
   uint32_t armed = 0, armed_parity = 0;
-  for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
-    // metadata of up to 32 items, one per lane, in two round trips
-    const int it = static_cast<int>(blockIdx.x) + (i0 + lane) * static_cast<int>(gridDim.x);
-    const ItemMeta<QMAX> im = decode_item<QMAX>(p, it, i0 + lane < nloc, true);
-    const float A = (i0 + lane < nloc) ? expf(p.A_log[im.h]) : 0.0f;
-    float beta[QMAX];
-#pragma unroll
-    for (int t = 0; t < QMAX; ++t)
-      beta[t] = (im.flags == kLive && t < im.n)
-                    ? sigmoid_fast(bf16_to_f32(p.raw_beta[static_cast<long long>(im.bos + t) * p.beta_stride + im.h]))
-                    : 0.0f;
-    // lane j's own item: the per-item header the prep team reads
-    SmallMeta<QMAX> own;
-    own.flags = im.flags;
-    own.bos = im.bos;
-    own.n = im.n;
-    own.a = im.a;
-    own.s = im.s;
-    own.r = im.r;
-    own.A = A;
-    own.pad = 0.0f;
-#pragma unroll
-    for (int t = 0; t < QMAX; ++t) own.beta[t] = beta[t];
-    own.fold_m = im.fold_m;
-    own.pad2 = 0;
-    own.fold_r = im.fold_r;
-    const int count = min(32, nloc - i0);
-    for (int j = 0; j < count && ok; ++j) {
-      const int i = i0 + j;
-      const int jflags = __shfl_sync(0xffffffffu, im.flags, j);
-      const int jn = __shfl_sync(0xffffffffu, im.n, j);
-      const int jh = __shfl_sync(0xffffffffu, im.h, j);
-      const int jfm = Lay::kFold ? __shfl_sync(0xffffffffu, im.fold_m, j) : 0;
-      const long long jfr = Lay::kFold ? shfl_ll(im.fold_r, j) : 0;
-      // fold variant: the item's pending key/gate and correction records
-      const uint32_t fold_bytes = (jflags & kLive) ? static_cast<uint32_t>(jfm) * (2 * KD * 2 + KD * 4) : 0u;
-      const int slot = i % Lay::kNumSmall;
-      ok = warp_wait(&bars.sm_empty[slot], ((i / Lay::kNumSmall) & 1) ^ 1, lane, abort_flag, p.wait_limit_ns);
-      if (!ok) break;
-      unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
-      // kda_verify_debug: this item's inputs are withheld (no copy, no
-      // arrival), so the prep team's bounded wait on them runs out
-      if (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x) == p.withhold_item) continue;
+  for (int i = 0; ok; ++i) {
+    // at least kLead entries past this one are published (the first pass
+    // fills the lead); drawn before the wait for the slot, which it overlaps
+    // when the prep team is the slower side
+    while (ok && !ended && drawn <= i + Lay::kLead) draw();
+    // the conv pass's rows are read from here on (the headers so far come
+    // from the caller's metadata, not from it); every CTA waits, so this
+    // grid cannot complete before the conv pass has
+    if (i == 0) wait_prior_grid();
+    if (!ok) break;
+    const int e = i % Lay::kTick;
+    const Meta m = *reinterpret_cast<const Meta*>(reinterpret_cast<const unsigned char*>(ring) + e * Lay::kTickBytes);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.tk_empty[e]);
+    const int slot = i % Lay::kNumSmall;
+    ok = warp_wait(&bars.sm_empty[slot], ((i / Lay::kNumSmall) & 1) ^ 1, lane, abort_flag, p.wait_limit_ns);
+    if (!ok) break;
+    unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
+    // a phase armed here is the slot's last so far (the exit drain waits for
+    // the last one; a later phase of the slot would alias its parity)
+    auto arm = [&] {
       armed |= 1u << slot;
       armed_parity = (armed_parity & ~(1u << slot)) | (static_cast<uint32_t>((i / Lay::kNumSmall) & 1) << slot);
-      if (lane == j) *reinterpret_cast<SmallMeta<QMAX>*>(sl) = own;
-      __syncwarp();  // orders lane j's header before lane 0's arrival on sm_full
-      if (jflags & kLive) {
-        // the item's rows of the conv pass's block (q | v, then k | gate), its
-        // head's dt_bias and, in the fold variant, its pending records: a few
-        // bulk copies from lane 0
-        if (lane == 0) {
-          const uint32_t rows = static_cast<uint32_t>(jn) * 2 * KD * 2;
-          uint64_t* bar = &bars.sm_full[slot];
-          mbar_arrive_expect_tx(bar, 2 * rows + KD * 4 + fold_bytes);
-          if (fold_bytes) fold_copies<KD, QMAX, VAR>(p, sl, jh, jfm, jfr, bar);
+    };
+    if (m.item < 0) {  // no items left: the prep team's end mark
+      arm();
+      if (lane == 0) {
+        reinterpret_cast<Meta*>(sl)->flags = kEnd;
+        mbar_arrive(&bars.sm_full[slot]);
+      }
+      break;
+    }
+    // kda_verify_debug: this item's inputs are withheld (no copy, no
+    // arrival), so the prep team's bounded wait on them runs out
+    if (m.item != p.withhold_item) {
+      arm();
+      if (lane == 0) {
+        *reinterpret_cast<Meta*>(sl) = m;
+        uint64_t* bar = &bars.sm_full[slot];
+        if (m.flags & kLive) {
+          // the item's rows of the conv pass's block (q | v, then k | gate),
+          // its head's dt_bias and, in the fold variant, its pending records:
+          // a few bulk copies
+          const int h = m.item - (m.item / p.H) * p.H;
+          const uint32_t rows = static_cast<uint32_t>(m.n) * 2 * KD * 2;
+          const uint32_t fold_bytes = static_cast<uint32_t>(m.fold_m) * (2 * KD * 2 + KD * 4);
+          mbar_arrive_expect_tx(bar, (rows ? 2 * rows + Lay::kBetaBytes : 0u) + KD * 4 + fold_bytes);
+          if (fold_bytes) fold_copies<KD, QMAX, VAR>(p, sl, h, m.fold_m, m.fold_r, bar);
           if (rows) {  // (a fold-only item has no window)
-            const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-            const uint16_t* blk = p.scratch + static_cast<long long>(it) * (4LL * p.Q * KD);
+            const uint16_t* blk = p.scratch + static_cast<long long>(m.item) * scratch_item_elems(p.Q, KD);
             bulk_g2s(sl + Lay::kQV, blk, rows, bar);
             bulk_g2s(sl + Lay::kKG, blk + 2LL * p.Q * KD, rows, bar);
+            bulk_g2s(sl + Lay::kBeta, blk + 4LL * p.Q * KD, Lay::kBetaBytes, bar);
           }
-          bulk_g2s(sl + Lay::kDt, p.dt_bias + static_cast<long long>(jh) * KD, KD * 4, bar);
+          bulk_g2s(sl + Lay::kDt, p.dt_bias + static_cast<long long>(h) * KD, KD * 4, bar);
+        } else {
+          mbar_arrive(bar);
         }
-        __syncwarp();
-      } else {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.sm_full[slot]);
       }
+      __syncwarp();
     }
   }
   if (!ok && lane == 0) {
@@ -495,11 +653,28 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
 
 // ---------------------------------------------------------------- state warp
 
+// The next item of the state warp from the ticket ring: its header's flags,
+// item number and state slot; false once the wait gave up.
+template <int KD, int QMAX, int VAR>
+__device__ __forceinline__ bool next_ticket(const VerifyParams& p, unsigned char* smem, int i, int lane,
+                                            const volatile int* abort_flag, int& flags, int& item, long long& slot) {
+  using Lay = Layout<KD, QMAX, VAR>;
+  Bars<KD, QMAX, VAR> bars(smem);
+  const int e = i % Lay::kTick;
+  if (!warp_wait(&bars.tk_full[e], (i / Lay::kTick) & 1, lane, abort_flag, p.wait_limit_ns)) return false;
+  const SmallMeta<QMAX>* m = reinterpret_cast<const SmallMeta<QMAX>*>(smem + Lay::oTick + e * Lay::kTickBytes);
+  flags = m->flags;
+  item = m->item;
+  slot = m->s;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars.tk_empty[e]);
+  return true;
+}
+
 template <int KD, int QMAX, int VAR>
 __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
   using Lay = Layout<KD, QMAX, VAR>;
   Bars<KD, QMAX, VAR> bars(smem);
-  const int nloc = local_items(p.B * p.H);
   uint32_t ch_cnt = 0;
   bool ok = true;
   // per chunk slot, the last armed phase: 0 never, 1 + its parity (shared
@@ -508,30 +683,28 @@ __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int la
   if (lane < Lay::kNumChunk) arm[lane] = 0;
   if (lane + 32 < Lay::kNumChunk) arm[lane + 32] = 0;
   __syncwarp();
-  for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
-    const int it = static_cast<int>(blockIdx.x) + (i0 + lane) * static_cast<int>(gridDim.x);
-    const ItemMeta<QMAX> im = decode_item<QMAX>(p, it, i0 + lane < nloc, false);
-    const int count = min(32, nloc - i0);
-    for (int j = 0; j < count && ok; ++j) {
-      if (!(__shfl_sync(0xffffffffu, im.flags, j) & kLive)) continue;
-      const int jh = __shfl_sync(0xffffffffu, im.h, j);
-      const long long js = shfl_ll(im.s, j);
-      // lane c streams row chunk c into the next free chunk slot
-      if (lane < kGemvWarps) {
-        const uint32_t cc = ch_cnt + lane;
-        const int pos = cc % Lay::kNumChunk;
-        ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((cc / Lay::kNumChunk) & 1) ^ 1, abort_flag, p.wait_limit_ns);
-        if (ok) {
-          arm[pos] = static_cast<uint8_t>(1 + ((cc / Lay::kNumChunk) & 1));
-          const float* src = p.state + js * p.state_slot_stride + static_cast<long long>(jh) * KD * KD;
-          mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
-          bulk_g2s(smem + Lay::oChunks + pos * Lay::kChunk, src + lane * Lay::RW * KD, Lay::kChunk,
-                   &bars.ch_full[pos]);
-        }
+  for (int i = 0; ok; ++i) {
+    int flags, item;
+    long long js;
+    ok = next_ticket<KD, QMAX, VAR>(p, smem, i, lane, abort_flag, flags, item, js);
+    if (!ok || item < 0) break;
+    if (!(flags & kLive)) continue;
+    const int jh = item - (item / p.H) * p.H;
+    // lane c streams row chunk c into the next free chunk slot
+    if (lane < kGemvWarps) {
+      const uint32_t cc = ch_cnt + lane;
+      const int pos = cc % Lay::kNumChunk;
+      ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((cc / Lay::kNumChunk) & 1) ^ 1, abort_flag, p.wait_limit_ns);
+      if (ok) {
+        arm[pos] = static_cast<uint8_t>(1 + ((cc / Lay::kNumChunk) & 1));
+        const float* src = p.state + js * p.state_slot_stride + static_cast<long long>(jh) * KD * KD;
+        mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
+        bulk_g2s(smem + Lay::oChunks + pos * Lay::kChunk, src + lane * Lay::RW * KD, Lay::kChunk,
+                 &bars.ch_full[pos]);
       }
-      ok = __all_sync(0xffffffffu, ok);
-      ch_cnt += kGemvWarps;
     }
+    ok = __all_sync(0xffffffffu, ok);
+    ch_cnt += kGemvWarps;
   }
   if (!ok && lane == 0) {
     report(p.workspace, KDA_DEVERR_TIMEOUT, blockIdx.x);
@@ -570,10 +743,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
   float* part = reinterpret_cast<float*>(smem + Lay::oPart);
   const int warp = pt >> 5;
   const int lane = pt & 31;
-  const int nloc = local_items(p.B * p.H);
-  for (int i = 0; i < nloc; ++i) {
-    const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    const int h = it - (it / p.H) * p.H;
+  for (int i = 0;; ++i) {
     const int slot = i % Lay::kNumSmall;
     const int oslot = i % Lay::kNumOp;
     unsigned char* sl = smem + Lay::oSmall + slot * Lay::kSmall;
@@ -582,8 +752,22 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
                     warp_wait(&bars.op_empty[oslot], ((i / Lay::kNumOp) & 1) ^ 1, lane, abort_flag, p.wait_limit_ns);
     if (!ok && lane == 0) misc[kMiscPrepFail] = 1;
     const SmallMeta<QMAX> m = *reinterpret_cast<const SmallMeta<QMAX>*>(sl);
+    if (ok && (m.flags & kEnd)) {  // every prep thread reads the same mark: hand it on, stop
+      if (pt == 0) {
+        reinterpret_cast<OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags = kEnd;
+        mbar_arrive(&bars.op_full[oslot]);
+      }
+      break;
+    }
+    const int h = m.item - (m.item / p.H) * p.H;
     const bool live = ok && (m.flags & kLive);
     const int n = m.n;
+    // the window's beta gates, for the operand header (read before the slot
+    // is released)
+    float beta[QMAX];
+#pragma unroll
+    for (int t = 0; t < QMAX; ++t)
+      beta[t] = (pt == 0 && live && t < n) ? reinterpret_cast<const float*>(sl + Lay::kBeta)[t] : 0.0f;
     const uint16_t* qv_rows = reinterpret_cast<const uint16_t*>(sl + Lay::kQV);  // [QMAX][2K] q | v
     const uint16_t* kg_rows = reinterpret_cast<const uint16_t*>(sl + Lay::kKG);  // [QMAX][2K] k | gate
 
@@ -766,10 +950,10 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       om->flags = live ? kLive : 0;
       om->bos = m.bos;
       om->n = n;
-      om->pad = 0;
+      om->h = h;
       om->r = m.r;
 #pragma unroll
-      for (int t = 0; t < QMAX; ++t) om->beta[t] = m.beta[t];
+      for (int t = 0; t < QMAX; ++t) om->beta[t] = beta[t];
       om->fold_m = 0;
       om->pad2 = 0;
       om->s = m.s;
@@ -964,17 +1148,16 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
   Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   float* red = reinterpret_cast<float*>(smem + Lay::oRed) + gw * Lay::kRedPerWarp;
-  const int nloc = local_items(p.B * p.H);
   uint32_t live = 0;
   bool ok = true;
-  for (int i = 0; i < nloc && ok; ++i) {
-    const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    const int h = it - (it / p.H) * p.H;
+  for (int i = 0; ok; ++i) {
     const int oslot = i % Lay::kNumOp;
     ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag, p.wait_limit_ns);
     if (!ok) break;
     const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
     const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta);
+    if (m.flags & kEnd) break;
+    const int h = m.h;
     if (m.flags & kLive) {
       const int n = m.n;
       const uint32_t pc = live * kGemvWarps + gw;
@@ -1098,28 +1281,26 @@ template <int KD, int QMAX, int VAR>
 __device__ void tc_produce_state(const VerifyParams& p, unsigned char* smem, int lane, volatile int* abort_flag) {
   using Lay = Layout<KD, QMAX, VAR>;
   Bars<KD, QMAX, VAR> bars(smem);
-  const int nloc = local_items(p.B * p.H);
   uint32_t g = 0;  // slices issued
   bool ok = true;
-  for (int i0 = 0; i0 < nloc && ok; i0 += 32) {
-    const int it = static_cast<int>(blockIdx.x) + (i0 + lane) * static_cast<int>(gridDim.x);
-    const ItemMeta<QMAX> im = decode_item<QMAX>(p, it, i0 + lane < nloc, false);
-    const int count = min(32, nloc - i0);
-    for (int j = 0; j < count && ok; ++j) {
-      if (!(__shfl_sync(0xffffffffu, im.flags, j) & kLive)) continue;
-      const int jh = __shfl_sync(0xffffffffu, im.h, j);
-      const int js = static_cast<int>(shfl_ll(im.s, j));
-      for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
-        const int pos = static_cast<int>(g % Lay::kNumChunk);
-        if (lane == 0) {
-          ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((g / Lay::kNumChunk) & 1) ^ 1, abort_flag, p.wait_limit_ns);
-          if (ok) {
-            mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
-            tma_load_3d(smem + Lay::oChunks + pos * Lay::kChunk, &p.tm_state, kb * 32, jh * KD, js, &bars.ch_full[pos]);
-          }
+  for (int i = 0; ok; ++i) {
+    int flags, item;
+    long long js;
+    ok = next_ticket<KD, QMAX, VAR>(p, smem, i, lane, abort_flag, flags, item, js);
+    if (!ok || item < 0) break;
+    if (!(flags & kLive)) continue;
+    const int jh = item - (item / p.H) * p.H;
+    for (int kb = 0; kb < 4 && ok; ++kb, ++g) {
+      const int pos = static_cast<int>(g % Lay::kNumChunk);
+      if (lane == 0) {
+        ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((g / Lay::kNumChunk) & 1) ^ 1, abort_flag, p.wait_limit_ns);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
+          tma_load_3d(smem + Lay::oChunks + pos * Lay::kChunk, &p.tm_state, kb * 32, jh * KD, static_cast<int>(js),
+                      &bars.ch_full[pos]);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
   }
   if (!ok && lane == 0) {
@@ -1176,17 +1357,18 @@ __device__ void tc_mma(const VerifyParams& p, unsigned char* smem, volatile int*
   constexpr uint32_t kIdesc = umma_idesc_tf32(128, Layout<KD, QMAX, VAR>::kMmaN);
   Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
-  const int nloc = local_items(p.B * p.H);
   const uint32_t taddr = static_cast<uint32_t>(misc[kMiscTaddr]);
   uint32_t g = 0, live = 0;
   LoPending lp{false, false, 0, 0, 0, 0, 0};
   bool ok = true;
-  for (int i = 0; i < nloc && ok; ++i) {
+  for (int i = 0; ok; ++i) {
     const int oslot = i % Lay::kNumOp;
     const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
     ok = mbar_wait_or_abort(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, abort_flag, p.wait_limit_ns);
     if (!ok) break;
-    if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
+    const int flags = reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags;
+    if (flags & kEnd) break;
+    if (!(flags & kLive)) {
       // finish the previous item first: its operand slot may be the next one
       // the prep team needs
       ok = tc_issue_lo<KD, QMAX, VAR>(smem, taddr, lp, abort_flag, p.wait_limit_ns);
@@ -1254,8 +1436,6 @@ __device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char*
                                            int lane, uint32_t taddr, const volatile int* abort_flag) {
   using Lay = Layout<KD, QMAX, VAR>;
   Bars<KD, QMAX, VAR> bars(smem);
-  const int it = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-  const int h = it - (it / p.H) * p.H;
   const int oslot = i % Lay::kNumOp;
   const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
   const uint32_t db = live & 1;
@@ -1269,6 +1449,7 @@ __device__ __forceinline__ bool tc_readout(const VerifyParams& p, unsigned char*
   __syncwarp();
   if (lane == 0) mbar_arrive(&bars.d_empty[db]);
   const OpMeta<QMAX> m = *reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta);
+  const int h = m.h;
   const int row = wq * 32 + lane;
   if constexpr (QMAX <= 4) {
     switch (m.n) {
@@ -1309,17 +1490,18 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
   // tcgen05.ld reaches the tensor-memory lanes of the warp's quadrant of the
   // CTA (warp index mod 4): this warp reads out rows 32 wq .. 32 wq + 31
   const int wq = static_cast<int>(threadIdx.x >> 5) & 3;
-  const int nloc = local_items(p.B * p.H);
   const uint32_t taddr = static_cast<uint32_t>(misc[kMiscTaddr]);
   uint32_t g = 0, live = 0;
   int pending = -1;  // live item awaiting readout
   bool ok = true;
-  for (int i = 0; i < nloc && ok; ++i) {
+  for (int i = 0; ok; ++i) {
     const int oslot = i % Lay::kNumOp;
     const unsigned char* op = smem + Lay::oOp + oslot * Lay::kOp;
     ok = warp_wait(&bars.op_full[oslot], (i / Lay::kNumOp) & 1, lane, abort_flag, p.wait_limit_ns);
     if (!ok) break;
-    if (!(reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags & kLive)) {
+    const int flags = reinterpret_cast<const OpMeta<QMAX>*>(op + Lay::kOpMeta)->flags;
+    if (flags & kEnd) break;
+    if (!(flags & kLive)) {
       // read the pending item out now: with no live item to follow soon, its
       // operand slot would be missing when the prep team comes round to it
       if (pending >= 0) ok = tc_readout<KD, QMAX, VAR>(p, smem, pending, live - 1, wq, lane, taddr, abort_flag);
@@ -1362,6 +1544,19 @@ __device__ void tc_split(const VerifyParams& p, unsigned char* smem, int st, vol
   }
 }
 
+// A CTA's last act (one thread, after every role): the finish time for
+// kda_verify_debug, and the count of finished CTAs, whose last zeroes the
+// ticket counter for the next launch (every CTA has drawn its last ticket
+// before it counts itself done).
+__device__ __forceinline__ void finish_cta(const VerifyParams& p) {
+  if (p.cta_times != nullptr) p.cta_times[2 * blockIdx.x + 1] = global_timer_ns();
+  __threadfence();
+  if (atomicAdd(p.workspace + kWsDone, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(p.workspace + kWsTicket, 0);
+    atomicExch(p.workspace + kWsDone, 0);
+  }
+}
+
 template <int KD, int QMAX, int VAR>
 __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_kernel(const __grid_constant__ VerifyParams p) {
   using Lay = Layout<KD, QMAX, VAR>;
@@ -1369,6 +1564,7 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
   volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::oMisc);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  if (p.cta_times != nullptr && tid == 0) p.cta_times[2 * blockIdx.x] = global_timer_ns();
   if (tid == 0) {
     Bars<KD, QMAX, VAR> bars(smem);
     for (int i = 0; i < Lay::kNumChunk; ++i) {
@@ -1394,6 +1590,10 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
       mbar_init(&bars.d_full[i], 1);
       mbar_init(&bars.d_empty[i], kSplitWarps);
     }
+    for (int i = 0; i < Lay::kTick; ++i) {
+      mbar_init(&bars.tk_full[i], 1);
+      mbar_init(&bars.tk_empty[i], 2);  // read by both producer warps
+    }
     for (int i = 0; i < 8; ++i)
       if (i != kMiscTaddr) misc[i] = 0;  // the tensor-memory base is written by the allocating warp
     fence_barrier_init();
@@ -1401,7 +1601,11 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
   if constexpr (Lay::kTC) {
     // the 128-byte swizzle of the MMA operands is anchored at 1024-byte boundaries
     if (smem_u32(smem) & 1023u) {
-      if (tid == 0) report(p.workspace, KDA_DEVERR_MISALIGNED, blockIdx.x);
+      if (tid == 0) {
+        report(p.workspace, KDA_DEVERR_MISALIGNED, blockIdx.x);
+        wait_prior_grid();
+        finish_cta(p);
+      }
       return;
     }
     // tensor memory for two D buffers of 4 QMAX fp32 columns, owned by the MMA warp
@@ -1412,7 +1616,7 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
   __syncthreads();
   if constexpr (Lay::kTC) tmem_fence_after();
   if (warp == 0) {
-    produce_inputs<KD, QMAX, VAR>(p, smem, tid & 31, misc + kMiscAbort);
+    produce_inputs<KD, QMAX, VAR>(p, smem, tid & 31, misc);
   } else if (warp == 1) {
     if constexpr (Lay::kTC)
       tc_produce_state<KD, QMAX, VAR>(p, smem, tid & 31, misc + kMiscAbort);
@@ -1438,6 +1642,9 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
       tmem_dealloc(static_cast<uint32_t>(misc[kMiscTaddr]), Lay::kTmemCols);
     }
   }
+  // every role is done (and the inputs warp has its last ticket back)
+  __syncthreads();
+  if (tid == 0) finish_cta(p);
 }
 
 // ---------------------------------------------------------------- tensor maps (host)
@@ -1509,19 +1716,30 @@ int sm_count() {
 }
 
 template <int KD, int QMAX, int VAR>
-cudaError_t launch(const VerifyParams& p, cudaStream_t stream) {
+cudaError_t launch(const VerifyParams& p, bool after_conv, cudaStream_t stream) {
   constexpr int bytes = Layout<KD, QMAX, VAR>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(verify_kernel<KD, QMAX, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   const int items = p.B * p.H;
-  const int grid = items < sm_count() ? items : sm_count();
-  verify_kernel<KD, QMAX, VAR><<<grid, Layout<KD, QMAX, VAR>::kThreads, bytes, stream>>>(p);
-  return cudaGetLastError();
+  // After the conv pass, the launch is programmatic: the CTAs may start
+  // (barrier set-up, state streaming) while the conv pass drains; the inputs
+  // warp waits for it before its first copy from the scratch.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(items < sm_count() ? items : sm_count()));
+  cfg.blockDim = dim3(Layout<KD, QMAX, VAR>::kThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_conv ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, verify_kernel<KD, QMAX, VAR>, p);
 }
 
 template <int KD, int QMAX, bool DF>
 cudaError_t launch_conv(const VerifyParams& p, cudaStream_t stream) {
-  conv_kernel<KD, QMAX, DF><<<p.B * p.H, KD, 0, stream>>>(p);
+  conv_kernel<KD, QMAX, DF><<<p.B * p.H, 3 * KD / 2, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1541,14 +1759,15 @@ cudaError_t launch_verify(const VerifyParams& params, int K, int variant, cudaSt
              : (p.conv_dim_first ? launch_conv<64, 8, true>(p, stream) : launch_conv<64, 8, false>(p, stream));
     if (e != cudaSuccess) return e;
   }
+  const bool pdl = p.T > 0;
   if (p.fold_qsl != nullptr) {  // the host accepts the fold for windows up to 4 only
     if (!q4) return cudaErrorInvalidValue;
-    return K == 128 ? launch<128, 4, kVarFold>(p, stream) : launch<64, 4, kVarFold>(p, stream);
+    return K == 128 ? launch<128, 4, kVarFold>(p, pdl, stream) : launch<64, 4, kVarFold>(p, pdl, stream);
   }
   if (K == 128 && use_tcgen05(variant, q4) && build_state_map(p, K))
-    return q4 ? launch<128, 4, kVarTcgen05>(p, stream) : launch<128, 8, kVarTcgen05>(p, stream);
-  if (K == 128) return q4 ? launch<128, 4, kVarPlain>(p, stream) : launch<128, 8, kVarPlain>(p, stream);
-  return q4 ? launch<64, 4, kVarPlain>(p, stream) : launch<64, 8, kVarPlain>(p, stream);
+    return q4 ? launch<128, 4, kVarTcgen05>(p, pdl, stream) : launch<128, 8, kVarTcgen05>(p, pdl, stream);
+  if (K == 128) return q4 ? launch<128, 4, kVarPlain>(p, pdl, stream) : launch<128, 8, kVarPlain>(p, pdl, stream);
+  return q4 ? launch<64, 4, kVarPlain>(p, pdl, stream) : launch<64, 8, kVarPlain>(p, pdl, stream);
 }
 
 }  // namespace kda

@@ -46,7 +46,7 @@ def test_exports_every_declared_function(lib):
 def test_abi_version_matches_header(lib):
     m = re.search(r"#define KDA_ABI_VERSION (\d+)", open(HEADER).read())
     assert lib.kda_abi_version() == int(m.group(1))
-    assert lib.kda_workspace_bytes() >= 8
+    assert lib.kda_workspace_bytes() >= 40  # error words, then the ticket counter at word 8
 
 
 def _c_layout(struct, fields):
@@ -71,7 +71,9 @@ int main(void) {{
     return {k: int(v) for k, v in (line.split() for line in out.splitlines())}
 
 
-@pytest.mark.parametrize("cls,cname", [(kda.VerifyArgs, "kda_verify_args"), (kda.CommitArgs, "kda_commit_args")])
+@pytest.mark.parametrize("cls,cname", [(kda.VerifyArgs, "kda_verify_args"), (kda.CommitArgs, "kda_commit_args"),
+                                      (kda.DebugArgs, "kda_debug_args"), (kda.FoldArgs, "kda_fold_args"),
+                                      (kda.AlignArgs, "kda_align_args")])
 def test_ctypes_mirror_matches_c_layout(cls, cname):
     fields = [f for f, _ in cls._fields_]
     c = _c_layout(cname, fields)
@@ -98,8 +100,9 @@ def _valid_verify_args():
     a.corr_row_stride = H * Q * K
     a.kg_row_stride = H * Q * 2 * K
     a.scratch = FAKE
-    a.scratch_bytes = 2 * H * Q * 4 * K * 2
+    a.scratch_bytes = 2 * H * (Q * 8 * K + 32)
     a.variant = 0
+    a.workspace = FAKE
     return a
 
 
@@ -133,11 +136,13 @@ def test_verify_rejects_before_launch(lib):
         (dict(conv_state=FAKE + 2), kda.KDA_ERR_MISALIGNED),
         (dict(out=FAKE + 1), kda.KDA_ERR_MISALIGNED),
         (dict(scratch=0), kda.KDA_ERR_INVALID_ARG),
-        (dict(scratch_bytes=2 * 4 * 4 * 4 * 64 * 2 - 16), kda.KDA_ERR_INVALID_ARG),
+        (dict(scratch_bytes=2 * 4 * (4 * 8 * 64 + 32) - 16), kda.KDA_ERR_INVALID_ARG),
         (dict(scratch=FAKE + 8), kda.KDA_ERR_MISALIGNED),
         (dict(variant=3), kda.KDA_ERR_INVALID_ARG),
         (dict(variant=-1), kda.KDA_ERR_INVALID_ARG),
         (dict(variant=2), kda.KDA_ERR_UNSUPPORTED),    # the tensor-core verify needs K == 128
+        (dict(workspace=0), kda.KDA_ERR_INVALID_ARG),  # it holds the schedule's ticket counter
+        (dict(workspace=FAKE + 2), kda.KDA_ERR_MISALIGNED),
     ]
     for change, want in cases:
         a = _valid_verify_args()
@@ -154,9 +159,9 @@ def test_verify_rejects_before_launch(lib):
 
 
 def test_verify_scratch_bytes(lib):
-    # [Q][2K] rows q | v and [Q][2K] rows k | gate, bf16, per (request, head)
-    assert lib.kda_verify_scratch_bytes(256, 32, 128, 4) == 256 * 32 * 4 * 4 * 128 * 2
-    assert lib.kda_verify_scratch_bytes(3, 5, 64, 7) == 3 * 5 * 7 * 4 * 64 * 2
+    # per (request, head): [Q][2K] bf16 rows q | v and k | gate, then 8 fp32 beta gates
+    assert lib.kda_verify_scratch_bytes(256, 32, 128, 4) == 256 * 32 * (4 * 8 * 128 + 32)
+    assert lib.kda_verify_scratch_bytes(3, 5, 64, 7) == 3 * 5 * (7 * 8 * 64 + 32)
     assert lib.kda_verify_scratch_bytes(0, 32, 128, 4) == 0
 
 
@@ -187,6 +192,8 @@ def test_verify_debug_rejects_before_launch(lib):
     assert lib.kda_verify_debug(ctypes.byref(a), ctypes.byref(d), None) == kda.KDA_ERR_INVALID_ARG
     d.withhold_item = -2
     assert lib.kda_verify_debug(ctypes.byref(a), ctypes.byref(d), None) == kda.KDA_ERR_INVALID_ARG
+    d.withhold_item, d.cta_times = -1, FAKE + 4
+    assert lib.kda_verify_debug(ctypes.byref(a), ctypes.byref(d), None) == kda.KDA_ERR_MISALIGNED
 
 
 def test_verify_empty_is_a_no_op(lib):

@@ -1,6 +1,8 @@
 """Whole decode steps captured in a CUDA graph: the library allocates nothing
-and never synchronises, and each verify's tensor maps travel by value in the
-launch parameters, so a replay must write exactly what eager launches write."""
+and never synchronises, each verify's tensor maps travel by value in the
+launch parameters, and the ticket counter that deals a verify's items (one
+workspace shared by every launch of the step) is back at zero after each
+launch, so a replay must write exactly what eager launches write."""
 from __future__ import annotations
 
 import pytest
@@ -31,15 +33,16 @@ def test_captured_step_replays_bit_for_bit(schedule):
     L = prob.cfg.L
     dm = device_meta(prob.meta, DEV)
     ctx = commit_context(prob)
+    ws = kda.new_workspace(DEV)
 
     def step():
         if schedule == "verify_then_commit":
             for l in range(L):
-                verify_layer(prob, l, dm)
-            commit_all(ctx, dm)
+                verify_layer(prob, l, dm, workspace=ws)
+            commit_all(ctx, dm, workspace=ws)
         else:
             for l in range(L):
-                verify_layer(prob, l, dm, fold=dm)
+                verify_layer(prob, l, dm, fold=dm, workspace=ws)
 
     tensors = _tensors(prob)
     start = {k: t.clone() for k, t in tensors.items()}
@@ -67,3 +70,5 @@ def test_captured_step_replays_bit_for_bit(schedule):
     torch.cuda.synchronize()
     for k, t in tensors.items():
         assert torch.equal(_bits(t), _bits(eager[k])), f"{schedule}: replay differs in {k}"
+    assert kda.read_device_error(ws) == 0
+    assert ws[8:10].tolist() == [0, 0], "the ticket counter is not back at zero"

@@ -128,9 +128,10 @@ def check_commit_layer(prob, l, hl, exact, meta, before=None, mask=None):
     return None
 
 
-def run_and_check(prob, *, commit=True, mask=None, layers=None, variant="auto"):
+def run_and_check(prob, *, commit=True, mask=None, layers=None, variant="auto", workspace=None):
     """Verify every layer on the GPU, then (optionally) commit all layers in one
-    launch; compare each with the oracle run on host copies of the inputs."""
+    launch; compare each with the oracle run on host copies of the inputs.
+    ``workspace``: the device workspace to use (error bits zero), else a new one."""
     cfg = prob.cfg
     meta = prob.meta
     layers = list(range(cfg.L)) if layers is None else layers
@@ -138,7 +139,7 @@ def run_and_check(prob, *, commit=True, mask=None, layers=None, variant="auto"):
         canary_fill_(t)
     live = meta.state_indices[meta.state_indices > 0]
     hls = {l: host_layer(prob, l, slots=live if mask is not None else None) for l in layers}
-    ws = kda.new_workspace(DEV)
+    ws = kda.new_workspace(DEV) if workspace is None else workspace
     dm = device_meta(meta, DEV)
     for l in range(cfg.L):
         verify_layer(prob, l, dm, workspace=ws, variant=variant)

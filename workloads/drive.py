@@ -47,15 +47,29 @@ def problem_scratch(prob: Problem) -> torch.Tensor:
     return sc
 
 
+def problem_workspace(prob: Problem) -> torch.Tensor:
+    """A device workspace for this workload's verifies and commits, allocated
+    once (its ticket counter is back at zero after every verify launch, so
+    launches in stream order share it)."""
+    ws = prob.extra.get("workspace")
+    if ws is None:
+        ws = kda.new_workspace(prob.fused.device)
+        prob.extra["workspace"] = ws
+    return ws
+
+
 def verify_layer(prob: Problem, l: int, dm: DeviceMeta, *, out=None, workspace=None, stream=None,
                  fused=None, fold: DeviceMeta | None = None, variant: str = "auto", debug=None) -> None:
     """One layer's verify.  With ``fold`` (the previous step's metadata) the
     previous step's accepted records are folded into the checkpoints first,
-    in the same launch (``kda_verify_fold``)."""
+    in the same launch (``kda_verify_fold``).  ``workspace``: the problem's
+    own (``problem_workspace``) unless given."""
     cfg = prob.cfg
     H, K = cfg.H, cfg.K
     f = prob.fused[l] if fused is None else fused
     scratch = problem_scratch(prob) if f.is_cuda else None
+    if workspace is None and f.is_cuda:
+        workspace = problem_workspace(prob)
     kda.verify(
         mixed_qkv=f[:, : 3 * H * K], raw_gate=f[:, 3 * H * K: 4 * H * K],
         raw_beta=f[:, 4 * H * K: 4 * H * K + H],

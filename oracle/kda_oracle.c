@@ -29,10 +29,12 @@
  * stored code: the bf16 value that every later step consumes.  The oracle
  * takes that decision from the plain definition: y = sum_j w_j x_j in double
  * (each product of a bf16 input and a bf16 or fp32 weight is exact in double),
- * SiLU(y) = y / (1 + e^-y) with the C library's exp, and one round-to-nearest-
- * even of that double to bf16.  The pins check the codes against an exact
+ * SiLU(y) = y / (1 + e^-y) with the C library's exp, and one rounding of that
+ * double to bf16 (nearest; an exact tie, which only arises where double
+ * cannot tell SiLU(y) from a large y, goes toward zero, the side the exact
+ * value lies on).  The pins check the codes against an exact
  * (arbitrary-precision) evaluation, including inputs placed next to a bf16
- * rounding boundary.
+ * rounding boundary and large sums that fall exactly on one.
  *
  * Readings taken where the pages are silent (each is listed in the design
  * notes of the repository):
@@ -70,10 +72,12 @@ static double bf16_value(uint16_t bits) {
     return (double)f;
 }
 
-/* Round a double straight to bf16, nearest-even, without passing through
- * fp32 (which would round twice).  bf16 keeps 8 significant bits and shares
- * fp32's exponent range; its subnormal quantum is 2^-133. */
-static uint16_t bf16_round(double x) {
+/* Round a double straight to bf16, nearest, without passing through fp32
+ * (which would round twice).  bf16 keeps 8 significant bits and shares fp32's
+ * exponent range; its subnormal quantum is 2^-133.  A value exactly halfway
+ * between two codes goes to the even one, or, with ties_down, to the one
+ * nearer zero. */
+static uint16_t bf16_round_ties(double x, int ties_down) {
     if (isnan(x)) return 0x7FC0;
     uint16_t sign = signbit(x) ? 0x8000 : 0;
     double ax = fabs(x);
@@ -83,7 +87,9 @@ static uint16_t bf16_round(double x) {
     (void)frexp(ax, &e); /* ax = f * 2^e, f in [0.5, 1) */
     int qexp = e - 8;
     if (qexp < -133) qexp = -133;
-    double rq = nearbyint(ldexp(ax, -qexp)); /* ties to even */
+    double sc = ldexp(ax, -qexp); /* exact: a power-of-two scaling */
+    double rq = nearbyint(sc);    /* ties to even */
+    if (ties_down && sc - floor(sc) == 0.5) rq = floor(sc);
     double r = ldexp(rq, qexp);
     if (r >= 0x1p128) return (uint16_t)(sign | 0x7F80);
     float f = (float)r; /* exact: r has at most 8 significant bits */
@@ -91,6 +97,8 @@ static uint16_t bf16_round(double x) {
     memcpy(&w, &f, sizeof w);
     return (uint16_t)(sign | (uint16_t)(w >> 16));
 }
+
+static uint16_t bf16_round(double x) { return bf16_round_ties(x, 0); }
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
@@ -100,6 +108,17 @@ static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
 static double silu(double y) { return y / (1.0 + exp(-y)); }
 
+/* The bf16 code of SiLU(y), correctly rounded.  For y > 0, SiLU(y) =
+ * y - y e^-y / (1 + e^-y) lies strictly below y; past y of about 37, 1 + e^-y
+ * rounds to 1 in double and the double SiLU equals y itself.  A y exactly
+ * halfway between two codes then stands for a value just below the midpoint,
+ * whose code is the one nearer zero, whichever of the two is even.  (SiLU(y)
+ * itself is never a midpoint for y != 0: e^-y is transcendental.) */
+static uint16_t silu_code(double y) {
+    double s = silu(y);
+    return bf16_round_ties(s, y > 0.0 && s == y);
+}
+
 /* [kernels] CuteRecoverSSMVerify.__call__ / [state] deferred_recoverssm_verify
  * (causal_conv1d_update with activation "silu"): y = sum_j w_j x_j over the W
  * taps, oldest first (w[W-1] on the newest input), SiLU, and the bf16 code of
@@ -107,7 +126,7 @@ static double silu(double y) { return y / (1.0 + exp(-y)); }
 static uint16_t conv_silu_code(const double *w, const double *x, int W) {
     double y = 0.0;
     for (int j = 0; j < W; ++j) y += w[j] * x[j];
-    return bf16_round(silu(y));
+    return silu_code(y);
 }
 
 /* [ops] _kda_gate: gate_input = raw_g + dt_bias; the bounded form is

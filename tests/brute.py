@@ -63,16 +63,19 @@ def bf16_midpoint_distance(v: np.ndarray) -> np.ndarray:
 
 def silu_codes_exact(y, digits: int = 60) -> np.ndarray:
     """bf16 codes of SiLU(y) = y / (1 + e^-y), correctly rounded, evaluated in
-    ``digits`` decimal digits (mpmath) and rounded to nearest even against the
-    bf16 grid at that magnitude.  y: [n] doubles taken as exact, or [n, W]
-    terms whose exact sum is y."""
+    ``digits`` decimal digits (mpmath) beyond what separates SiLU(y) from y
+    (about 0.43 y digits for large positive y, so that a y lying exactly on a
+    bf16 midpoint is resolved to the side SiLU(y) lies on), and rounded to
+    nearest against the bf16 grid at that magnitude.  y: [n] doubles taken
+    as exact, or [n, W] terms whose exact sum is y."""
     import mpmath
     y = np.asarray(y, np.float64)
     terms = y.reshape(y.shape[0], -1) if y.ndim == 2 else y.reshape(-1, 1)
     out = np.empty(terms.shape[0], np.uint16)
-    with mpmath.workdps(digits):
-        half = mpmath.mpf(1) / 2
-        for i in range(terms.shape[0]):
+    for i in range(terms.shape[0]):
+        extra = int(max(0.0, float(terms[i].sum())) * 0.4343) + 5
+        with mpmath.workdps(digits + extra):
+            half = mpmath.mpf(1) / 2
             yy = mpmath.fsum(mpmath.mpf(float(t)) for t in terms[i])
             s = yy / (1 + mpmath.exp(-yy))
             if s == 0:
@@ -82,8 +85,11 @@ def silu_codes_exact(y, digits: int = 60) -> np.ndarray:
             _, e = mpmath.frexp(a)                           # a = f 2^e, f in [1/2, 1)
             q = mpmath.ldexp(1, max(int(e) - 8, -133))
             k = int(mpmath.floor(a / q))
-            rem = a / q - k                                  # never exactly 1/2: SiLU(y) is transcendental for y != 0
-            if rem > half or (rem == half and k % 2 == 1):
+            rem = a / q - k
+            # never exactly 1/2 (SiLU(y) is transcendental for y != 0) unless
+            # the precision fell short of separating SiLU(y) from y
+            assert rem != half, f"y = {float(yy)!r}: SiLU not resolved from a bf16 midpoint"
+            if rem > half:
                 k += 1
             val = float(k * q)                               # at most 8 significant bits: exact
             bits = int(np.array([val], np.float32).view(np.uint32)[0] >> 16)

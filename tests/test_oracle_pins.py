@@ -149,6 +149,44 @@ def test_conv_code_next_to_rounding_boundaries():
     assert np.mean(naive != want) > 0.1
 
 
+def _large_midpoint_sums(seed):
+    """Conv inputs whose tap sum y is exactly a bf16 midpoint above 37, where
+    double precision cannot tell SiLU(y) = y - y e^-y / (1 + e^-y) from y: one
+    tap w x with w = 1.5 2^a and x = v 2^b (both bf16), 3 v a 9-bit odd
+    number, the other taps zero.  Returns (w, x, y, n3): n3 marks the sums
+    whose even neighbour is the upper one, where nearest-even rounding of y
+    gives the wrong code."""
+    rng = np.random.default_rng(seed)
+    ws, xs, ys, n3 = [], [], [], []
+    for v in range(87, 171, 2):             # 3 v in [261, 511]: nine significant bits, the last one set
+        sh = int(rng.integers(-2, 6))       # y = 3 v 2^sh, from about 65 to 16 000
+        a = int(rng.integers(-2, 3))        # the power of two split between w and x
+        w = 1.5 * 2.0 ** a
+        x = v * 2.0 ** (sh - a + 1)         # w x = 3 v 2^sh
+        y = w * x
+        ws.append([0.0, 0.0, 0.0, w])
+        xs.append([0.0, 0.0, 0.0, x])
+        ys.append(y)
+        n3.append((3 * v) % 4 == 3)
+    return np.array(ws), np.array(xs), np.array(ys), np.array(n3)
+
+
+def test_conv_code_large_sums_on_a_midpoint():
+    """A sum that is exactly a bf16 midpoint stands for SiLU just below it:
+    the code is the one nearer zero (the exact evaluation decides), although
+    double precision sees SiLU(y) == y there and nearest-even would pick the
+    upper code in about half of the cases."""
+    pytest.importorskip("mpmath")
+    w, x, y, n3 = _large_midpoint_sums(seed=31)
+    assert (y > 37).all() and (brute.bf16_midpoint_distance(y) == 0).all()
+    want = brute.silu_codes_exact(w * x)
+    np.testing.assert_array_equal(oracle.conv_silu_bf16(w, x), want)
+    np.testing.assert_array_equal(want, brute.bf16_rne(y - y * 2.0 ** -30))  # the code below the midpoint
+    assert (want != brute.bf16_rne(y))[n3].all() and n3.sum() >= 10
+    # negative sums of the same size: SiLU is tiny there, and decided plainly
+    np.testing.assert_array_equal(oracle.conv_silu_bf16(w, -x), brute.silu_codes_exact(w * -x))
+
+
 def test_silu_codes_exact_against_known_roundings():
     """The 60-digit reference itself: SiLU(0) = 0, large y rounds like y, and
     values far from a boundary agree with the double evaluation."""

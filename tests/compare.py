@@ -78,3 +78,19 @@ def assert_same_written(gpu_written, ref_written, what):
         missing = np.argwhere(~gpu_written & ref_written)[:5]
         raise AssertionError(f"{what}: written sets differ; GPU-only {extra.tolist()}, "
                              f"oracle-only {missing.tolist()}")
+
+
+def conv_adversarial_rows():
+    """The rows of tests/golden/conv_adversarial.txt: (kinds [n], fp32 conv
+    weights [n, 4] as doubles), for a conv fed with inputs of 1.0."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "conv_adversarial.txt")
+    kinds, rows = [], []
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split()
+            kinds.append(parts[0])
+            rows.append([float.fromhex(v) for v in parts[1:5]])
+    return np.array(kinds), np.array(rows, np.float64)

@@ -12,6 +12,7 @@ import torch
 from scipy.special import expit
 
 import brute
+import compare
 import oracle
 from oracle_io import host_layer, run_commit, run_verify
 from workloads import CONFIGS, Config, make_problem
@@ -185,6 +186,15 @@ def test_conv_code_large_sums_on_a_midpoint():
     assert (want != brute.bf16_rne(y))[n3].all() and n3.sum() >= 10
     # negative sums of the same size: SiLU is tiny there, and decided plainly
     np.testing.assert_array_equal(oracle.conv_silu_bf16(w, -x), brute.silu_codes_exact(w * -x))
+
+
+def test_conv_adversarial_fixture_codes_are_exact():
+    """The adversarial rows the GPU conv test runs (tests/golden/
+    conv_adversarial.txt): the oracle's codes are the exact ones."""
+    pytest.importorskip("mpmath")
+    kinds, w = compare.conv_adversarial_rows()
+    assert set(kinds) == {"near", "tie", "large"} and len(w) > 500
+    np.testing.assert_array_equal(oracle.conv_silu_bf16(w, np.ones_like(w)), brute.silu_codes_exact(w))
 
 
 def test_silu_codes_exact_against_known_roundings():

@@ -325,6 +325,52 @@ def run_deferred(args, prob, dm, stream, dev, world):
     return d_start.elapsed_time(d_end), steps
 
 
+def run_long_window(args, dev):
+    """The long-window workload (C3: B=512, H=32, Q=8, one layer) on both
+    schedules, one GPU: verify then commit (the tensor-core verify, the
+    default at Q = 8, and the commit launch) against the deferred schedule
+    (kda_verify_fold on the CUDA cores, no commit launch).  Every step uses
+    the same request metadata, so each step's fold folds what the step before
+    accepted."""
+    from workloads import CONFIGS, make_problem
+    from workloads.drive import commit_all, commit_context, device_meta, verify_layer
+
+    cfg = CONFIGS["C3"]
+    prob = make_problem(cfg, dev)
+    acct = step_accounting(cfg, prob.meta)
+    dm = device_meta(prob.meta, dev)
+    ctx = commit_context(prob)
+    stream = torch.cuda.current_stream(dev)
+
+    def plain():
+        for l in range(cfg.L):
+            verify_layer(prob, l, dm, stream=stream)
+        commit_all(ctx, dm, stream=stream)
+
+    def deferred():
+        for l in range(cfg.L):
+            verify_layer(prob, l, dm, stream=stream, fold=dm)
+
+    out = {}
+    steps = max(5, args.steps // 2)
+    for name, fn in (("verify_then_commit", plain), ("deferred", deferred)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"ms_per_step": ms, "tokens_per_s": acct["tokens"] / (ms / 1e3)}
+    out["workload"] = "C3: B=512, H=32, K=V=128, Q=8, 1 layer, lower-bound gate"
+    out["steps"] = steps
+    return out
+
+
 def run_gpu(args, rank, local, world):
     import linear_attention_ssm_kda_gb300 as kda
     from linear_attention_ssm_kda_gb300 import _build
@@ -394,8 +440,11 @@ def run_gpu(args, rank, local, world):
     if not args.no_e2e:
         e2e_ms, e2e_steps, h2d, d2h = run_e2e(args, prob, ctx, stream, dev, world)
     d_ms, d_steps = None, 0
-    if not args.no_deferred and cfg.Q <= 4:
+    if not args.no_deferred:
         d_ms, d_steps = run_deferred(args, prob, dm, stream, dev, world)
+    long_window = None
+    if not args.no_deferred and world == 1 and args.config != "C3":
+        long_window = run_long_window(args, dev)
 
     # aggregate over ranks: units of all ranks / the slowest rank's time
     t_max = max_over_ranks(elapsed_ms, world)
@@ -465,6 +514,7 @@ def run_gpu(args, rank, local, world):
             "algorithmic_bytes_per_step": acct["deferred_step_bytes"], "steps": d_steps,
             "schedule": "each layer's verify first folds the previous step's accepted records into the "
                         "checkpoint (kda_verify_fold), no commit launch"},
+        "long_window": long_window,
         # each kda_verify is two launches (the conv pass, then the verify kernel)
         "gpu_launches": args.steps * (2 * L + 1),
         "clocks": clk,

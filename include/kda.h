@@ -245,9 +245,9 @@ typedef struct kda_commit_args {
  * fold == NULL or fold->query_start_loc == NULL runs the plain verify.  With
  * T == 0 (every window empty) only the folds run, and the activation
  * pointers may be NULL.
- * Supported: Q <= 4 (KDA_ERR_UNSUPPORTED otherwise); the other arguments and
- * errors are those of kda_verify; a pending record row out of range is a
- * device error (KDA_DEVERR_ROW_RANGE) that skips the item.
+ * The fold runs on the CUDA cores whatever args->variant says.  The other
+ * arguments and errors are those of kda_verify; a pending record row out of
+ * range is a device error (KDA_DEVERR_ROW_RANGE) that skips the item.
  */
 typedef struct kda_fold_args {
     const int32_t *query_start_loc;  /* [B+1] of the step whose records are pending */
@@ -368,7 +368,7 @@ const char *kda_last_error(void);
 /* ABI version of this header (bumped on any layout change). */
 int32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

@@ -238,7 +238,7 @@ def verify(*, mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, lower_bound, state,
     step's query_start_loc [B+1] and accepted counts [B], and optionally its
     record rows ``fold_record_indices``) this is ``kda_verify_fold``: each
     request's pending records are first folded into its checkpoint, which is
-    written back, and the verify runs on the folded state (windows up to 4).
+    written back, and the verify runs on the folded state (on the CUDA cores).
 
     ``scratch`` is a device buffer of at least ``verify_scratch_bytes(B, H,
     K, window)`` bytes for the conv pass's output; when None, one is taken

@@ -187,8 +187,6 @@ kda_status kda_verify(const kda_verify_args* a, kda_stream_t stream) {
 kda_status kda_verify_fold(const kda_verify_args* a, const kda_fold_args* f, kda_stream_t stream) {
   if (f == nullptr || f->query_start_loc == nullptr) return kda_verify(a, stream);
   if (f->num_accepted == nullptr) return fail(KDA_ERR_INVALID_ARG, "kda_verify_fold: num_accepted is NULL");
-  if (a != nullptr && a->Q > 4)
-    return fail(KDA_ERR_UNSUPPORTED, "kda_verify_fold: windows up to 4 tokens (Q = %d)", a->Q);
   kda::VerifyParams p;
   bool noop = false;
   const kda_status st = verify_params(a, true, p, &noop);

@@ -114,7 +114,6 @@ struct Layout {
   // streams as K-slices of 32 (128 rows x 128 bytes, 128-byte swizzle) and the
   // products S0 [X | Y] come from tcgen05 MMAs; otherwise CUDA-core gemv warps.
   static_assert(VAR != kVarTcgen05 || (KD == 128 && (QMAX == 4 || QMAX == 8)), "the tensor-core path covers K = 128");
-  static_assert(VAR != kVarFold || QMAX <= 4, "the fold variant covers windows up to 4");
   static_assert(QMAX * 4 <= kScratchBetaBytes, "the block's beta area holds a window");
   static constexpr bool kTC = VAR == kVarTcgen05;
   static constexpr bool kFold = VAR == kVarFold;
@@ -1760,9 +1759,9 @@ cudaError_t launch_verify(const VerifyParams& params, int K, int variant, cudaSt
     if (e != cudaSuccess) return e;
   }
   const bool pdl = p.T > 0;
-  if (p.fold_qsl != nullptr) {  // the host accepts the fold for windows up to 4 only
-    if (!q4) return cudaErrorInvalidValue;
-    return K == 128 ? launch<128, 4, kVarFold>(p, pdl, stream) : launch<64, 4, kVarFold>(p, pdl, stream);
+  if (p.fold_qsl != nullptr) {
+    if (K == 128) return q4 ? launch<128, 4, kVarFold>(p, pdl, stream) : launch<128, 8, kVarFold>(p, pdl, stream);
+    return q4 ? launch<64, 4, kVarFold>(p, pdl, stream) : launch<64, 8, kVarFold>(p, pdl, stream);
   }
   if (K == 128 && use_tcgen05(variant, q4) && build_state_map(p, K))
     return q4 ? launch<128, 4, kVarTcgen05>(p, pdl, stream) : launch<128, 8, kVarTcgen05>(p, pdl, stream);

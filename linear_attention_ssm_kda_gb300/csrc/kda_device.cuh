@@ -262,7 +262,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 // deferred_recoverssm_verify: causal_conv1d_update with activation "silu",
 // output in the activation dtype).  Three tiers decide it:
 //   1. fp32 (conv_silu_bf16x2, two codes at once on the packed fp32x2
-//      unit): y by an fma chain, SiLU by the procedure in silu_f32x2, and a
+//      unit): y by an fma chain, SiLU on the special-function unit
+//      (silu_f32x2), and a
 //      bound E on |computed - exact|.  When no bf16 rounding boundary lies
 //      within E of the computed value, the hardware rounding of it is the
 //      correctly rounded code.  Otherwise the code is marked doubtful (about
@@ -277,57 +278,44 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
-// SiLU(y) = y sigma(y) in fp32 from IEEE-754 adds, multiplies and fmas:
-//   z = e^-|y|: x = max(-|y|, -104); n = x log2 e rounded to nearest even (one
-//     fma with 1.5 * 2^23, whose ulp is 1, leaves n in the low mantissa bits);
-//     Cody-Waite reduction r = x - n ln2 with ln2 split in a 15-bit head (n
-//     times it is exact) and a tail; e^r by its Taylor series to r^7/7! in
-//     Horner form (|r| <= 0.347); z = e^r 2^n1 2^n2, n1 = floor(n/2), n2 = n - n1;
-//   1/(1+z) for 1+z in [1, 2]: r0 = 24/17 - (8/17)(1+z), then three Newton steps;
-//   sigma = 1/(1+z) for y >= 0 and z/(1+z) below, SiLU = y sigma.
+// SiLU(y) = y sigma(y), sigma = 1 / (1 + e^-y), on the special-function unit:
+//   e^-y = 2^(-y log2 e) with the argument split exactly: th = RN(-y L) for
+//     L = log2 e rounded to fp32, r = fma(-y, L, -th) (the product's exact
+//     rounding error) and tl = r - y (log2 e - L); then e^-y =
+//     ex2(th) (1 + tl ln 2) (tl is below 2^-16 |th|, so the series' next term
+//     is far below the unit's own error).  y is clamped at 104, past which
+//     e^-y is below the fp32 range and sigma is 1;
+//   sigma by the unit's reciprocal of 1 + e^-y, SiLU = y sigma.
 // Its relative error against the exact SiLU of the fp32 input is at most
-// kSiluRelErr for every y >= -80 (checked over all fp32 inputs).  sigma is
-// returned for the error bound.
+// kSiluRelErr for every y >= -80 (checked over all fp32 inputs on GB300).
+// sigma is returned for the error bound.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 __device__ __forceinline__ float2 silu_f32x2(float2 y, float2& sigma) {
-  constexpr float kLog2e = 0x1.715476p+0f;
-  constexpr float kShifter = 0x1.8p+23f;
-  constexpr float kLn2Hi = 0x1.62e4p-1f;
-  constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
-  const float2 x = make_float2(fmaxf(-fabsf(y.x), -104.0f), fmaxf(-fabsf(y.y), -104.0f));
-  // n = rint(x log2 e) through the shifter, lane by lane on the scalar unit
-  const float ta = __fmaf_rn(x.x, kLog2e, kShifter), tb = __fmaf_rn(x.y, kLog2e, kShifter);
-  const float2 nf = make_float2(__fsub_rn(ta, kShifter), __fsub_rn(tb, kShifter));
-  const int na = __float_as_int(ta) - __float_as_int(kShifter);
-  const int nb = __float_as_int(tb) - __float_as_int(kShifter);
-  float2 r = __ffma2_rn(nf, f2(-kLn2Hi), x);
-  r = __ffma2_rn(nf, f2(-kLn2Lo), r);
-  // 1/k! rounded to fp32, k = 7 .. 2
-  float2 q = f2(0x1.a01a02p-13f);
-  q = __ffma2_rn(q, r, f2(0x1.6c16c2p-10f));
-  q = __ffma2_rn(q, r, f2(0x1.111112p-7f));
-  q = __ffma2_rn(q, r, f2(0x1.555556p-5f));
-  q = __ffma2_rn(q, r, f2(0x1.555556p-3f));
-  q = __ffma2_rn(q, r, f2(0.5f));
-  q = __ffma2_rn(q, r, f2(1.0f));
-  q = __ffma2_rn(q, r, f2(1.0f));
-  const int na1 = na >> 1, nb1 = nb >> 1;  // arithmetic shift: floor(n / 2)
-  q = __fmul2_rn(q, make_float2(__int_as_float((na1 + 127) << 23), __int_as_float((nb1 + 127) << 23)));
-  const float2 z =
-      __fmul2_rn(q, make_float2(__int_as_float((na - na1 + 127) << 23), __int_as_float((nb - nb1 + 127) << 23)));
-  const float2 d = __fadd2_rn(f2(1.0f), z);
-  const float2 dn = make_float2(-d.x, -d.y);
-  float2 rc = __ffma2_rn(f2(-0x1.e1e1e2p-2f), d, f2(0x1.69696ap+0f));
-#pragma unroll
-  for (int i = 0; i < 3; ++i) {
-    const float2 e = __ffma2_rn(dn, rc, f2(1.0f));
-    rc = __ffma2_rn(rc, e, rc);
-  }
-  sigma = __fmul2_rn(make_float2(y.x >= 0.0f ? 1.0f : z.x, y.y >= 0.0f ? 1.0f : z.y), rc);
+  constexpr float kL = 0x1.715476p+0f;     // log2 e to fp32
+  constexpr float kLlo = 0x1.4ae0cp-26f;   // log2 e - kL
+  constexpr float kLn2 = 0x1.62e43p-1f;
+  const float2 yc = make_float2(fminf(y.x, 104.0f), fminf(y.y, 104.0f));
+  const float2 th = __fmul2_rn(yc, f2(-kL));
+  const float2 r = __ffma2_rn(yc, f2(-kL), make_float2(-th.x, -th.y));
+  const float2 tl = __ffma2_rn(yc, f2(-kLlo), r);
+  float2 e = make_float2(ex2_approx(th.x), ex2_approx(th.y));
+  e = __ffma2_rn(e, __fmul2_rn(tl, f2(kLn2)), e);
+  const float2 d = __fadd2_rn(f2(1.0f), e);
+  sigma = make_float2(rcp_approx(d.x), rcp_approx(d.y));
   return __fmul2_rn(y, sigma);
 }
 
 // Relative error bound of silu_f32x2 (in units of 2^-24, with margin over the
-// largest error seen across all fp32 inputs >= -80: 4.1) and the lowest y
+// largest error seen across all fp32 inputs >= -80: 5.58) and the lowest y
 // tier 1 serves (below it e^-|y| nears the subnormal range).
 constexpr float kSiluRelErr = 6.0f * 0x1p-24f;
 constexpr float kTier1MinY = -80.0f;

@@ -64,7 +64,7 @@ namespace kda {
 namespace {
 
 constexpr int kConvWidth = 4;
-constexpr int kPrepWarps = 6;  // one key channel per thread (K = 128: four of them busy)
+constexpr int kPrepWarps = 4;  // one key channel per thread
 constexpr int kGemvWarps = 8;  // one state row chunk (16 rows at K = 128) each
 constexpr int kPrepConvThreads = 32 * kPrepWarps;
 constexpr int kBarPrep = 1;

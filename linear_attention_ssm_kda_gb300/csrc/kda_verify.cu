@@ -158,9 +158,11 @@ struct Layout {
   static constexpr int kOpKd = kOpDall + (kFold ? KD * 4 : 0);
   static constexpr int kOpFc = kOpKd + (kFold ? QMAX * KD * 4 : 0);
   static constexpr int kOp = ru(kOpFc + (kFold ? QMAX * KD * 4 : 0), kTC ? 1024 : 128);
-  // prep runs up to two items ahead of the gemv team; on the tensor-core path
-  // an item's slot is also held until its readout, one item later
-  static constexpr int kNumOp = kTC ? (QMAX <= 4 ? 4 : 3) : QMAX <= 4 ? 3 : 2;
+  // prep runs up to three items ahead of the gemv team (windows up to 4:
+  // measured on C2, 4 slots 0.171 ms per call against 0.180 with 3, no gain
+  // from 5 or 6); on the tensor-core path an item's slot is also held until
+  // its readout, one item later
+  static constexpr int kNumOp = kTC ? (QMAX <= 4 ? 4 : 3) : QMAX <= 4 ? 4 : 2;
   // per-warp scratch
   static constexpr int kRedPerWarp = kTC ? 0 : 2 * QMAX * RW;         // floats
   static constexpr int kFoldIdx = 2 * QMAX + QMAX * QMAX;  // fold variant: |k_u|^2 of the pending keys
@@ -381,8 +383,10 @@ __device__ __forceinline__ void pair_codes(const float (&wa)[kConvWidth], const 
   }
 }
 
+// Eight CTAs per SM (registers capped at 40, a few spilled): the pass is
+// latency-bound, and more CTAs in flight measured faster than no spills.
 template <int KD, int QMAX, bool DF>
-__global__ void __launch_bounds__(3 * KD / 2) conv_kernel(const __grid_constant__ VerifyParams p) {
+__global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_constant__ VerifyParams p) {
   // The verify kernel may start now: it waits for this grid before it reads
   // the scratch, and its other work (state streaming) does not depend on it.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -105,8 +105,9 @@ enum {
  * T == 0 or B == 0 is a no-op returning KDA_OK.
  *
  * Two kernels run, in stream order: the conv pass (one CTA per (request,
- * head): the codes y_t, packed with the raw gate rows and the beta gates
- * sigmoid(raw_beta) into `scratch`, and the rolled conv state) and the
+ * head): the codes y_t, packed with the raw gate rows, the beta gates
+ * sigmoid(raw_beta) and the decays e^g into `scratch`, and the rolled conv
+ * state) and the
  * verify proper (persistent, one CTA per SM; it may start while the conv
  * pass drains and waits for it before reading `scratch`).
  * `scratch` is caller-owned device memory of at least
@@ -174,9 +175,9 @@ typedef enum kda_verify_variant {
     KDA_VERIFY_TCGEN05 = 2
 } kda_verify_variant;
 
-/* Bytes of scratch the verify needs: B * H blocks of Q * 8K + 32 bytes (the
+/* Bytes of scratch the verify needs: B * H blocks of Q * 12K + 32 bytes (the
  * conv pass's output per (request, head): [Q][2K] bf16 rows q | v, [Q][2K]
- * rows k | gate, then 8 fp32 beta gates). */
+ * rows k | gate, 8 fp32 beta gates, then [Q][K] fp32 decays e^g). */
 size_t kda_verify_scratch_bytes(int32_t B, int32_t H, int32_t K, int32_t Q);
 
 

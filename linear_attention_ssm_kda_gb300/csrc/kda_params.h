@@ -15,14 +15,21 @@ constexpr int kWsDone = 9;
 constexpr int kWsWords = 16;
 
 // The conv pass's block per (request, head) item in the scratch: [Q][2K] bf16
-// rows q | v, [Q][2K] rows k | raw gate, then 8 fp32 sigmoid(raw beta) (of
-// which the first n are written).  In uint16 elements.
+// rows q | v, [Q][2K] rows k | raw gate, 8 fp32 sigmoid(raw beta), then
+// [Q][K] fp32 decays e^g of the key channels (rows t < n written).  In
+// uint16 elements; scratch_eg_elem is where the decays start.
 constexpr int kScratchBetaBytes = 32;
 #if defined(__CUDACC__)
 __host__ __device__
 #endif
-constexpr long long scratch_item_elems(int Q, int K) {
+constexpr long long scratch_eg_elem(int Q, int K) {
   return 4LL * Q * K + kScratchBetaBytes / 2;
+}
+#if defined(__CUDACC__)
+__host__ __device__
+#endif
+constexpr long long scratch_item_elems(int Q, int K) {
+  return scratch_eg_elem(Q, K) + 2LL * Q * K;
 }
 
 struct VerifyParams {

@@ -8,8 +8,8 @@
 //   conv_kernel    one CTA per (request, head): the conv + SiLU codes of the
 //                  head's q, k and v channels, correctly rounded to bf16, and
 //                  the rolled conv state; the codes go, with the raw gate
-//                  rows and the beta gates, into the item's block of the
-//                  caller's scratch;
+//                  rows, the beta gates and the key channels' decays e^g,
+//                  into the item's block of the caller's scratch;
 //   verify_kernel  the verify proper, below, launched as the conv pass's
 //                  programmatic dependent: its CTAs set up and stream state
 //                  while the conv pass drains, and wait for it before the
@@ -135,9 +135,10 @@ struct Layout {
   static constexpr int kDt = kKG + QMAX * 2 * KD * 2;                  // [KD] dt_bias
   static constexpr int kBeta = kDt + KD * 4;  // [8] fp32 sigmoid(raw beta), from the conv pass's block
   static constexpr int kBetaBytes = kScratchBetaBytes;
+  static constexpr int kEg = kBeta + kBetaBytes;  // [QMAX][KD] fp32 decays e^g, from the conv pass's block
   // fold variant: the pending records of the item, [QMAX][2K] bf16 key/gate
   // and [QMAX][V] fp32 corrections (V == K)
-  static constexpr int kFoldKg = ru(kBeta + kBetaBytes, 128);
+  static constexpr int kFoldKg = ru(kEg + QMAX * KD * 4, 128);
   static constexpr int kFoldC = kFoldKg + (kFold ? QMAX * 2 * KD * 2 : 0);
   static constexpr int kSmall = ru(kFoldC + (kFold ? QMAX * KD * 4 : 0), 128);
   // operand slot (prep -> gemv).  Tensor-core path: first the MMA's B operand,
@@ -319,8 +320,8 @@ __device__ __forceinline__ ItemMeta<QMAX> item_meta(const VerifyParams& p, const
 // taps untouched).  The codes go, with the raw gate rows, into the item's
 // block of the caller's scratch: [Q][2K] bf16 rows q | v, then [Q][2K] rows
 // k | raw gate, rows t < n written, then the window's beta gates
-// sigmoid(raw beta) in fp32.  The k | gate rows are the item's key / gate
-// record verbatim.  Null items, empty windows and items with bad metadata are
+// sigmoid(raw beta) and the key channels' decays e^g, in fp32.  The k | gate
+// rows are the item's key / gate record verbatim.  Null items, empty windows and items with bad metadata are
 // skipped here; the verify kernel reports the latter.
 //
 // A pair's values travel as 32-bit words, channel c in the low half and
@@ -437,6 +438,13 @@ __global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_consta
 #pragma unroll
     for (int t = 0; t < QMAX; ++t) gate[t] = t < n ? load_pair(gr + t * p.gate_stride, g32) : 0u;
   }
+  // the key group: both channels' dt_bias and the head's A = e^A_log, for the decays
+  float2 dtb = make_float2(0.0f, 0.0f);
+  float A = 0.0f;
+  if (g == 1) {
+    dtb = __ldg(reinterpret_cast<const float2*>(p.dt_bias + static_cast<long long>(h) * KD + k));
+    A = expf(p.A_log[h]);
+  }
   // thread t < n of the q group: the gate sigmoid(raw beta) of token t
   const int tb = static_cast<int>(threadIdx.x);
   const uint16_t rbeta = tb < n ? p.raw_beta[static_cast<long long>(im.bos + tb) * p.beta_stride + h] : uint16_t(0);
@@ -450,9 +458,18 @@ __global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_consta
   for (int t = 0; t < QMAX; ++t)
     if (t < n) *reinterpret_cast<uint32_t*>(dst + t * 2 * KD) = y[t];
   if (g == 1) {
+    // the gate record, and the decays e^g of both channels for the verify
+    float* egb = reinterpret_cast<float*>(p.scratch + static_cast<long long>(it) * scratch_item_elems(p.Q, KD) +
+                                          scratch_eg_elem(p.Q, KD)) + k;
 #pragma unroll
-    for (int t = 0; t < QMAX; ++t)
-      if (t < n) *reinterpret_cast<uint32_t*>(dst + t * 2 * KD + KD) = gate[t];
+    for (int t = 0; t < QMAX; ++t) {
+      if (t < n) {
+        *reinterpret_cast<uint32_t*>(dst + t * 2 * KD + KD) = gate[t];
+        const float ea = kda_decay_fast(lo_f32(gate[t]), dtb.x, A, p.lower_bound_gate, p.lower_bound);
+        const float eb = kda_decay_fast(hi_f32(gate[t]), dtb.y, A, p.lower_bound_gate, p.lower_bound);
+        *reinterpret_cast<float2*>(egb + t * KD) = make_float2(ea, eb);
+      }
+    }
   }
   if (tb < n)
     reinterpret_cast<float*>(p.scratch + static_cast<long long>(it) * scratch_item_elems(p.Q, KD) + 4LL * p.Q * KD)[tb] =
@@ -626,15 +643,19 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
           const int h = m.item - (m.item / p.H) * p.H;
           const uint32_t rows = static_cast<uint32_t>(m.n) * 2 * KD * 2;
           const uint32_t fold_bytes = static_cast<uint32_t>(m.fold_m) * (2 * KD * 2 + KD * 4);
-          mbar_arrive_expect_tx(bar, (rows ? 2 * rows + Lay::kBetaBytes : 0u) + KD * 4 + fold_bytes);
+          const uint32_t egs = static_cast<uint32_t>(m.n) * KD * 4;
+          const uint32_t dts = Lay::kFold ? KD * 4 : 0u;
+          mbar_arrive_expect_tx(bar, (rows ? 2 * rows + Lay::kBetaBytes + egs : 0u) + dts + fold_bytes);
           if (fold_bytes) fold_copies<KD, QMAX, VAR>(p, sl, h, m.fold_m, m.fold_r, bar);
           if (rows) {  // (a fold-only item has no window)
             const uint16_t* blk = p.scratch + static_cast<long long>(m.item) * scratch_item_elems(p.Q, KD);
             bulk_g2s(sl + Lay::kQV, blk, rows, bar);
             bulk_g2s(sl + Lay::kKG, blk + 2LL * p.Q * KD, rows, bar);
             bulk_g2s(sl + Lay::kBeta, blk + 4LL * p.Q * KD, Lay::kBetaBytes, bar);
+            bulk_g2s(sl + Lay::kEg, blk + scratch_eg_elem(p.Q, KD), egs, bar);
           }
-          bulk_g2s(sl + Lay::kDt, p.dt_bias + static_cast<long long>(h) * KD, KD * 4, bar);
+          // the fold variant decodes the pending keys' decays with this layer's gate
+          if (Lay::kFold) bulk_g2s(sl + Lay::kDt, p.dt_bias + static_cast<long long>(h) * KD, KD * 4, bar);
         } else {
           mbar_arrive(bar);
         }
@@ -802,17 +823,12 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
     float qv[QMAX], kv[QMAX], eg[QMAX];
     if (live && pt < KD) {
       const int k = pt;
-      const float dtb = reinterpret_cast<const float*>(sl + Lay::kDt)[k];
+      const float* egr = reinterpret_cast<const float*>(sl + Lay::kEg);  // [QMAX][KD] from the conv pass
 #pragma unroll
       for (int t = 0; t < QMAX; ++t) {
-        // every row of the window is read (rows past n hold stale bytes) and
-        // the values of a missing token are discarded by selects, so the
-        // QMAX gates evaluate side by side without branches
         qv[t] = t < n ? bf16_to_f32(qv_rows[t * 2 * KD + k]) : 0.0f;
         kv[t] = t < n ? bf16_to_f32(kg_rows[t * 2 * KD + k]) : 0.0f;
-        const uint16_t rg = kg_rows[t * 2 * KD + KD + k];
-        const float e = kda_decay_fast(bf16_to_f32(rg), dtb, m.A, p.lower_bound_gate, p.lower_bound);
-        eg[t] = t < n ? e : 0.0f;
+        eg[t] = t < n ? egr[t * KD + k] : 0.0f;
       }
       // vals: [t] |q_t|^2, [QMAX + t] |k_t|^2, [2QMAX + t QMAX + u] k_u D_{u+1..t} k_t (u < t),
       //       [2QMAX + u QMAX + t] k_u D_{u+1..t} q_t (u <= t); zero past n (qv = kv = 0 there).
@@ -844,6 +860,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
         static_assert(Lay::kFoldIdx + QMAX <= NREDP, "room for the pending keys' norms");
         const int mf = m.fold_m;
         if (mf > 0) {
+          const float dtb = reinterpret_cast<const float*>(sl + Lay::kDt)[k];
           const uint16_t* fkg = reinterpret_cast<const uint16_t*>(sl + Lay::kFoldKg);
           const float* fc = reinterpret_cast<const float*>(sl + Lay::kFoldC);
           float* dall = reinterpret_cast<float*>(op + Lay::kOpDall);

@@ -100,7 +100,7 @@ def _valid_verify_args():
     a.corr_row_stride = H * Q * K
     a.kg_row_stride = H * Q * 2 * K
     a.scratch = FAKE
-    a.scratch_bytes = 2 * H * (Q * 8 * K + 32)
+    a.scratch_bytes = 2 * H * (Q * 12 * K + 32)
     a.variant = 0
     a.workspace = FAKE
     return a
@@ -136,7 +136,7 @@ def test_verify_rejects_before_launch(lib):
         (dict(conv_state=FAKE + 2), kda.KDA_ERR_MISALIGNED),
         (dict(out=FAKE + 1), kda.KDA_ERR_MISALIGNED),
         (dict(scratch=0), kda.KDA_ERR_INVALID_ARG),
-        (dict(scratch_bytes=2 * 4 * (4 * 8 * 64 + 32) - 16), kda.KDA_ERR_INVALID_ARG),
+        (dict(scratch_bytes=2 * 4 * (4 * 12 * 64 + 32) - 16), kda.KDA_ERR_INVALID_ARG),
         (dict(scratch=FAKE + 8), kda.KDA_ERR_MISALIGNED),
         (dict(variant=3), kda.KDA_ERR_INVALID_ARG),
         (dict(variant=-1), kda.KDA_ERR_INVALID_ARG),
@@ -159,9 +159,9 @@ def test_verify_rejects_before_launch(lib):
 
 
 def test_verify_scratch_bytes(lib):
-    # per (request, head): [Q][2K] bf16 rows q | v and k | gate, then 8 fp32 beta gates
-    assert lib.kda_verify_scratch_bytes(256, 32, 128, 4) == 256 * 32 * (4 * 8 * 128 + 32)
-    assert lib.kda_verify_scratch_bytes(3, 5, 64, 7) == 3 * 5 * (7 * 8 * 64 + 32)
+    # per (request, head): [Q][2K] bf16 rows q | v and k | gate, 8 fp32 beta gates, [Q][K] fp32 decays
+    assert lib.kda_verify_scratch_bytes(256, 32, 128, 4) == 256 * 32 * (4 * 12 * 128 + 32)
+    assert lib.kda_verify_scratch_bytes(3, 5, 64, 7) == 3 * 5 * (7 * 12 * 64 + 32)
     assert lib.kda_verify_scratch_bytes(0, 32, 128, 4) == 0
 
 

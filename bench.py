@@ -325,6 +325,32 @@ def run_deferred(args, prob, dm, stream, dev, world):
     return d_start.elapsed_time(d_end), steps
 
 
+def verify_tail(prob, dm, stream, dev):
+    """The verify kernel's schedule on one layer of the workload, after the
+    timed region: kda_verify_debug's timer hook gives each CTA's start and
+    finish on the GPU's global timer; reported is the kernel's span and the
+    spread between the first and the last CTA to finish."""
+    import linear_attention_ssm_kda_gb300 as kda
+    from workloads.drive import verify_layer
+
+    cfg = prob.cfg
+    items = cfg.B * cfg.H
+    grid = min(items, torch.cuda.get_device_properties(dev).multi_processor_count)
+    times = torch.zeros(2 * items, dtype=torch.int64, device=dev)
+    ws = kda.new_workspace(dev)
+    spans, spreads = [], []
+    for _ in range(5):
+        verify_layer(prob, 0, dm, workspace=ws, stream=stream, debug=(-1, 1_000_000_000, times))
+        torch.cuda.synchronize(dev)
+        t = times[: 2 * grid].view(grid, 2).cpu()
+        spans.append(float(t[:, 1].max() - t[:, 0].min()) / 1e3)
+        spreads.append(float(t[:, 1].max() - t[:, 1].min()) / 1e3)
+    span, spread = statistics.median(spans), statistics.median(spreads)
+    return {"ctas": grid, "kernel_span_us": span, "finish_spread_us": spread,
+            "finish_spread_frac": spread / span if span > 0 else None,
+            "how": "median of 5 launches of one layer with per-CTA global-timer stamps (kda_verify_debug)"}
+
+
 def run_long_window(args, dev):
     """The long-window workload (C3: B=512, H=32, Q=8, one layer) on both
     schedules, one GPU: verify then commit (the tensor-core verify, the
@@ -439,6 +465,7 @@ def run_gpu(args, rank, local, world):
     e2e_ms, e2e_steps, h2d, d2h = None, 0, 0, 0
     if not args.no_e2e:
         e2e_ms, e2e_steps, h2d, d2h = run_e2e(args, prob, ctx, stream, dev, world)
+    tail = verify_tail(prob, dm, stream, dev) if world == 1 else None
     d_ms, d_steps = None, 0
     if not args.no_deferred:
         d_ms, d_steps = run_deferred(args, prob, dm, stream, dev, world)
@@ -515,6 +542,7 @@ def run_gpu(args, rank, local, world):
             "schedule": "each layer's verify first folds the previous step's accepted records into the "
                         "checkpoint (kda_verify_fold), no commit launch"},
         "long_window": long_window,
+        "verify_schedule": tail,
         # each kda_verify is two launches (the conv pass, then the verify kernel)
         "gpu_launches": args.steps * (2 * L + 1),
         "clocks": clk,

@@ -94,7 +94,8 @@ struct SmallMeta {
   int flags, item, bos, n, a;
   int fold_m;  // fold variant: pending records to fold, and their row
   long long s, r, fold_r;
-  float A, pad;
+  float A;
+  int h;  // the item's head
 };
 
 // Prep -> gemv, per item (head of an operand slot).
@@ -543,7 +544,7 @@ __device__ __forceinline__ SmallMeta<QMAX> item_header(const VerifyParams& p, co
   m.r = im.r;
   m.fold_r = im.fold_r;
   m.A = l.it >= 0 ? expf(l.alog) : 0.0f;
-  m.pad = 0.0f;
+  m.h = im.h;
   return m;
 }
 
@@ -640,7 +641,7 @@ __device__ void produce_inputs(const VerifyParams& p, unsigned char* smem, int l
           // the item's rows of the conv pass's block (q | v, then k | gate),
           // its head's dt_bias and, in the fold variant, its pending records:
           // a few bulk copies
-          const int h = m.item - (m.item / p.H) * p.H;
+          const int h = m.h;
           const uint32_t rows = static_cast<uint32_t>(m.n) * 2 * KD * 2;
           const uint32_t fold_bytes = static_cast<uint32_t>(m.fold_m) * (2 * KD * 2 + KD * 4);
           const uint32_t egs = static_cast<uint32_t>(m.n) * KD * 4;
@@ -757,11 +758,55 @@ __device__ __forceinline__ void reduce_scatter_stage(float* acc, int mask, bool 
   }
 }
 
+// Plan of a warp sum of N values per lane: H reduce-scatter stages over lane
+// bits 16, 8, ... (each halves the count and costs 2 x the count in
+// instructions: two selects, a shuffle and an add per pair), then an
+// all-reduce of the C = N / 2^H values left over the 5 - H low lane bits
+// (2 instructions per value and bit).  N is first padded to P (a multiple of
+// 2^H); the cheapest (P, H) is taken.  Afterwards lane l holds the totals of
+// values [C (l >> (5 - H)), + C).
+template <int N>
+struct WarpSumPlan {
+  static constexpr int cost(int p, int h) {
+    int c = 0, w = p;
+    for (int i = 0; i < h; ++i) { c += 2 * w; w /= 2; }
+    return c + 2 * w * (5 - h);
+  }
+  static constexpr int best_h() {
+    int bh = 5, bc = cost(ru(N, 32), 5);
+    for (int h = 0; h <= 5; ++h) {
+      const int c = cost(ru(N, 1 << h), h);
+      if (c < bc) { bc = c; bh = h; }
+    }
+    return bh;
+  }
+  static constexpr int H = best_h();
+  static constexpr int P = ru(N, 1 << H);
+  static constexpr int C = P >> H;
+};
+
+template <int P, int H, int C>
+__device__ __forceinline__ void warp_sum_values(float* vals, int lane) {
+  if constexpr (H > 0) reduce_scatter_stage<P>(vals, 16, (lane & 16) != 0);
+  if constexpr (H > 1) reduce_scatter_stage<P / 2>(vals, 8, (lane & 8) != 0);
+  if constexpr (H > 2) reduce_scatter_stage<P / 4>(vals, 4, (lane & 4) != 0);
+  if constexpr (H > 3) reduce_scatter_stage<P / 8>(vals, 2, (lane & 2) != 0);
+  if constexpr (H > 4) reduce_scatter_stage<P / 16>(vals, 1, (lane & 1) != 0);
+#pragma unroll
+  for (int b = 0; b < 5 - H; ++b) {
+#pragma unroll
+    for (int i = 0; i < C; ++i) vals[i] += __shfl_xor_sync(0xffffffffu, vals[i], 1 << b);
+  }
+}
+
 template <int KD, int QMAX, int VAR>
 __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatile int* misc) {
   using Lay = Layout<KD, QMAX, VAR>;
-  constexpr int NREDP = Lay::kPart;  // |q_t|^2, |k_t|^2, raw M / N grid, padded to 32
-  constexpr int PER = NREDP / 32;
+  constexpr int NREDP = Lay::kPart;  // |q_t|^2, |k_t|^2, raw M / N grid (and the fold's norms), padded to 32
+  // the warp sum over the key channels: only the values in use, by the
+  // cheapest mix of reduce-scatter and all-reduce stages
+  using Plan = WarpSumPlan<Lay::kFoldIdx + (Lay::kFold ? QMAX : 0)>;
+  static_assert(Plan::P <= NREDP, "the summed values fit the per-warp parts");
   Bars<KD, QMAX, VAR> bars(smem);
   volatile int* abort_flag = misc + kMiscAbort;
   float* part = reinterpret_cast<float*>(smem + Lay::oPart);
@@ -783,7 +828,7 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
       }
       break;
     }
-    const int h = m.item - (m.item / p.H) * p.H;
+    const int h = m.h;
     const bool live = ok && (m.flags & kLive);
     const int n = m.n;
     // the window's beta gates, for the operand header (read before the slot
@@ -885,13 +930,11 @@ __device__ void prep(const VerifyParams& p, unsigned char* smem, int pt, volatil
           dall[k] = suffix;
         }
       }
-      reduce_scatter_stage<NREDP>(vals, 16, (lane & 16) != 0);
-      reduce_scatter_stage<NREDP / 2>(vals, 8, (lane & 8) != 0);
-      reduce_scatter_stage<NREDP / 4>(vals, 4, (lane & 4) != 0);
-      reduce_scatter_stage<NREDP / 8>(vals, 2, (lane & 2) != 0);
-      reduce_scatter_stage<NREDP / 16>(vals, 1, (lane & 1) != 0);
+      warp_sum_values<Plan::P, Plan::H, Plan::C>(vals, lane);
+      if ((lane & ((1 << (5 - Plan::H)) - 1)) == 0) {
 #pragma unroll
-      for (int v = 0; v < PER; ++v) part[warp * NREDP + lane * PER + v] = vals[v];
+        for (int v = 0; v < Plan::C; ++v) part[warp * NREDP + (lane >> (5 - Plan::H)) * Plan::C + v] = vals[v];
+      }
     }
     named_barrier(kBarPrep, kPrepConvThreads);
     if (misc[kMiscPrepFail]) break;  // every prep thread sees the same flag here

@@ -329,7 +329,7 @@ constexpr float kTier1MinY = -80.0f;
 // The fma chain starts from +0, so an exactly zero sum is +0 (SiLU(0) = +0).
 // Its error dy is at most u (|y_2| + |y_3| + |y_4|) over the partial sums y_k,
 // u = 2^-24, plus u |y_1| for fp32 weights (a bf16 weight times a bf16 input
-// is exact; e0 is 1 for fp32 weights and 0 for bf16), so
+// is exact; e0 is 1 for fp32 weights (kW32) and 0 for bf16), so
 // dy^2 <= 4 u^2 (e0 y_1^2 + y_2^2 + y_3^2 + y_4^2).  The conv error moves s by
 // at most slope dy, where |SiLU'| <= 1.1 everywhere and |SiLU'(t)| =
 // |sigma(t) + SiLU(t)(1 - sigma(t))| <= sigma + |SiLU|, which over
@@ -341,8 +341,9 @@ constexpr float kTier1MinY = -80.0f;
 // below 2^-20 s^2 (the next midpoint is at least 2^-10 |s| away).  The
 // constants carry slack for the bound's own rounding; the 2^-126 term makes
 // every |s| below 2^-63 doubtful, where the squares leave the normal range.
+template <bool kW32>
 __device__ __forceinline__ uint32_t conv_silu_bf16x2(const float wa[4], const float wb[4], const float xa[4],
-                                                     const float xb[4], float e0, uint32_t* doubt) {
+                                                     const float xb[4], uint32_t* doubt) {
   constexpr float k4U2 = 0x1.0001p-46f;                            // 4 u^2
   constexpr float k2Eps2 = 2.0f * 36.0f * 0x1p-48f * 1.0001f;       // 2 kSiluRelErr^2
   const float2 y1 = __ffma2_rn(make_float2(wa[0], wb[0]), make_float2(xa[0], xb[0]), f2(0.0f));
@@ -352,8 +353,11 @@ __device__ __forceinline__ uint32_t conv_silu_bf16x2(const float wa[4], const fl
   float2 sigma;
   const float2 s = silu_f32x2(y, sigma);
   // dy^2 bound
-  float2 q = __fmul2_rn(__fmul2_rn(f2(e0), y1), y1);
-  q = __ffma2_rn(y2, y2, q);
+  float2 q;
+  if constexpr (kW32)
+    q = __ffma2_rn(y2, y2, __fmul2_rn(y1, y1));
+  else
+    q = __fmul2_rn(y2, y2);
   q = __ffma2_rn(y3, y3, q);
   q = __ffma2_rn(y, y, q);
   const float2 dy2 = __fmul2_rn(f2(k4U2), q);

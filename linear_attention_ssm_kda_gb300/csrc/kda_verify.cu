@@ -351,10 +351,9 @@ __device__ __forceinline__ void store_pair(uint16_t* ptr, uint32_t v, bool w32) 
 
 // The codes of one channel pair: sq[j] holds both channels' sequence value j
 // (the W - 1 taps, then the window); y[t] the two codes of token t.
-template <int QMAX>
+template <int QMAX, bool W32>
 __device__ __forceinline__ void pair_codes(const float (&wa)[kConvWidth], const float (&wb)[kConvWidth],
-                                           const uint32_t (&sq)[kConvWidth - 1 + QMAX], int n, float e0,
-                                           uint32_t (&y)[QMAX]) {
+                                           const uint32_t (&sq)[kConvWidth - 1 + QMAX], int n, uint32_t (&y)[QMAX]) {
   uint32_t doubt = 0;
 #pragma unroll
   for (int t = 0; t < QMAX; ++t) {
@@ -363,7 +362,7 @@ __device__ __forceinline__ void pair_codes(const float (&wa)[kConvWidth], const 
       const float xa[kConvWidth] = {lo_f32(sq[t]), lo_f32(sq[t + 1]), lo_f32(sq[t + 2]), lo_f32(sq[t + 3])};
       const float xb[kConvWidth] = {hi_f32(sq[t]), hi_f32(sq[t + 1]), hi_f32(sq[t + 2]), hi_f32(sq[t + 3])};
       uint32_t d;
-      y[t] = conv_silu_bf16x2(wa, wb, xa, xb, e0, &d);
+      y[t] = conv_silu_bf16x2<W32>(wa, wb, xa, xb, &d);
       doubt |= d << (2 * t);
     }
   }
@@ -387,7 +386,8 @@ __device__ __forceinline__ void pair_codes(const float (&wa)[kConvWidth], const 
 
 // Eight CTAs per SM (registers capped at 40, a few spilled): the pass is
 // latency-bound, and more CTAs in flight measured faster than no spills.
-template <int KD, int QMAX, bool DF>
+// DF: dim-first conv state; W32: fp32 conv weights (else bf16).
+template <int KD, int QMAX, bool DF, bool W32>
 __global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_constant__ VerifyParams p) {
   // The verify kernel may start now: it waits for this grid before it reads
   // the scratch, and its other work (state streaming) does not depend on it.
@@ -401,8 +401,20 @@ __global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_consta
   const int h = it - (it / p.H) * p.H;
   const long long HK = static_cast<long long>(p.H) * KD;
   const long long c = g * HK + static_cast<long long>(h) * KD + k;  // the pair's first channel (even)
+  // the item's metadata, decoded once by the first warp and shared
+  __shared__ int s_meta[6];
+  if (threadIdx.x < 32) {
+    const ItemMeta<QMAX> m0 = item_meta<QMAX>(p, load_item(p, it), false);
+    if (threadIdx.x == 0) {
+      s_meta[0] = (m0.flags & kLive) ? m0.n : 0;
+      s_meta[1] = m0.a;
+      s_meta[2] = m0.bos;
+      s_meta[3] = static_cast<int>(m0.s);
+      s_meta[4] = static_cast<int>(m0.s >> 32);
+    }
+  }
   float wa[kConvWidth], wb[kConvWidth];
-  if (p.conv_weight_fp32) {
+  if (W32) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(p.conv_weight) + c);
     const float4 b = __ldg(reinterpret_cast<const float4*>(p.conv_weight) + c + 1);
     wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
@@ -412,9 +424,16 @@ __global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_consta
     wa[0] = lo_f32(wv.x); wa[1] = hi_f32(wv.x); wa[2] = lo_f32(wv.y); wa[3] = hi_f32(wv.y);
     wb[0] = lo_f32(wv.z); wb[1] = hi_f32(wv.z); wb[2] = lo_f32(wv.w); wb[3] = hi_f32(wv.w);
   }
-  const ItemMeta<QMAX> im = item_meta<QMAX>(p, load_item(p, it), false);
-  if (!(im.flags & kLive) || im.n <= 0) return;
-  const int n = im.n;
+  __syncthreads();
+  const int n = s_meta[0];  // 0: nothing to convolve (a null, empty or bad item)
+  if (n <= 0) return;
+  struct {
+    int a, bos;
+    long long s;
+  } im;
+  im.a = s_meta[1];
+  im.bos = s_meta[2];
+  im.s = static_cast<long long>(static_cast<uint32_t>(s_meta[3])) | (static_cast<long long>(s_meta[4]) << 32);
   const int Lc = p.Q + kConvWidth - 2;
   const bool x32 = (p.qkv_stride & 1) == 0 && (reinterpret_cast<uintptr_t>(p.mixed_qkv) & 3u) == 0;
   const bool g32 = (p.gate_stride & 1) == 0 && (reinterpret_cast<uintptr_t>(p.raw_gate) & 3u) == 0;
@@ -451,7 +470,7 @@ __global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_consta
   const uint16_t rbeta = tb < n ? p.raw_beta[static_cast<long long>(im.bos + tb) * p.beta_stride + h] : uint16_t(0);
   // the codes: a bf16 weight times a bf16 input is exact in fp32; an fp32 weight's product rounds
   uint32_t y[QMAX];
-  pair_codes<QMAX>(wa, wb, sq, n, p.conv_weight_fp32 ? 1.0f : 0.0f, y);
+  pair_codes<QMAX, W32>(wa, wb, sq, n, y);
   // the item's block: q at [t][k], v at [t][K + k], k at [Q + t][k], gate at [Q + t][K + k]
   uint16_t* blk = p.scratch + static_cast<long long>(it) * scratch_item_elems(p.Q, KD) + k;
   uint16_t* dst = g == 0 ? blk : g == 2 ? blk + KD : blk + 2LL * p.Q * KD;
@@ -1803,7 +1822,10 @@ cudaError_t launch(const VerifyParams& p, bool after_conv, cudaStream_t stream) 
 
 template <int KD, int QMAX, bool DF>
 cudaError_t launch_conv(const VerifyParams& p, cudaStream_t stream) {
-  conv_kernel<KD, QMAX, DF><<<p.B * p.H, 3 * KD / 2, 0, stream>>>(p);
+  if (p.conv_weight_fp32)
+    conv_kernel<KD, QMAX, DF, true><<<p.B * p.H, 3 * KD / 2, 0, stream>>>(p);
+  else
+    conv_kernel<KD, QMAX, DF, false><<<p.B * p.H, 3 * KD / 2, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -61,6 +61,10 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
   const int b = rem / p.H;
   const int h = rem - b * p.H;
 
+  // the layer's tables, loaded with the request's metadata (one round trip)
+  const long long state_base = p.state_base[l], state_stride = p.state_stride[l];
+  const long long corr_base = p.corr_base[l], corr_stride = p.corr_stride[l];
+  const long long kg_base = p.kg_base[l], kg_stride = p.kg_stride[l];
   // ---- plan: skip null slots and empty commits ----
   const long long s = p.state_indices[b];
   if (s <= p.null_block_id) return;
@@ -89,9 +93,6 @@ __global__ void __launch_bounds__(kThreads, 3) commit_kernel(const CommitParams 
     }
     rb = p.boundary_recovery_lens ? min(max(p.boundary_recovery_lens[b], 0), m) : 0;
   }
-  const long long state_base = p.state_base[l], state_stride = p.state_stride[l];
-  const long long corr_base = p.corr_base[l], corr_stride = p.corr_stride[l];
-  const long long kg_base = p.kg_base[l], kg_stride = p.kg_stride[l];
   if (!aligned16(state_base) || !aligned16(state_stride * 4) || !aligned16(corr_base) ||
       !aligned16(corr_stride * 4) || !aligned16(kg_base) || !aligned16(kg_stride * 2)) {
     if (tid == 0) report(p.workspace, KDA_DEVERR_MISALIGNED, item);

@@ -384,11 +384,12 @@ __device__ __forceinline__ void pair_codes(const float (&wa)[kConvWidth], const 
   }
 }
 
-// Eight CTAs per SM (registers capped at 40, a few spilled): the pass is
-// latency-bound, and more CTAs in flight measured faster than no spills.
+// Seven CTAs per SM (registers capped at 48, a few spilled): the pass is
+// latency-bound, and more CTAs in flight measured faster than five without
+// spills (eight, at 40 registers, spilled more and measured slower).
 // DF: dim-first conv state; W32: fp32 conv weights (else bf16).
 template <int KD, int QMAX, bool DF, bool W32>
-__global__ void __launch_bounds__(3 * KD / 2, 8) conv_kernel(const __grid_constant__ VerifyParams p) {
+__global__ void __launch_bounds__(3 * KD / 2, 7) conv_kernel(const __grid_constant__ VerifyParams p) {
   // The verify kernel may start now: it waits for this grid before it reads
   // the scratch, and its other work (state streaming) does not depend on it.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -384,9 +384,9 @@ __device__ __forceinline__ void pair_codes(const float (&wa)[kConvWidth], const 
   }
 }
 
-// Seven CTAs per SM (registers capped at 48, a few spilled): the pass is
-// latency-bound, and more CTAs in flight measured faster than five without
-// spills (eight, at 40 registers, spilled more and measured slower).
+// Seven CTAs per SM (42 warps, eleven on some scheduler: 40 registers, a few
+// spilled): the pass is latency-bound, and more CTAs in flight measured
+// faster than five without spills (eight also get 40 and measured slower).
 // DF: dim-first conv state; W32: fp32 conv weights (else bf16).
 template <int KD, int QMAX, bool DF, bool W32>
 __global__ void __launch_bounds__(3 * KD / 2, 7) conv_kernel(const __grid_constant__ VerifyParams p) {

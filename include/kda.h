@@ -343,8 +343,8 @@ kda_status kda_commit(const kda_commit_args *args, kda_stream_t stream);
  * the stream.
  *   - L > KDA_NOALLOC_MAX_LAYERS: KDA_ERR_UNSUPPORTED, nothing enqueued.
  *   - The first call on a device does the set-up: it resolves the scratch's
- *     device address (cudaGetSymbolAddress), which may load the module.  Make
- *     that first call before any stream capture.
+ *     device address (cudaGetSymbolAddress), which may load the module.
+ *     Recording this call in a CUDA graph is not tested.
  *   - Nothing in the scratch has to start at zero: each call writes every
  *     table entry its kernel reads, before the kernel, in stream order.  The
  *     optional workspace is the caller's and is used as for kda_commit.

@@ -54,20 +54,22 @@ def _check_step(prob, l, hl, res, what):
     assert_f32_close(prob.corr[l].cpu().numpy(), res["corr_exact"], corr_m, what=f"{what} corr")
 
 
-@pytest.mark.parametrize("name", ["C4", "C0", "C3"])
+@pytest.mark.parametrize("name", ["C4", "C0", "C3", "C0-Q6"])
 def test_fold_chain_matches_commit_then_verify(name):
     """Three decode steps.  Step 0 is a plain verify; steps 1 and 2 fold the
     previous step's accepted tokens and verify in one launch per layer.  Step
     2 empties three windows, so those requests are folded only.  C4 brings
     null slots and activation rows at 8-byte offsets; C0 the K = 64 build;
-    C3 windows of 8 tokens with the lower-bound gate and outliers."""
-    cfg = CONFIGS[name]
+    C3 windows of 8 tokens with the lower-bound gate and outliers; C0-Q6 a
+    window of 6 on the window-of-8 build."""
     if name == "C4":
-        prob = make_problem(cfg, DEV, B=96, L=2, slots=256)
+        prob = make_problem(CONFIGS[name], DEV, B=96, L=2, slots=256)
     elif name == "C3":
-        prob = make_problem(cfg, DEV, B=48, L=2, slots=128)
+        prob = make_problem(CONFIGS[name], DEV, B=48, L=2, slots=128)
+    elif name == "C0-Q6":
+        prob = make_problem(CONFIGS["C0"].replace(Q=6), DEV)
     else:
-        prob = make_problem(cfg, DEV)
+        prob = make_problem(CONFIGS[name], DEV)
     cfg = prob.cfg
     rng = np.random.default_rng(2024)
     hls = [host_layer(prob, l) for l in range(cfg.L)]

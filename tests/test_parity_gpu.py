@@ -176,7 +176,11 @@ C0_VARIANTS = {
     "record_rows": dict(record_by_request=True),
     "null_slot": dict(null_count=1),
     "window3": dict(Q=3),
+    "window2": dict(Q=2),
     "window1": dict(Q=1),
+    # windows of 5 to 7 run the window-of-8 build with the scratch laid out
+    # for their own Q (the inputs warp then copies the block in parts)
+    "window6": dict(Q=6),
 }
 
 

@@ -47,6 +47,16 @@ def test_c3_cuda_core_path_when_forced():
     run_and_check(prob, variant="cuda_core")
 
 
+@pytest.mark.parametrize("window", [2, 5, 7])
+@pytest.mark.parametrize("variant", ["tcgen05", "cuda_core"])
+def test_windows_below_the_build_maximum(window, variant):
+    """Windows of 2 and of 5 to 7 run the builds for 4 and 8 with a smaller
+    Q: the MMA's B operand is zero past 2n, and the scratch is laid out for
+    the call's own Q."""
+    prob = make_problem(CONFIGS["C3"].replace(Q=window), DEV, B=32, slots=96)
+    run_and_check(prob, variant=variant)
+
+
 def test_c4_null_slots_and_misaligned_rows_reduced():
     prob = make_problem(CONFIGS["C4"], DEV, B=96, L=2, slots=256)
     assert (prob.meta.state_indices <= 0).sum() > 0

@@ -505,6 +505,10 @@ def run_gpu(args, rank, local, world):
                                                     layers=args.layers)  # bounded: ~10-20 s
         cpu = {"value": cv, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample,
                "s_per_full_step": cstep}
+        # the same oracle on one thread, one layer of the step (about a second)
+        _, one_layer, _, _, _ = time_oracle(args.config, steps=1, warmup=0, threads=1, layers=1)
+        cpu["one_thread"] = {"s_per_layer": one_layer, "s_per_layer_all_cores": cstep / cfg.L,
+                             "sample": f"{args.config}: the request batch, verify + commit of one layer, 1 step"}
     line = {
         "metric": METRIC,
         "value": value,

@@ -170,7 +170,7 @@ struct Layout {
   static constexpr int kFoldIdx = 2 * QMAX + QMAX * QMAX;  // fold variant: |k_u|^2 of the pending keys
   static constexpr int kPart = ru(kFoldIdx + (kFold ? QMAX : 0), 32);         // reduced values per prep warp
   static constexpr int kFixed = kNumSmall * kSmall + kNumOp * kOp + kGemvWarps * kRedPerWarp * 4 +
-                                kPrepWarps * kPart * 4 + 32 + 64 + kTick * kTickBytes +
+                                kPrepWarps * kPart * 4 + 32 + 64 + 64 + kTick * kTickBytes +
                                 (2 * kNumSmall + 2 * kNumOp + 4 + 2 * kTick) * 8 + (kTC ? 1024 : 0);
   static constexpr int kBarsPerChunk = kTC ? 4 : 2;
   static constexpr int kChunkFit = (kSmemLimit - kFixed - 64 * kBarsPerChunk * 8) / kChunk;
@@ -183,7 +183,8 @@ struct Layout {
   static constexpr int oPart = oRed + kGemvWarps * kRedPerWarp * 4;
   static constexpr int oMisc = oPart + kPrepWarps * kPart * 4;  // int[8]
   static constexpr int oArm = oMisc + 32;                      // uint8[64]: last armed phase per chunk slot
-  static constexpr int oTick = ru(oArm + 64, 16);               // SmallMeta[kTick]: the ticket ring
+  static constexpr int oLap = oArm + 64;                        // uint8[64]: lap last armed per chunk slot
+  static constexpr int oTick = ru(oLap + 64, 16);               // SmallMeta[kTick]: the ticket ring
   static constexpr int oBars = ru(oTick + kTick * kTickBytes, 8);
   static constexpr int kNumBars = kBarsPerChunk * kNumChunk + 2 * kNumSmall + 2 * kNumOp + 4 + 2 * kTick;
   static constexpr int kBytes = oBars + kNumBars * 8;
@@ -233,6 +234,34 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
                                           uint64_t limit_ns) {
   bool ok = true;
   if (lane == 0) ok = mbar_wait_or_abort(bar, parity, abort_flag, limit_ns);
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok && lane != 0) mbar_acquire_seen(bar, parity);
+  return ok;
+}
+
+// warp_wait for a chunk of the state ring, seen by a gemv warp.  A gemv
+// warp takes every eighth chunk and may run up to three items (24 chunks)
+// ahead of another, so it can come to a chunk slot one lap ahead of a copy
+// still in flight there; the parity alone would then match the slot's
+// previous, completed phase.  The state warp records in `lap` the lap it
+// arms in each slot, only once the slot's previous lap has been consumed:
+// lane 0 first waits (bounded, with a short sleep per poll) for the slot to
+// show this warp's lap, after which the parity names a single phase.
+__device__ __forceinline__ bool warp_wait_chunk(uint64_t* bar, const unsigned char* lap_base, int pos, uint32_t lap_no,
+                                                int lane, const volatile int* abort_flag, uint64_t limit_ns) {
+  const uint32_t parity = lap_no & 1;
+  bool ok = true;
+  if (lane == 0) {
+    const volatile uint8_t* lap = reinterpret_cast<const volatile uint8_t*>(lap_base);
+    const uint8_t want = static_cast<uint8_t>(lap_no);
+    // (an iteration bound: each poll sleeps at most about 128 ns, so the
+    // bound is a couple of seconds at most)
+    for (uint32_t it = 0; ok && lap[pos] != want; ++it) {
+      if (*abort_flag || it >= (1u << 24)) ok = false;
+      else __nanosleep(64);
+    }
+    if (ok) ok = mbar_wait_or_abort(bar, parity, abort_flag, limit_ns);
+  }
   ok = __all_sync(0xffffffffu, ok);
   if (ok && lane != 0) mbar_acquire_seen(bar, parity);
   return ok;
@@ -725,6 +754,7 @@ __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int la
   // per chunk slot, the last armed phase: 0 never, 1 + its parity (shared
   // memory, written by the arming lane; waited for at exit)
   volatile uint8_t* arm = reinterpret_cast<volatile uint8_t*>(smem + Lay::oArm);
+  volatile uint8_t* lap = reinterpret_cast<volatile uint8_t*>(smem + Lay::oLap);
   if (lane < Lay::kNumChunk) arm[lane] = 0;
   if (lane + 32 < Lay::kNumChunk) arm[lane + 32] = 0;
   __syncwarp();
@@ -742,6 +772,7 @@ __device__ void produce_state(const VerifyParams& p, unsigned char* smem, int la
       ok = mbar_wait_or_abort(&bars.ch_empty[pos], ((cc / Lay::kNumChunk) & 1) ^ 1, abort_flag, p.wait_limit_ns);
       if (ok) {
         arm[pos] = static_cast<uint8_t>(1 + ((cc / Lay::kNumChunk) & 1));
+        lap[pos] = static_cast<uint8_t>(cc / Lay::kNumChunk);  // before the phase is armed
         const float* src = p.state + js * p.state_slot_stride + static_cast<long long>(jh) * KD * KD;
         mbar_arrive_expect_tx(&bars.ch_full[pos], Lay::kChunk);
         bulk_g2s(smem + Lay::oChunks + pos * Lay::kChunk, src + lane * Lay::RW * KD, Lay::kChunk,
@@ -1246,7 +1277,8 @@ __device__ void gemv_team(const VerifyParams& p, unsigned char* smem, int gw, in
       const int n = m.n;
       const uint32_t pc = live * kGemvWarps + gw;
       const int pos = pc % Lay::kNumChunk;
-      ok = warp_wait(&bars.ch_full[pos], (pc / Lay::kNumChunk) & 1, lane, abort_flag, p.wait_limit_ns);
+      ok = warp_wait_chunk(&bars.ch_full[pos], smem + Lay::oLap, pos, pc / Lay::kNumChunk, lane, abort_flag,
+                           p.wait_limit_ns);
       if (!ok) break;
       float* st = reinterpret_cast<float*>(smem + Lay::oChunks + pos * Lay::kChunk);
       const float* vec = reinterpret_cast<const float*>(op + Lay::kOpVec);
@@ -1680,6 +1712,7 @@ __global__ void __launch_bounds__(Layout<KD, QMAX, VAR>::kThreads, 1) verify_ker
     }
     for (int i = 0; i < 8; ++i)
       if (i != kMiscTaddr) misc[i] = 0;  // the tensor-memory base is written by the allocating warp
+    for (int i = 0; i < 64; ++i) (smem + Lay::oLap)[i] = 0xff;  // no lap armed yet
     fence_barrier_init();
   }
   if constexpr (Lay::kTC) {

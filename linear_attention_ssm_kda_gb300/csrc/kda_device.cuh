@@ -259,12 +259,13 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 //      correctly rounded code.  Otherwise the code is marked doubtful (about
 //      6 in 10^4 codes on the decode workloads' data, 2 in 10^3 with
 //      outliers).
-//   2. float-float (conv_code_exact): y exactly as a pair of floats, e^-|y| by
-//      a 32-entry table and a short series, SiLU by a pair-of-floats quotient,
-//      relative error far below 2^-36; decides every code not within 2^-36 of
-//      a boundary.
-//   3. double: the definition evaluated in fp64 (exact products, the sum in
-//      tap order, y / (1 + e^-y)) and rounded once, for what tier 2 leaves.
+//   2. float-float (conv_code_ff): y exactly as a pair of floats, e^-|y| by a
+//      32-entry table and a short series, SiLU by a pair-of-floats quotient,
+//      relative error far below 2^-36; for |y| <= 87 it decides every code
+//      not within 2^-36 of a boundary.
+//   3. double (conv_code_f64): the definition evaluated in fp64 (exact
+//      products, the sum in tap order, y / (1 + e^-y)) and rounded once, for
+//      what tier 2 leaves.  conv_code_exact runs tiers 2 and 3.
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 

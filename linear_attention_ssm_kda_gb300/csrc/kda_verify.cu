@@ -32,15 +32,18 @@
 //   inputs (1 warp)  draws the tickets, decodes each item's request metadata
 //                    a few items ahead (a ring of headers, which the state
 //                    warp follows) and copies each item's rows of the conv
-//                    pass's block (q | v, then k | gate) and its head's
-//                    dt_bias into a ring of small slots (bulk copies);
+//                    pass's block (q | v, k | gate, the beta gates and the
+//                    decays; the fold variant adds the head's dt_bias and
+//                    the pending records) into a ring of small slots (bulk
+//                    copies);
 //   state (1 warp)   streams each live item's 64 KB fp32 state as eight row
 //                    chunks into a ring of chunk slots, running ahead of the
-//                    arithmetic by two to three items;
-//   prep (6 warps)   one key channel per thread: the key / gate record (one
-//                    bulk store of the block's k | gate rows), the gates,
-//                    the norms and the closed-form operands X_t, Y_t, M, N,
-//                    handed on through a ring of operand slots;
+//                    arithmetic by two to three items, and records the lap it
+//                    arms in each slot;
+//   prep (4 warps)   one key channel per thread: the key / gate record (one
+//                    bulk store of the block's k | gate rows), the norms and
+//                    the closed-form operands X_t, Y_t, M, N, handed on
+//                    through a ring of operand slots;
 //   gemv (8 warps)   each on its own row chunk of the state: P | R with
 //                    packed fp32x2 FMAs, then the corrections and outputs of
 //                    its rows.
